@@ -1,0 +1,110 @@
+// Internal launch interface between the C-ABI layer (mla_api.cu) and the kernels.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/mla.h"
+#include "common.cuh"
+
+namespace mla {
+
+// One decode "group" is one (request, query token) pair: 128 heads attending over the
+// request's keys 0..p_t. A work item is a contiguous page range of one group.
+struct WorkItem {
+  int group;
+  int page_begin;   // group-relative page index
+  int page_end;
+  int single;       // 1: the item covers the whole group -> write the final output
+};
+
+// Byte offsets of every region of the decode workspace (all 256-byte aligned).
+struct DecodeWorkspace {
+  size_t status;        // int32 status word (+ padding)
+  size_t worker_off;    // int32 [G + 1]
+  size_t items;         // WorkItem [G + groups]
+  size_t group_first;   // int32 [groups]
+  size_t group_last;    // int32 [groups]
+  size_t group_kv;      // int32 [groups]
+  size_t q_lat;         // act dtype [groups][H][D]
+  size_t part_o;        // fp32 [G + groups][H][d_c]
+  size_t part_lse;      // fp32 [G + groups][H]
+  size_t total;
+  int workers;          // G
+  int groups;           // batch * q_len
+  int max_items;        // G + groups
+};
+
+struct PlanParams {
+  const int32_t* seq_lens;
+  int batch, q_len, page_size, max_pages, workers;
+  int* worker_off;
+  WorkItem* items;
+  int* group_first;
+  int* group_last;
+  int* group_kv;
+  int32_t* status;
+};
+
+struct DecodeParams {
+  const void* q_lat;          // [groups][H][D]
+  const void* cache;          // [num_pages][P][D]
+  const int32_t* block_table;
+  int max_pages, num_pages;
+  int batch, q_len;
+  int H, d_c, d_r, D, P;
+  float scale_log2;           // softmax_scale * log2(e) (* cache_scale for fp8)
+  float out_scale;            // cache_scale for an fp8 cache, else 1
+  void* out_latent;           // [groups][H][d_c] act dtype
+  float* lse;                 // [groups][H]
+  const int* worker_off;
+  const WorkItem* items;
+  const int* group_first;
+  const int* group_last;
+  const int* group_kv;
+  float* part_o;
+  float* part_lse;
+  int32_t* status;
+  int workers;
+};
+
+// Counts kernels launched through the library (read by mla_kernel_launches).
+void note_launch(int n = 1);
+
+// ---- launchers (return cudaGetLastError() of the launch) --------------------------------
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t s);
+
+cudaError_t launch_query_prologue(mla_dtype act, const void* q_nope, const void* q_pe,
+                                  const void* W_UK_abs, const int32_t* seq_lens, int batch,
+                                  int q_len, int H, int d_n, int d_c, int d_r,
+                                  const RopeTable& rt, void* q_lat, cudaStream_t s);
+
+cudaError_t launch_decode_simt(mla_dtype act, mla_dtype cache, const DecodeParams& p,
+                               cudaStream_t s);
+
+cudaError_t launch_combine(mla_dtype act, const DecodeParams& p, int groups, cudaStream_t s);
+
+cudaError_t launch_append_latent(mla_dtype act, mla_dtype cache, const void* c_kv,
+                                 const void* k_pe, int T, const int32_t* req_ids,
+                                 const int32_t* positions, const int32_t* block_table, int batch,
+                                 int max_pages, void* cache_ptr, int num_pages, int P, int d_c,
+                                 int d_r, int rotate, const RopeTable& rt, float cache_scale,
+                                 int32_t* status, cudaStream_t s);
+
+cudaError_t launch_append_from_h(mla_dtype act, mla_dtype cache, const void* h, const void* W,
+                                 int T, int d, const int32_t* req_ids, const int32_t* positions,
+                                 const int32_t* block_table, int batch, int max_pages,
+                                 void* cache_ptr, int num_pages, int P, int d_c, int d_r,
+                                 const RopeTable& rt, float cache_scale, int32_t* status,
+                                 cudaStream_t s);
+
+cudaError_t launch_absorb(mla_dtype act, const void* W_UK, const void* W_UV, const void* W_O,
+                          void* W_UK_abs, void* W_comb, int H, int d_c, int d_n, int d_v, int d,
+                          cudaStream_t s);
+
+// out = o_lat . W_comb; `acc` is an fp32 [rows][N] accumulator in the caller's workspace.
+cudaError_t launch_output_proj_simt_ws(mla_dtype act, const void* o_lat, const void* W_comb,
+                                       int rows, int K, int N, void* out, float* acc,
+                                       cudaStream_t s);
+
+}  // namespace mla

@@ -1,0 +1,744 @@
+// SIMT kernels of libmla: cache append (from latents or from hidden states), the tiled
+// fp32-accumulating GEMM used by the weight fold, the query prologue and the output
+// projection, the split planner, the SIMT decode kernel and the LSE combine.
+//
+// Page notation: huny.dev "DeepSeek MLA 해부" §2-1 (c_t = h_t W^DKV), §2-3 (k^R =
+// RoPE(h_t W^KR), scores = content + rotary), §3-1 (absorbed query), §3-2 (W^UV W^O
+// fold); secrett2633.cloud "[vLLM] Multi-head Latent Attention" (64-token pages, MQA
+// decode over one combined kv_c_and_k_pe_cache, LSE return, split count num_splits).
+#include <math.h>
+#include <stdio.h>
+
+#include "internal.h"
+
+namespace mla {
+
+// ======================================================================== tiled SIMT GEMM
+// C[z] (M x N) = A[z] (M x K, row-major, lda) * B[z] (K x N, row-major, ldb), fp32
+// accumulation; the epilogue receives 4 consecutive columns of one row.
+constexpr int GT_M = 64, GT_N = 64, GT_K = 16;
+
+template <typename TA, typename TB, class Epi>
+__global__ void __launch_bounds__(256) simt_gemm_kernel(const TA* __restrict__ A, long long lda,
+                                                        long long sA, const TB* __restrict__ B,
+                                                        long long ldb, long long sB, int M, int N,
+                                                        int K, int k_chunk, Epi epi) {
+  __shared__ float As[GT_K][GT_M + 4];
+  __shared__ float Bs[GT_K][GT_N + 4];
+  const int z = blockIdx.z;
+  const int zb = z / ((K + k_chunk - 1) / k_chunk);       // batch index
+  const int zk = z % ((K + k_chunk - 1) / k_chunk);       // K split index
+  A += (long long)zb * sA;
+  B += (long long)zb * sB;
+  const int m0 = blockIdx.y * GT_M, n0 = blockIdx.x * GT_N;
+  const int tid = threadIdx.x, tx = tid % 16, ty = tid / 16;
+  const int kb = zk * k_chunk, ke = min(K, kb + k_chunk);
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int k0 = kb; k0 < ke; k0 += GT_K) {
+    for (int i = tid; i < GT_M * GT_K; i += 256) {
+      const int r = i / GT_K, kk = i % GT_K, gm = m0 + r, gk = k0 + kk;
+      As[kk][r] = (gm < M && gk < ke) ? to_f32(A[(long long)gm * lda + gk]) : 0.f;
+    }
+    for (int i = tid; i < GT_K * GT_N; i += 256) {
+      const int kk = i / GT_N, c = i % GT_N, gk = k0 + kk, gn = n0 + c;
+      Bs[kk][c] = (gk < ke && gn < N) ? to_f32(B[(long long)gk * ldb + gn]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < GT_K; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = m0 + ty * 4 + i;
+    if (row < M) epi(zb, row, n0 + tx * 4, acc[i], N);
+  }
+}
+
+template <typename TA, typename TB, class Epi>
+static cudaError_t simt_gemm(const TA* A, long long lda, long long sA, const TB* B, long long ldb,
+                             long long sB, int M, int N, int K, int batch, int k_splits, Epi epi,
+                             cudaStream_t s) {
+  if (M <= 0 || N <= 0 || K <= 0 || batch <= 0) return cudaSuccess;
+  int k_chunk = (K + k_splits - 1) / k_splits;
+  k_chunk = (k_chunk + GT_K - 1) / GT_K * GT_K;
+  const int splits = (K + k_chunk - 1) / k_chunk;
+  dim3 grid((N + GT_N - 1) / GT_N, (M + GT_M - 1) / GT_M, batch * splits);
+  simt_gemm_kernel<TA, TB, Epi><<<grid, 256, 0, s>>>(A, lda, sA, B, ldb, sB, M, N, K, k_chunk, epi);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// Plain store into C[z * sC + row * ldc + col].
+template <typename TC>
+struct StoreEpi {
+  TC* C;
+  long long ldc, sC;
+  __device__ void operator()(int z, int row, int col0, const float* v, int N) const {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (col0 + j < N) C[(long long)z * sC + (long long)row * ldc + col0 + j] = from_f32<TC>(v[j]);
+  }
+};
+
+// fp32 atomic accumulation (split-K partial sums).
+struct AtomicAddEpi {
+  float* C;
+  long long ldc;
+  __device__ void operator()(int, int row, int col0, const float* v, int N) const {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (col0 + j < N) atomicAdd(&C[(long long)row * ldc + col0 + j], v[j]);
+  }
+};
+
+// ======================================================================== cache append
+// Validates one append row; returns the destination row of the cache or -1.
+__device__ __forceinline__ long long append_slot(const int32_t* req_ids, const int32_t* positions,
+                                                 const int32_t* block_table, int batch,
+                                                 int max_pages, int num_pages, int P, int r,
+                                                 int32_t* status, int* pos_out) {
+  const int b = req_ids[r], pos = positions[r];
+  if (b < 0 || b >= batch || pos < 0 || pos / P >= max_pages) {
+    flag_status(status, MLA_ERR_DEVICE_GUARD);
+    return -1;
+  }
+  const int page = block_table[(long long)b * max_pages + pos / P];
+  if (page < 0 || page >= num_pages) {
+    flag_status(status, MLA_ERR_DEVICE_GUARD);
+    return -1;
+  }
+  *pos_out = pos;
+  return (long long)page * P + pos % P;
+}
+
+// One block per token row: [c_kv | RoPE(k_pe)] encoded into its page slot.
+template <typename AT, typename CT>
+__global__ void __launch_bounds__(128) append_latent_kernel(
+    const AT* __restrict__ c_kv, const AT* __restrict__ k_pe, const int32_t* req_ids,
+    const int32_t* positions, const int32_t* block_table, int batch, int max_pages,
+    CT* __restrict__ cache, int num_pages, int P, int d_c, int d_r, int rotate, RopeTable rt,
+    float cache_scale, int32_t* status) {
+  const int r = blockIdx.x;
+  int pos = 0;
+  const long long slot = append_slot(req_ids, positions, block_table, batch, max_pages, num_pages,
+                                     P, r, (threadIdx.x == 0) ? status : nullptr, &pos);
+  if (slot < 0) return;
+  const int D = d_c + d_r;
+  CT* dst = cache + slot * D;
+  for (int e = threadIdx.x; e < D / 2; e += blockDim.x) {
+    const int col = 2 * e;
+    float x0, x1;
+    if (col < d_c) {
+      x0 = to_f32(c_kv[(long long)r * d_c + col]);
+      x1 = to_f32(c_kv[(long long)r * d_c + col + 1]);
+    } else {
+      const int kc = col - d_c;
+      x0 = to_f32(k_pe[(long long)r * d_r + kc]);
+      x1 = to_f32(k_pe[(long long)r * d_r + kc + 1]);
+      if (rotate) {
+        float sn, cs;
+        rope_sincos(rt, kc / 2, pos, &sn, &cs);
+        const float y0 = x0 * cs - x1 * sn;
+        const float y1 = x0 * sn + x1 * cs;
+        x0 = y0;
+        x1 = y1;
+      }
+    }
+    dst[col] = CacheCodec<CT>::encode(x0, cache_scale);
+    dst[col + 1] = CacheCodec<CT>::encode(x1, cache_scale);
+  }
+}
+
+// GEMM epilogue of the append from hidden states: row r of [c | k_raw] = h_r W.
+template <typename CT>
+struct AppendEpi {
+  const int32_t* req_ids;
+  const int32_t* positions;
+  const int32_t* block_table;
+  int batch, max_pages, num_pages, P, d_c, d_r;
+  CT* cache;
+  RopeTable rt;
+  float cache_scale;
+  int32_t* status;
+  __device__ void operator()(int, int row, int col0, const float* v, int N) const {
+    int pos = 0;
+    const long long slot = append_slot(req_ids, positions, block_table, batch, max_pages,
+                                       num_pages, P, row, (col0 == 0) ? status : nullptr, &pos);
+    if (slot < 0) return;
+    CT* dst = cache + slot * (d_c + d_r);
+#pragma unroll
+    for (int j = 0; j < 4; j += 2) {
+      const int col = col0 + j;
+      if (col >= N) break;
+      float x0 = v[j], x1 = v[j + 1];
+      if (col >= d_c) {
+        float sn, cs;
+        rope_sincos(rt, (col - d_c) / 2, pos, &sn, &cs);
+        const float y0 = x0 * cs - x1 * sn;
+        const float y1 = x0 * sn + x1 * cs;
+        x0 = y0;
+        x1 = y1;
+      }
+      dst[col] = CacheCodec<CT>::encode(x0, cache_scale);
+      dst[col + 1] = CacheCodec<CT>::encode(x1, cache_scale);
+    }
+  }
+};
+
+// ======================================================================== weight fold
+template <typename T>
+__global__ void transpose_heads_kernel(const T* __restrict__ W_UK, T* __restrict__ W_UK_abs, int H,
+                                       int d_c, int d_n) {
+  const long long n_total = (long long)H * d_n * d_c;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n_total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int c = (int)(i % d_c);
+    const long long hn = i / d_c;
+    const int n = (int)(hn % d_n), h = (int)(hn / d_n);
+    W_UK_abs[i] = W_UK[(long long)c * H * d_n + (long long)h * d_n + n];
+  }
+}
+
+// ======================================================================== query prologue
+template <typename T>
+__global__ void q_rope_kernel(const T* __restrict__ q_pe, const int32_t* seq_lens, int batch,
+                              int q_len, int H, int d_c, int d_r, RopeTable rt, T* __restrict__ q_lat) {
+  const long long pairs = (long long)batch * q_len * H * (d_r / 2);
+  const int D = d_c + d_r;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < pairs;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int k = (int)(i % (d_r / 2));
+    const long long gh = i / (d_r / 2);           // (b * q_len + t) * H + h
+    const long long g = gh / H;
+    const int b = (int)(g / q_len), t = (int)(g % q_len);
+    const int pos = seq_lens[b] - q_len + t;
+    const float x0 = to_f32(q_pe[gh * d_r + 2 * k]);
+    const float x1 = to_f32(q_pe[gh * d_r + 2 * k + 1]);
+    float y0 = 0.f, y1 = 0.f;
+    if (pos >= 0) {
+      float sn, cs;
+      rope_sincos(rt, k, pos, &sn, &cs);
+      y0 = x0 * cs - x1 * sn;
+      y1 = x0 * sn + x1 * cs;
+    }
+    q_lat[gh * D + d_c + 2 * k] = from_f32<T>(y0);
+    q_lat[gh * D + d_c + 2 * k + 1] = from_f32<T>(y1);
+  }
+}
+
+// ======================================================================== split planner
+// In-place inclusive prefix sum of a[0..n) in shared memory by one block.
+__device__ void block_inclusive_scan(int* a, int n, int* warp_tot) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int per = (n + nt - 1) / nt;
+  const int b0 = min(n, tid * per), b1 = min(n, b0 + per);
+  int run = 0;
+  for (int i = b0; i < b1; ++i) {
+    run += a[i];
+    a[i] = run;
+  }
+  // exclusive scan of the per-thread totals
+  const int lane = tid & 31, wid = tid >> 5;
+  int x = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tot[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int w = (lane < (nt + 31) / 32) ? warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_tot[lane] = w;
+  }
+  __syncthreads();
+  const int offset = x - run + (wid > 0 ? warp_tot[wid - 1] : 0);
+  for (int i = b0; i < b1; ++i) a[i] += offset;
+  __syncthreads();
+}
+
+// Largest g in [0, n) with cu[g] <= x (cu non-decreasing, cu[0] = 0 <= x < cu[n]).
+__device__ __forceinline__ int group_of(const int* cu, int n, long long x) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu[mid] <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// The flattened sequence of all groups' key pages is cut into `workers` equal ranges;
+// worker w processes its range as one work item per group it touches. An item that
+// covers a whole group writes the final output, the others write partials merged by
+// the combine kernel.
+__global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
+  extern __shared__ int sm[];
+  const int groups = p.batch * p.q_len;
+  int* cu = sm;                             // [groups + 1]
+  int* wc = sm + groups + 1;                // [workers + 1]
+  int* warp_tot = wc + p.workers + 1;       // [32]
+  const int tid = threadIdx.x, nt = blockDim.x;
+  // each decode call reports its own status: clear the word before anything can flag it
+  if (tid == 0) *p.status = 0;
+  __syncthreads();
+  for (int g = tid; g < groups; g += nt) {
+    const int b = g / p.q_len, t = g % p.q_len;
+    const int S = p.seq_lens[b];
+    int kv = 0;
+    if (S != 0) {
+      if (S < p.q_len || (long long)S > (long long)p.max_pages * p.page_size) {
+        if (t == 0) flag_status(p.status, MLA_ERR_DEVICE_GUARD);
+      } else {
+        kv = S - p.q_len + t + 1;
+      }
+    }
+    p.group_kv[g] = kv;
+    p.group_first[g] = -1;
+    p.group_last[g] = -2;
+    cu[g + 1] = (kv + p.page_size - 1) / p.page_size;
+  }
+  if (tid == 0) {
+    cu[0] = 0;
+    wc[0] = 0;
+  }
+  __syncthreads();
+  block_inclusive_scan(cu + 1, groups, warp_tot);
+  const long long T = cu[groups];
+  for (int w = tid; w < p.workers; w += nt) {
+    const long long lo = T * w / p.workers, hi = T * (w + 1) / p.workers;
+    int cnt = 0;
+    if (hi > lo) {
+      const int g0 = group_of(cu, groups, lo), g1 = group_of(cu, groups, hi - 1);
+      for (int g = g0; g <= g1; ++g) cnt += (cu[g + 1] > cu[g]);
+    }
+    wc[w + 1] = cnt;
+  }
+  __syncthreads();
+  block_inclusive_scan(wc + 1, p.workers, warp_tot);
+  for (int w = tid; w <= p.workers; w += nt) p.worker_off[w] = wc[w];
+  for (int w = tid; w < p.workers; w += nt) {
+    const long long lo = T * w / p.workers, hi = T * (w + 1) / p.workers;
+    if (hi <= lo) continue;
+    int idx = wc[w];
+    const int g0 = group_of(cu, groups, lo), g1 = group_of(cu, groups, hi - 1);
+    for (int g = g0; g <= g1; ++g) {
+      const int a = cu[g], e = cu[g + 1];
+      if (e == a) continue;
+      const int pb = (int)(max(lo, (long long)a) - a), pe = (int)(min(hi, (long long)e) - a);
+      WorkItem it;
+      it.group = g;
+      it.page_begin = pb;
+      it.page_end = pe;
+      it.single = (pb == 0 && pe == e - a);
+      p.items[idx] = it;
+      if (pb == 0) p.group_first[g] = idx;
+      if (pe == e - a) p.group_last[g] = idx;
+      ++idx;
+    }
+  }
+}
+
+// ======================================================================== SIMT decode
+// One CTA = one worker x 8 heads (one warp per head). Per page: the page rows are
+// copied into shared memory with an odd word stride (conflict-free row-parallel reads);
+// lanes own tokens for the scores and latent dims for the output accumulation.
+template <typename CT> struct PageElem;
+template <> struct PageElem<float> {
+  __device__ __forceinline__ static float get(const uint32_t* row, int k) {
+    return __uint_as_float(row[k]);
+  }
+  __device__ __forceinline__ static float dot(const uint32_t* row, const float* q, int D) {
+    float acc = 0.f;
+    for (int w = 0; w < D; ++w) acc = fmaf(q[w], __uint_as_float(row[w]), acc);
+    return acc;
+  }
+};
+template <> struct PageElem<bf16> {
+  __device__ __forceinline__ static float get(const uint32_t* row, int k) {
+    const uint32_t w = row[k >> 1];
+    return __uint_as_float((k & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  }
+  __device__ __forceinline__ static float dot(const uint32_t* row, const float* q, int D) {
+    float acc = 0.f;
+    for (int w = 0; w < D / 2; ++w) {
+      const uint32_t v = row[w];
+      acc = fmaf(q[2 * w], __uint_as_float(v << 16), acc);
+      acc = fmaf(q[2 * w + 1], __uint_as_float(v & 0xFFFF0000u), acc);
+    }
+    return acc;
+  }
+};
+template <> struct PageElem<uint8_t> {
+  __device__ __forceinline__ static float get(const uint32_t* row, int k) {
+    return fp8_to_f32((uint8_t)(row[k >> 2] >> (8 * (k & 3))));
+  }
+  __device__ __forceinline__ static float dot(const uint32_t* row, const float* q, int D) {
+    float acc = 0.f;
+    for (int w = 0; w < D / 4; ++w) {
+      const uint32_t v = row[w];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) acc = fmaf(q[4 * w + b], fp8_to_f32((uint8_t)(v >> (8 * b))), acc);
+    }
+    return acc;
+  }
+};
+
+constexpr int SIMT_HEADS = 8;
+
+template <typename QT, typename CT, int VPL>
+__global__ void __launch_bounds__(256) decode_simt_kernel(DecodeParams p) {
+  extern __shared__ __align__(16) uint32_t smem_simt[];
+  const int D = p.D, P = p.P;
+  const int row_words = (int)((D * sizeof(CT) + 3) / 4);
+  const int stride = row_words | 1;
+  uint32_t* page_s = smem_simt;                                   // [P][stride]
+  float* q_s = reinterpret_cast<float*>(smem_simt + P * stride);   // [SIMT_HEADS][D]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * SIMT_HEADS + warp;
+  const bool head_ok = h < p.H;
+  const CT* cache = reinterpret_cast<const CT*>(p.cache);
+  const QT* q_lat = reinterpret_cast<const QT*>(p.q_lat);
+  const int it0 = p.worker_off[blockIdx.x], it1 = p.worker_off[blockIdx.x + 1];
+  for (int it = it0; it < it1; ++it) {
+    const WorkItem item = p.items[it];
+    const int g = item.group, b = g / p.q_len;
+    const int kv = p.group_kv[g];
+    __syncthreads();
+    for (int i = threadIdx.x; i < SIMT_HEADS * D; i += blockDim.x) {
+      const int hh = blockIdx.y * SIMT_HEADS + i / D;
+      q_s[i] = hh < p.H ? to_f32(q_lat[((long long)g * p.H + hh) * D + i % D]) : 0.f;
+    }
+    float m = -INFINITY, l = 0.f;
+    float o[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) o[i] = 0.f;
+    for (int pg = item.page_begin; pg < item.page_end; ++pg) {
+      const int page_id = p.block_table[(long long)b * p.max_pages + pg];
+      const bool page_ok = page_id >= 0 && page_id < p.num_pages;
+      const int ntok = min(P, kv - pg * P);
+      __syncthreads();
+      if (page_ok) {
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(cache + (long long)page_id * P * D);
+        for (int i = threadIdx.x; i < ntok * row_words; i += blockDim.x)
+          page_s[(i / row_words) * stride + i % row_words] = src[i];
+      } else if (threadIdx.x == 0) {
+        flag_status(p.status, MLA_ERR_DEVICE_GUARD);
+      }
+      __syncthreads();
+      if (!page_ok || !head_ok) continue;
+      const float* qh = q_s + warp * D;
+      float s0 = -INFINITY, s1 = -INFINITY;
+      if (lane < ntok) s0 = PageElem<CT>::dot(page_s + lane * stride, qh, D) * p.scale_log2;
+      if (lane + 32 < ntok) s1 = PageElem<CT>::dot(page_s + (lane + 32) * stride, qh, D) * p.scale_log2;
+      const float m_new = fmaxf(m, warp_max(fmaxf(s0, s1)));
+      const float alpha = exp2f(m - m_new);
+      const float p0 = exp2f(s0 - m_new), p1 = exp2f(s1 - m_new);
+      l = l * alpha + warp_sum(p0 + p1);
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) o[i] *= alpha;
+      for (int j = 0; j < ntok; ++j) {
+        const float pj = __shfl_sync(0xffffffffu, (j < 32) ? p0 : p1, j & 31);
+        const uint32_t* row = page_s + j * stride;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          const int k = lane + 32 * i;
+          if (k < p.d_c) o[i] = fmaf(pj, PageElem<CT>::get(row, k), o[i]);
+        }
+      }
+      m = m_new;
+    }
+    if (head_ok) {
+      const float inv_l = (l > 0.f) ? p.out_scale / l : 0.f;
+      const float lse_v = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
+      if (item.single) {
+        QT* out = reinterpret_cast<QT*>(p.out_latent) + ((long long)g * p.H + h) * p.d_c;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          const int k = lane + 32 * i;
+          if (k < p.d_c) out[k] = from_f32<QT>(o[i] * inv_l);
+        }
+        if (lane == 0) p.lse[(long long)g * p.H + h] = lse_v;
+      } else {
+        float* out = p.part_o + ((long long)it * p.H + h) * p.d_c;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+          const int k = lane + 32 * i;
+          if (k < p.d_c) out[k] = o[i] * inv_l;
+        }
+        if (lane == 0) p.part_lse[(long long)it * p.H + h] = lse_v;
+      }
+    }
+  }
+}
+
+// ======================================================================== LSE combine
+// out = sum_s exp(lse_s - L) o_s with L = log sum_s exp(lse_s) over a group's items;
+// groups with no item (empty requests) get out = 0, lse = -inf.
+template <typename QT>
+__global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
+  const int gh = blockIdx.x;
+  const int g = gh / p.H, h = gh % p.H;
+  const int k = blockIdx.y * blockDim.x + threadIdx.x;
+  const int first = p.group_first[g], last = p.group_last[g];
+  const int n = (first >= 0 && last >= first) ? last - first + 1 : 0;
+  QT* out = reinterpret_cast<QT*>(p.out_latent) + (long long)gh * p.d_c;
+  if (n == 1) return;
+  if (n == 0) {
+    if (k < p.d_c) out[k] = from_f32<QT>(0.f);
+    if (k == 0) p.lse[gh] = -INFINITY;
+    return;
+  }
+  float m = -INFINITY;
+  for (int s = 0; s < n; ++s) m = fmaxf(m, p.part_lse[(long long)(first + s) * p.H + h]);
+  if (m == -INFINITY) {
+    if (k < p.d_c) out[k] = from_f32<QT>(0.f);
+    if (k == 0) p.lse[gh] = -INFINITY;
+    return;
+  }
+  float sum = 0.f;
+  for (int s = 0; s < n; ++s) sum += expf(p.part_lse[(long long)(first + s) * p.H + h] - m);
+  const float L = m + logf(sum);
+  if (k < p.d_c) {
+    float acc = 0.f;
+    for (int s = 0; s < n; ++s) {
+      const long long slot = (long long)(first + s) * p.H + h;
+      acc = fmaf(expf(p.part_lse[slot] - L), p.part_o[slot * p.d_c + k], acc);
+    }
+    out[k] = from_f32<QT>(acc);
+  }
+  if (k == 0) p.lse[gh] = L;
+}
+
+template <typename T>
+__global__ void f32_to_act_kernel(const float* __restrict__ src, T* __restrict__ dst, long long n) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += (long long)gridDim.x * blockDim.x)
+    dst[i] = from_f32<T>(src[i]);
+}
+
+// ======================================================================== launchers
+cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
+  const size_t smem = (size_t)(p.batch * p.q_len + 1 + p.workers + 1 + 32) * sizeof(int);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  plan_kernel<<<1, 1024, smem, s>>>(p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t query_prologue_t(const void* q_nope, const void* q_pe, const void* W_UK_abs,
+                                    const int32_t* seq_lens, int batch, int q_len, int H, int d_n,
+                                    int d_c, int d_r, const RopeTable& rt, void* q_lat,
+                                    cudaStream_t s) {
+  const int groups = batch * q_len, D = d_c + d_r;
+  StoreEpi<T> epi{reinterpret_cast<T*>(q_lat), (long long)H * D, (long long)D};
+  // per head h: q_lat[g][h][0:d_c] = q_nope[g][h][:] . W_UK_abs[h]
+  cudaError_t e = simt_gemm(reinterpret_cast<const T*>(q_nope), (long long)H * d_n, (long long)d_n,
+                            reinterpret_cast<const T*>(W_UK_abs), (long long)d_c,
+                            (long long)d_n * d_c, groups, d_c, d_n, H, 1, epi, s);
+  if (e != cudaSuccess) return e;
+  const long long pairs = (long long)groups * H * (d_r / 2);
+  const int blocks = (int)min((pairs + 255) / 256, 4096LL);
+  if (blocks > 0) {
+    q_rope_kernel<T><<<blocks, 256, 0, s>>>(reinterpret_cast<const T*>(q_pe), seq_lens, batch, q_len,
+                                           H, d_c, d_r, rt, reinterpret_cast<T*>(q_lat));
+    note_launch();
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_query_prologue(mla_dtype act, const void* q_nope, const void* q_pe,
+                                  const void* W_UK_abs, const int32_t* seq_lens, int batch,
+                                  int q_len, int H, int d_n, int d_c, int d_r,
+                                  const RopeTable& rt, void* q_lat, cudaStream_t s) {
+  if (act == MLA_F32)
+    return query_prologue_t<float>(q_nope, q_pe, W_UK_abs, seq_lens, batch, q_len, H, d_n, d_c,
+                                   d_r, rt, q_lat, s);
+  return query_prologue_t<bf16>(q_nope, q_pe, W_UK_abs, seq_lens, batch, q_len, H, d_n, d_c, d_r,
+                                rt, q_lat, s);
+}
+
+template <typename QT, typename CT, int VPL>
+static cudaError_t decode_simt_t(const DecodeParams& p, cudaStream_t s) {
+  const int row_words = (int)((p.D * sizeof(CT) + 3) / 4);
+  const int stride = row_words | 1;
+  const size_t smem = (size_t)p.P * stride * 4 + (size_t)SIMT_HEADS * p.D * 4;
+  auto kern = decode_simt_kernel<QT, CT, VPL>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  dim3 grid(p.workers, (p.H + SIMT_HEADS - 1) / SIMT_HEADS);
+  kern<<<grid, 256, smem, s>>>(p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+template <typename QT, typename CT>
+static cudaError_t decode_simt_vpl(const DecodeParams& p, cudaStream_t s) {
+  const int vpl = (p.d_c + 31) / 32;
+  if (vpl <= 2) return decode_simt_t<QT, CT, 2>(p, s);
+  if (vpl <= 4) return decode_simt_t<QT, CT, 4>(p, s);
+  if (vpl <= 8) return decode_simt_t<QT, CT, 8>(p, s);
+  return decode_simt_t<QT, CT, 16>(p, s);
+}
+
+cudaError_t launch_decode_simt(mla_dtype act, mla_dtype cache, const DecodeParams& p,
+                               cudaStream_t s) {
+  if (act == MLA_F32) return decode_simt_vpl<float, float>(p, s);
+  if (cache == MLA_BF16) return decode_simt_vpl<bf16, bf16>(p, s);
+  return decode_simt_vpl<bf16, uint8_t>(p, s);
+}
+
+cudaError_t launch_combine(mla_dtype act, const DecodeParams& p, int groups, cudaStream_t s) {
+  if (groups <= 0) return cudaSuccess;
+  dim3 grid(groups * p.H, (p.d_c + 127) / 128);
+  if (act == MLA_F32) combine_kernel<float><<<grid, 128, 0, s>>>(p);
+  else combine_kernel<bf16><<<grid, 128, 0, s>>>(p);
+  note_launch();
+  return cudaGetLastError();
+}
+
+template <typename AT, typename CT>
+static cudaError_t append_latent_t(const void* c_kv, const void* k_pe, int T,
+                                   const int32_t* req_ids, const int32_t* positions,
+                                   const int32_t* block_table, int batch, int max_pages,
+                                   void* cache_ptr, int num_pages, int P, int d_c, int d_r,
+                                   int rotate, const RopeTable& rt, float cache_scale,
+                                   int32_t* status, cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  append_latent_kernel<AT, CT><<<T, 128, 0, s>>>(
+      reinterpret_cast<const AT*>(c_kv), reinterpret_cast<const AT*>(k_pe), req_ids, positions,
+      block_table, batch, max_pages, reinterpret_cast<CT*>(cache_ptr), num_pages, P, d_c, d_r,
+      rotate, rt, cache_scale, status);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append_latent(mla_dtype act, mla_dtype cache, const void* c_kv,
+                                 const void* k_pe, int T, const int32_t* req_ids,
+                                 const int32_t* positions, const int32_t* block_table, int batch,
+                                 int max_pages, void* cache_ptr, int num_pages, int P, int d_c,
+                                 int d_r, int rotate, const RopeTable& rt, float cache_scale,
+                                 int32_t* status, cudaStream_t s) {
+  if (act == MLA_F32)
+    return append_latent_t<float, float>(c_kv, k_pe, T, req_ids, positions, block_table, batch,
+                                         max_pages, cache_ptr, num_pages, P, d_c, d_r, rotate, rt,
+                                         cache_scale, status, s);
+  if (cache == MLA_BF16)
+    return append_latent_t<bf16, bf16>(c_kv, k_pe, T, req_ids, positions, block_table, batch,
+                                       max_pages, cache_ptr, num_pages, P, d_c, d_r, rotate, rt,
+                                       cache_scale, status, s);
+  return append_latent_t<bf16, uint8_t>(c_kv, k_pe, T, req_ids, positions, block_table, batch,
+                                        max_pages, cache_ptr, num_pages, P, d_c, d_r, rotate, rt,
+                                        cache_scale, status, s);
+}
+
+template <typename AT, typename CT>
+static cudaError_t append_from_h_t(const void* h, const void* W, int T, int d,
+                                   const int32_t* req_ids, const int32_t* positions,
+                                   const int32_t* block_table, int batch, int max_pages,
+                                   void* cache_ptr, int num_pages, int P, int d_c, int d_r,
+                                   const RopeTable& rt, float cache_scale, int32_t* status,
+                                   cudaStream_t s) {
+  AppendEpi<CT> epi{req_ids, positions, block_table, batch, max_pages, num_pages, P, d_c, d_r,
+                    reinterpret_cast<CT*>(cache_ptr), rt, cache_scale, status};
+  const int D = d_c + d_r;
+  return simt_gemm(reinterpret_cast<const AT*>(h), (long long)d, 0LL,
+                   reinterpret_cast<const AT*>(W), (long long)D, 0LL, T, D, d, 1, 1, epi, s);
+}
+
+cudaError_t launch_append_from_h(mla_dtype act, mla_dtype cache, const void* h, const void* W,
+                                 int T, int d, const int32_t* req_ids, const int32_t* positions,
+                                 const int32_t* block_table, int batch, int max_pages,
+                                 void* cache_ptr, int num_pages, int P, int d_c, int d_r,
+                                 const RopeTable& rt, float cache_scale, int32_t* status,
+                                 cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  if (act == MLA_F32)
+    return append_from_h_t<float, float>(h, W, T, d, req_ids, positions, block_table, batch,
+                                         max_pages, cache_ptr, num_pages, P, d_c, d_r, rt,
+                                         cache_scale, status, s);
+  if (cache == MLA_BF16)
+    return append_from_h_t<bf16, bf16>(h, W, T, d, req_ids, positions, block_table, batch,
+                                       max_pages, cache_ptr, num_pages, P, d_c, d_r, rt,
+                                       cache_scale, status, s);
+  return append_from_h_t<bf16, uint8_t>(h, W, T, d, req_ids, positions, block_table, batch,
+                                        max_pages, cache_ptr, num_pages, P, d_c, d_r, rt,
+                                        cache_scale, status, s);
+}
+
+template <typename T>
+static cudaError_t absorb_t(const void* W_UK, const void* W_UV, const void* W_O, void* W_UK_abs,
+                           void* W_comb, int H, int d_c, int d_n, int d_v, int d, cudaStream_t s) {
+  const long long n = (long long)H * d_n * d_c;
+  transpose_heads_kernel<T><<<(int)min((n + 255) / 256, 8192LL), 256, 0, s>>>(
+      reinterpret_cast<const T*>(W_UK), reinterpret_cast<T*>(W_UK_abs), H, d_c, d_n);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // block i of W_comb = W_UV[:, i*d_v:(i+1)*d_v] . W_O[i*d_v:(i+1)*d_v, :]
+  StoreEpi<T> epi{reinterpret_cast<T*>(W_comb), (long long)d, (long long)d_c * d};
+  return simt_gemm(reinterpret_cast<const T*>(W_UV), (long long)H * d_v, (long long)d_v,
+                   reinterpret_cast<const T*>(W_O), (long long)d, (long long)d_v * d, d_c, d, d_v,
+                   H, 1, epi, s);
+}
+
+cudaError_t launch_absorb(mla_dtype act, const void* W_UK, const void* W_UV, const void* W_O,
+                          void* W_UK_abs, void* W_comb, int H, int d_c, int d_n, int d_v, int d,
+                          cudaStream_t s) {
+  if (act == MLA_F32) return absorb_t<float>(W_UK, W_UV, W_O, W_UK_abs, W_comb, H, d_c, d_n, d_v, d, s);
+  return absorb_t<bf16>(W_UK, W_UV, W_O, W_UK_abs, W_comb, H, d_c, d_n, d_v, d, s);
+}
+
+// out = o_lat . W_comb with split-K partial sums accumulated in fp32 in `acc`
+// ([rows][N], zeroed here), then converted to the activation dtype.
+template <typename T>
+static cudaError_t output_proj_t(const void* o_lat, const void* W_comb, int rows, int K, int N,
+                                 void* out, float* acc, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(acc, 0, (size_t)rows * N * sizeof(float), s);
+  if (e != cudaSuccess) return e;
+  const int splits = max(1, min(64, K / 1024));
+  AtomicAddEpi epi{acc, (long long)N};
+  e = simt_gemm(reinterpret_cast<const T*>(o_lat), (long long)K, 0LL,
+                reinterpret_cast<const T*>(W_comb), (long long)N, 0LL, rows, N, K, 1, splits, epi, s);
+  if (e != cudaSuccess) return e;
+  const long long n = (long long)rows * N;
+  f32_to_act_kernel<T><<<(int)min((n + 255) / 256, 4096LL), 256, 0, s>>>(acc, reinterpret_cast<T*>(out), n);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_output_proj_simt_ws(mla_dtype act, const void* o_lat, const void* W_comb,
+                                       int rows, int K, int N, void* out, float* acc,
+                                       cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (act == MLA_F32) return output_proj_t<float>(o_lat, W_comb, rows, K, N, out, acc, s);
+  return output_proj_t<bf16>(o_lat, W_comb, rows, K, N, out, acc, s);
+}
+
+}  // namespace mla

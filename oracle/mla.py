@@ -167,18 +167,25 @@ def absorbed_query(q_nope, W_UK_abs):
                      np.asarray(W_UK_abs, np.float64))
 
 
-def decode_absorbed(c, k_rot, q_nope, q_pe, W_UK_abs, scale: float, theta: float = 10000.0):
+def decode_absorbed(c, k_rot, q_nope, q_pe, W_UK_abs, scale: float, theta: float = 10000.0,
+                    heads=None):
     """Weight-absorbed decode of one request, all heads ([P1] §3-1 and §3-2; [P2]
     "위치 정보와 압축의 충돌": score = q_hat . c_s + q^R . k^R_s).
 
     The MQA form of [P3] "MLA의 MQA 디코딩 경로": every head attends over the one
     shared latent row [c_j ; k^R_j]. Same positions and causal rule as
-    decode_decompressed. Returns o_lat [q][H][d_c] (= sum_j A_j c_j) and lse [q][H].
+    decode_decompressed. ``heads`` optionally restricts the computation to a list of
+    head indices (the outputs then follow that order). Returns o_lat [q][h][d_c]
+    (= sum_j A_j c_j) and lse [q][h].
     """
     c = np.asarray(c, np.float64)
     k_rot = np.asarray(k_rot, np.float64)
     q_nope = np.asarray(q_nope, np.float64)
     q_pe = np.asarray(q_pe, np.float64)
+    if heads is not None:
+        heads = list(heads)
+        q_nope, q_pe = q_nope[:, heads], q_pe[:, heads]
+        W_UK_abs = np.asarray(W_UK_abs)[heads]
     S, d_c = c.shape
     q, H = q_nope.shape[0], q_nope.shape[1]
     o = np.zeros((q, H, d_c))

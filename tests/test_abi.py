@@ -1,0 +1,121 @@
+"""The C-ABI library: it builds, loads, exports every entry point declared in
+include/mla.h, and rejects bad arguments on the host before launching anything.
+No test here needs a GPU or runs a kernel."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+import mla_latent_kv_04_gb300 as M
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+           if f.endswith(".h")]
+
+
+def _declared_functions():
+    names = set()
+    for h in HEADERS:
+        src = open(h, encoding="utf-8").read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        src = re.sub(r"typedef[^;]*;", "", src, flags=re.S)
+        for m in re.finditer(r"\b(mla_[A-Za-z0-9_]+)\s*\(", src):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(M.LIB_PATH):
+        if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+            pytest.fail("libmla.so is not built and nvcc is unavailable")
+        from mla_latent_kv_04_gb300 import build
+        build.build()
+    return M.lib()
+
+
+def test_header_declares_the_four_calls():
+    names = _declared_functions()
+    for f in ("mla_absorb_weights", "mla_append_cache", "mla_decode", "mla_output_proj"):
+        assert f in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(M.LIB_PATH)
+    missing = [n for n in _declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_python_binding_names_match_header():
+    for n in _declared_functions():
+        if n in ("mla_decode_ex",):
+            continue
+        assert hasattr(M, n), n
+
+
+def test_status_strings(lib):
+    assert M.mla_status_string(0) == "ok"
+    assert "workspace" in M.mla_status_string(3)
+    assert M.mla_version() >= 100
+
+
+def _cfg(**kw):
+    c = M.make_config(W.V2, "bf16", "bf16")
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("num_heads", 0, M.MLA_ERR_INVALID),
+    ("d_rope", 63, M.MLA_ERR_INVALID),
+    ("page_size", 128, M.MLA_ERR_UNSUPPORTED),
+    ("rope_interleaved", 0, M.MLA_ERR_UNSUPPORTED),
+    ("cache_dtype", M.MLA_F32, M.MLA_ERR_UNSUPPORTED),
+    ("act_dtype", 7, M.MLA_ERR_INVALID),
+])
+def test_bad_config_is_rejected_before_any_launch(lib, field, value, code):
+    n = ctypes.c_size_t(0)
+    st = lib.mla_decode_workspace_size(ctypes.byref(_cfg(**{field: value})), 4, 1, None,
+                                       ctypes.byref(n))
+    assert st == code
+
+
+def test_fp8_needs_a_scale(lib):
+    c = _cfg(cache_dtype=M.MLA_FP8_E4M3, cache_scale=0.0)
+    n = ctypes.c_size_t(0)
+    assert lib.mla_decode_workspace_size(ctypes.byref(c), 4, 1, None, ctypes.byref(n)) == M.MLA_ERR_INVALID
+
+
+def test_null_pointers_and_small_workspace_are_rejected(lib):
+    c = _cfg()
+    # null inputs
+    st = lib.mla_decode(ctypes.byref(c), None, None, None, None, 1, None, 1, None, 1, 1, None, None,
+                        None, 0, None)
+    assert st == M.MLA_ERR_INVALID
+    # all pointers non-null but no workspace: a fake non-null address is never dereferenced
+    fake = ctypes.c_void_p(256)
+    st = lib.mla_decode(ctypes.byref(c), fake, fake, fake, fake, 1, fake, 1, fake, 1, 1, fake, fake,
+                        None, 0, None)
+    assert st == M.MLA_ERR_WORKSPACE
+    st = lib.mla_output_proj(ctypes.byref(c), fake, fake, 2, fake, None, 0, None)
+    assert st == M.MLA_ERR_WORKSPACE
+    st = lib.mla_append_cache_latent(ctypes.byref(c), None, None, 3, None, None, None, 1, 1, None, 1,
+                                     1, None, None)
+    assert st == M.MLA_ERR_INVALID
+    # T == 0 is a no-op that touches nothing
+    st = lib.mla_append_cache_latent(ctypes.byref(c), None, None, 0, None, None, None, 1, 1, None, 1,
+                                     1, None, None)
+    assert st == M.MLA_OK
+
+
+def test_workspace_grows_with_batch(lib):
+    c = _cfg()
+    a = M.mla_decode_workspace_size(c, 4, 1, num_workers=8)
+    b = M.mla_decode_workspace_size(c, 64, 2, num_workers=8)
+    assert b > a > 0
+    assert M.mla_output_proj_workspace_size(c, 32) == 32 * 5120 * 4
