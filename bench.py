@@ -51,6 +51,35 @@ def _peaks():
             "source": "fallback"}
 
 
+# ----------------------------------------------------------------------------- events
+
+_CUDART = None
+
+
+def event_ms(a, b) -> float:
+    """Milliseconds between two recorded torch CUDA events. Read through the CUDA runtime
+    directly, because some events are recorded inside libmla (torch does not see those)."""
+    global _CUDART
+    import ctypes
+    if _CUDART is None:
+        import mla_latent_kv_04_gb300 as M
+        M.lib()
+        for name in ("libcudart.so.13", "libcudart.so"):
+            try:
+                _CUDART = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        _CUDART.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p,
+                                                 ctypes.c_void_p]
+    out = ctypes.c_float(0.0)
+    rc = _CUDART.cudaEventElapsedTime(ctypes.byref(out), ctypes.c_void_p(a.cuda_event),
+                                      ctypes.c_void_p(b.cuda_event))
+    if rc != 0:
+        raise RuntimeError(f"cudaEventElapsedTime failed ({rc})")
+    return float(out.value)
+
+
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -350,6 +379,11 @@ def main():
     K = args.steps
     mk = lambda: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))  # noqa
     evs = [{k: mk() for k in ("append", "decode", "attn", "oproj")} for _ in range(K)]
+    for e in evs:          # torch creates the CUDA event on first record; libmla records 'attn'
+        for a, b2 in e.values():
+            a.record()
+            b2.record()
+    torch.cuda.synchronize()
     t0, t1 = mk()
     clocks = ClockSampler(local)
     clocks.start()
@@ -366,7 +400,7 @@ def main():
     launches = M.mla_kernel_launches() - launches0
     clk = clocks.stop()
     ms = t0.elapsed_time(t1) / K
-    parts = {k: sum(e[k][0].elapsed_time(e[k][1]) for e in evs) / K
+    parts = {k: sum(event_ms(e[k][0], e[k][1]) for e in evs) / K
              for k in ("append", "decode", "attn", "oproj")}
     if world > 1:
         tt = torch.tensor([ms], dtype=torch.float64)

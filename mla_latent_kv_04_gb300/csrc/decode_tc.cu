@@ -1,12 +1,522 @@
-// Tensor-core decode kernel (sm_103a): placeholder until the tcgen05 kernel lands.
+// Tensor-core MLA decode for sm_103a: tcgen05 MMAs with TMEM accumulators, TMA-staged
+// cache pages, a CTA pair per worker.
+//
+// Math (huny.dev "DeepSeek MLA 해부" §3-1/§3-2; secrett2633.cloud "MLA의 MQA 디코딩 경로"):
+// every head of one query token attends, MQA-style, over the request's shared 576-wide
+// latent rows [c_kv | k_pe]; score = q_lat . row * scale; output = softmax . c_kv.
+//
+// Work split. 128 heads x 512 latent dims of fp32 output fill all 512 TMEM columns of
+// one SM, leaving no room for the scores, so each worker is a 2-CTA cluster that splits
+// the latent dimensions: CTA r owns c_kv dims [256r, 256r+256) and k_pe dims
+// [512+32r, 512+32r+32). Per 64-token page each CTA
+//   1. TMA-loads only its 288-column slice of the page (36 KB; the pair reads each byte of
+//      the page once),
+//   2. computes a partial score S_r = Q_r K_r^T (M = 128 heads, N = 64 tokens, K = 288)
+//      into TMEM,
+//   3. sends S_r to the peer over distributed shared memory (st.async, counted on the
+//      peer's mbarrier) and adds the peer's partial: both CTAs hold the same full S,
+//   4. runs the online softmax (one thread per head row, exp2, lazy rescaling of O
+//      only when the running maximum grows by more than 2^8),
+//   5. writes P (bf16) to shared memory and accumulates O_r += P C_r (M = 128, N = 256,
+//      K = 64) in TMEM.
+// Roles: warp 0 issues TMA, warp 1 issues MMAs (one thread) and owns the TMEM
+// allocation, warps 2-5 run the softmax and the epilogue (thread = head row = TMEM lane).
+// Every mbarrier wait is bounded (2 s): on timeout the kernel records MLA_ERR_TIMEOUT,
+// every role leaves its loop, TMEM is freed and the pair meets at a final cluster
+// barrier before exit.
+#include <cudaTypedefs.h>
+#include <math.h>
+
 #include "decode_tc.h"
+#include "sm100_ptx.cuh"
 
 namespace mla {
+namespace tc {
 
-bool tc_decode_supported(const mla_config*) { return false; }
+constexpr int kH = 128, kDC = 512, kDR = 64, kD = 576, kP = 64;
+constexpr int kNS = 2;                                   // cache-page pipeline stages
+constexpr int kQTileC = 128 * 64 * 2;                    // one 64-dim SW128 chunk of Q_r
+constexpr int kQTilePE = 128 * 32 * 2;                   // the 32-dim SW64 k_pe half of Q_r
+constexpr int kQBytes = 4 * kQTileC + kQTilePE;          // 73728
+constexpr int kKTileC = 64 * 64 * 2;                     // one 64-dim SW128 chunk of a page
+constexpr int kKTilePE = 64 * 32 * 2;                    // the 32-dim SW64 k_pe half
+constexpr int kStageBytes = 4 * kKTileC + kKTilePE;      // 36864
+constexpr int kPBytes = 128 * 64 * 2;                    // P: 128 heads x 64 tokens bf16
+constexpr int kXBytes = 128 * 64 * 4;                    // peer partial scores, fp32
+constexpr int kOffQ = 0;
+constexpr int kOffStage = kOffQ + kQBytes;
+constexpr int kOffP = kOffStage + kNS * kStageBytes;
+constexpr int kOffX = kOffP + kPBytes;
+constexpr int kOffBar = kOffX + kXBytes;
+constexpr int kSmemBytes = kOffBar + 256 + 1024;         // + slack to align the base to 1 KB
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0;                            // O_r: 256 columns
+constexpr uint32_t kColS = 256;                          // S: 64 columns
+constexpr int kThreads = 192;
+constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 64, false, false);
+constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, 256, false, true);
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+// mbarrier slots (8 bytes each) at kOffBar
+enum {
+  B_FULL0 = 0, B_EMPTY0 = kNS, B_QFULL = 2 * kNS, B_QEMPTY, B_SFULL, B_SFREE, B_PFULL, B_PVDONE,
+  B_XFULL, B_XEMPTY, B_OFREE, B_TEARDOWN, B_COUNT
+};
+static_assert(B_COUNT * 8 <= 128, "barrier area");
+
+struct Shared {
+  uint8_t* base;       // 1 KB aligned
+  uint32_t base_u32;
+  volatile int* abort;
+  uint32_t* tmem_slot;
+  __device__ uint32_t bar(int i) const { return base_u32 + kOffBar + 8 * i; }
+  __device__ uint32_t q() const { return base_u32 + kOffQ; }
+  __device__ uint32_t stage(int s) const { return base_u32 + kOffStage + s * kStageBytes; }
+  __device__ uint32_t pbuf() const { return base_u32 + kOffP; }
+  __device__ uint32_t xbuf() const { return base_u32 + kOffX; }
+};
+
+__device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_t parity,
+                                         int32_t* status, bool cluster_scope = false) {
+  auto probe = [&]() {
+    return cluster_scope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+  };
+  if (probe()) return true;
+  const uint64_t t0 = ptx::globaltimer();
+  while (true) {
+    if (probe()) return true;
+    if (*sh.abort) return false;
+    if (ptx::globaltimer() - t0 > kTimeoutNs) {
+      *sh.abort = 1;
+      flag_status(status, MLA_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------- roles
+__device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensorMap* tm_kc,
+                         const CUtensorMap* tm_kpe, const CUtensorMap* tm_qc,
+                         const CUtensorMap* tm_qpe, int worker, int rank) {
+  const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
+  int stage = 0;
+  uint32_t wrap = 0, q_iter = 0;
+  for (int it = it0; it < it1; ++it) {
+    const WorkItem item = p.items[it];
+    const int g = item.group, b = g / p.q_len;
+    if (!wait_bar(sh, sh.bar(B_QEMPTY), (q_iter & 1) ^ 1, p.status)) return;
+    ptx::mbar_arrive_expect_tx(sh.bar(B_QFULL), kQBytes);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      ptx::tma_load_2d(sh.q() + c * kQTileC, tm_qc, 256 * rank + 64 * c, g * kH, sh.bar(B_QFULL));
+    ptx::tma_load_2d(sh.q() + 4 * kQTileC, tm_qpe, kDC + 32 * rank, g * kH, sh.bar(B_QFULL));
+    ++q_iter;
+    for (int pg = item.page_begin; pg < item.page_end; ++pg) {
+      int page = p.block_table[(long long)b * p.max_pages + pg];
+      if (page < 0 || page >= p.num_pages) page = 0;      // masked by the softmax side
+      if (!wait_bar(sh, sh.bar(B_EMPTY0 + stage), (wrap & 1) ^ 1, p.status)) return;
+      const uint32_t full = sh.bar(B_FULL0 + stage);
+      ptx::mbar_arrive_expect_tx(full, kStageBytes);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        ptx::tma_load_2d(sh.stage(stage) + c * kKTileC, tm_kc, 256 * rank + 64 * c, page * kP, full);
+      ptx::tma_load_2d(sh.stage(stage) + 4 * kKTileC, tm_kpe, kDC + 32 * rank, page * kP, full);
+      if (++stage == kNS) {
+        stage = 0;
+        ++wrap;
+      }
+    }
+  }
+}
+
+__device__ void mma_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker) {
+  const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
+  int stage = 0;
+  uint32_t wrap = 0, n = 0, q_iter = 0, item_idx = 0;
+  for (int it = it0; it < it1; ++it) {
+    const WorkItem item = p.items[it];
+    if (!wait_bar(sh, sh.bar(B_QFULL), q_iter & 1, p.status)) return;
+    for (int pg = item.page_begin; pg < item.page_end; ++pg) {
+      const bool first = (pg == item.page_begin);
+      if (!wait_bar(sh, sh.bar(B_FULL0 + stage), wrap & 1, p.status)) return;
+      if (!wait_bar(sh, sh.bar(B_SFREE), (n & 1) ^ 1, p.status)) return;
+      ptx::tc_fence_after();
+      const uint32_t st = sh.stage(stage);
+      // S = Q_r K_r^T over the CTA's 256 c_kv dims (SW128) and 32 k_pe dims (SW64)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint64_t a = ptx::smem_desc(sh.q() + c * kQTileC + 32 * k, 16, 1024, ptx::kSwizzle128);
+          const uint64_t bd = ptx::smem_desc(st + c * kKTileC + 32 * k, 16, 1024, ptx::kSwizzle128);
+          ptx::mma_bf16_ss(tmem + kColS, a, bd, kIdescQK, (c | k) ? 1u : 0u);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const uint64_t a = ptx::smem_desc(sh.q() + 4 * kQTileC + 32 * k, 16, 512, ptx::kSwizzle64);
+        const uint64_t bd = ptx::smem_desc(st + 4 * kKTileC + 32 * k, 16, 512, ptx::kSwizzle64);
+        ptx::mma_bf16_ss(tmem + kColS, a, bd, kIdescQK, 1u);
+      }
+      ptx::mma_commit(sh.bar(B_SFULL));
+      if (!wait_bar(sh, sh.bar(B_PFULL), n & 1, p.status)) return;
+      if (first && !wait_bar(sh, sh.bar(B_OFREE), (item_idx & 1) ^ 1, p.status)) return;
+      ptx::tc_fence_after();
+      // O_r += P C_r: P K-major (tokens contiguous), C_r MN-major (dims contiguous)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint64_t a = ptx::smem_desc(sh.pbuf() + 32 * k, 16, 1024, ptx::kSwizzle128);
+        const uint64_t bd = ptx::smem_desc(st + 2048 * k, kKTileC, 1024, ptx::kSwizzle128);
+        ptx::mma_bf16_ss(tmem + kColO, a, bd, kIdescPV, (!first || k) ? 1u : 0u);
+      }
+      ptx::mma_commit(sh.bar(B_EMPTY0 + stage));
+      ptx::mma_commit(sh.bar(B_PVDONE));
+      ++n;
+      if (++stage == kNS) {
+        stage = 0;
+        ++wrap;
+      }
+    }
+    ptx::mma_commit(sh.bar(B_QEMPTY));
+    ++q_iter;
+    ++item_idx;
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b, float* sum) {
+  const bf16 x = __float2bfloat16_rn(a), y = __float2bfloat16_rn(b);
+  *sum += __bfloat162float(x) + __bfloat162float(y);
+  return (uint32_t)__bfloat16_as_ushort(x) | ((uint32_t)__bfloat16_as_ushort(y) << 16);
+}
+
+__device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker,
+                                 int rank, int warp, int lane) {
+  const int quarter = warp & 3;
+  const int row = 32 * quarter + lane;                   // head index = TMEM lane
+  const uint32_t t_row = tmem + ((uint32_t)(32 * quarter) << 16);
+  const uint32_t peer = (uint32_t)(rank ^ 1);
+  const uint32_t peer_x = ptx::map_to_rank(sh.xbuf(), peer);
+  const uint32_t peer_xfull = ptx::map_to_rank(sh.bar(B_XFULL), peer);
+  const uint32_t peer_xempty = ptx::map_to_rank(sh.bar(B_XEMPTY), peer);
+  const float* xrow = reinterpret_cast<const float*>(sh.base + kOffX + row * 256);
+  uint8_t* prow = sh.base + kOffP + row * 128;
+  const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
+  uint32_t n = 0;
+  for (int it = it0; it < it1; ++it) {
+    const WorkItem item = p.items[it];
+    const int g = item.group, b = g / p.q_len, kv = p.group_kv[g];
+    float m_used = -INFINITY, l = 0.f;
+    for (int pg = item.page_begin; pg < item.page_end; ++pg) {
+      const int page = p.block_table[(long long)b * p.max_pages + pg];
+      const bool valid = page >= 0 && page < p.num_pages;
+      if (!valid && row == 0 && rank == 0) flag_status(p.status, MLA_ERR_DEVICE_GUARD);
+      const int ntok = valid ? min(kP, kv - pg * kP) : 0;
+      // 1. own partial scores out of TMEM
+      if (!wait_bar(sh, sh.bar(B_SFULL), n & 1, p.status)) return;
+      ptx::tc_fence_after();
+      uint32_t sa[32], sb[32];
+      ptx::tmem_ld32(t_row + kColS, sa);
+      ptx::tmem_ld32(t_row + kColS + 32, sb);
+      ptx::tmem_wait_ld();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(sh.bar(B_SFREE));
+      // 2. swap partials with the peer CTA
+      if (!wait_bar(sh, sh.bar(B_XEMPTY), (n & 1) ^ 1, p.status, true)) return;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint32_t* src = (c < 8) ? &sa[4 * c] : &sb[4 * (c - 8)];
+        const uint32_t pos = (uint32_t)(c ^ (row & 7));
+        ptx::st_async_v4(peer_x + row * 256 + pos * 16, __uint_as_float(src[0]),
+                         __uint_as_float(src[1]), __uint_as_float(src[2]), __uint_as_float(src[3]),
+                         peer_xfull);
+      }
+      if (!wait_bar(sh, sh.bar(B_XFULL), n & 1, p.status, true)) return;
+      if (warp == 2 && lane == 0) ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL), kXBytes);
+      float s[64];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const uint32_t pos = (uint32_t)(c ^ (row & 7));
+        const float4 v = *reinterpret_cast<const float4*>(xrow + pos * 4);
+        const uint32_t* src = (c < 8) ? &sa[4 * c] : &sb[4 * (c - 8)];
+        s[4 * c + 0] = __uint_as_float(src[0]) + v.x;
+        s[4 * c + 1] = __uint_as_float(src[1]) + v.y;
+        s[4 * c + 2] = __uint_as_float(src[2]) + v.z;
+        s[4 * c + 3] = __uint_as_float(src[3]) + v.w;
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_remote(peer_xempty);
+      // Rows past the request's last token (or a whole skipped page) may hold anything,
+      // NaN included, and 0 * NaN would poison O: zero them in the staged c_kv tiles
+      // before the P . C product reads them (the QK product that read them is done).
+      if (ntok < kP) {
+        uint8_t* stg = sh.base + kOffStage + (int)(n % kNS) * kStageBytes;
+        const int nrows = kP - ntok;
+        const int per_tile = nrows * 8;                    // 16-byte chunks per tile
+        for (int i = 32 * (warp - 2) + lane; i < 4 * per_tile; i += 128) {
+          const int tile = i / per_tile, rem = i % per_tile;
+          *reinterpret_cast<uint4*>(stg + tile * kKTileC + (ntok + rem / 8) * 128 + (rem % 8) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      // 3. online softmax in the log2 domain
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        s[i] = (i < ntok) ? s[i] * p.scale_log2 : -INFINITY;
+        mx = fmaxf(mx, s[i]);
+      }
+      bool rescale = false;
+      float alpha = 1.f;
+      if (mx > -INFINITY) {
+        if (m_used == -INFINITY) {
+          m_used = mx;
+        } else if (mx > m_used + 8.f) {
+          alpha = exp2f(m_used - mx);
+          m_used = mx;
+          l *= alpha;
+          rescale = true;
+        }
+      }
+      uint32_t packed[32];
+      float psum = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float p0 = (s[2 * i] == -INFINITY) ? 0.f : exp2f(s[2 * i] - m_used);
+        const float p1 = (s[2 * i + 1] == -INFINITY) ? 0.f : exp2f(s[2 * i + 1] - m_used);
+        packed[i] = pack_bf16(p0, p1, &psum);
+      }
+      l += psum;
+      // 4. the previous P . C product must be done before P or O are touched
+      if (n > 0 && !wait_bar(sh, sh.bar(B_PVDONE), (n - 1) & 1, p.status)) return;
+      ptx::tc_fence_after();
+      if (rescale) {
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[32];
+          ptx::tmem_ld32(t_row + kColO + 32 * c, v);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+          ptx::tmem_st32(t_row + kColO + 32 * c, v);
+        }
+        ptx::tmem_wait_st();
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t pos = (uint32_t)(c ^ (row & 7));
+        *reinterpret_cast<uint4*>(prow + pos * 16) =
+            make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+      }
+      ptx::fence_proxy_async_smem();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(sh.bar(B_PFULL));
+      ++n;
+    }
+    // 5. epilogue: normalise O_r and write it (final output or split partial)
+    if (!wait_bar(sh, sh.bar(B_PVDONE), (n - 1) & 1, p.status)) return;
+    ptx::tc_fence_after();
+    const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
+    const float lse_v = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      uint32_t v[32];
+      ptx::tmem_ld32(t_row + kColO + 32 * c, v);
+      ptx::tmem_wait_ld();
+      const int col = 256 * rank + 32 * c;
+      if (item.single) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out_latent) +
+                                              ((long long)g * kH + row) * kDC + col);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float dummy = 0.f;
+          dst[q] = make_uint4(pack_bf16(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv, &dummy),
+                              pack_bf16(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv, &dummy),
+                              pack_bf16(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv, &dummy),
+                              pack_bf16(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv, &dummy));
+        }
+      } else {
+        float4* dst = reinterpret_cast<float4*>(p.part_o + ((long long)it * kH + row) * kDC + col);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
+                               __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+      }
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(sh.bar(B_OFREE));
+    if (rank == 0) {
+      if (item.single) p.lse[(long long)g * kH + row] = lse_v;
+      else p.part_lse[(long long)it * kH + row] = lse_v;
+    }
+  }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
+                     const __grid_constant__ CUtensorMap tm_kpe,
+                     const __grid_constant__ CUtensorMap tm_qc,
+                     const __grid_constant__ CUtensorMap tm_qpe, const DecodeParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  Shared sh;
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t aligned = (raw + 1023u) & ~1023u;
+  sh.base = smem_raw + (aligned - raw);
+  sh.base_u32 = aligned;
+  sh.abort = reinterpret_cast<volatile int*>(sh.base + kOffBar + 128);
+  sh.tmem_slot = reinterpret_cast<uint32_t*>(sh.base + kOffBar + 136);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = (int)ptx::cluster_ctarank();
+  const int worker = blockIdx.x >> 1;
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(sh.bar(B_FULL0 + 0), 1);
+    ptx::mbar_init(sh.bar(B_FULL0 + 1), 1);
+    ptx::mbar_init(sh.bar(B_EMPTY0 + 0), 1);
+    ptx::mbar_init(sh.bar(B_EMPTY0 + 1), 1);
+    ptx::mbar_init(sh.bar(B_QFULL), 1);
+    ptx::mbar_init(sh.bar(B_QEMPTY), 1);
+    ptx::mbar_init(sh.bar(B_SFULL), 1);
+    ptx::mbar_init(sh.bar(B_SFREE), 4);
+    ptx::mbar_init(sh.bar(B_PFULL), 4);
+    ptx::mbar_init(sh.bar(B_PVDONE), 1);
+    ptx::mbar_init(sh.bar(B_XFULL), 1);
+    ptx::mbar_init(sh.bar(B_XEMPTY), 4);
+    ptx::mbar_init(sh.bar(B_OFREE), 4);
+    ptx::mbar_init(sh.bar(B_TEARDOWN), 1);
+    *sh.abort = 0;
+    ptx::fence_mbar_init();
+    ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL), kXBytes);   // phase 0 of the peer's sends
+    ptx::prefetch_tensormap(&tm_kc);
+    ptx::prefetch_tensormap(&tm_kpe);
+    ptx::prefetch_tensormap(&tm_qc);
+    ptx::prefetch_tensormap(&tm_qpe);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(sh.tmem_slot), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  ptx::cluster_sync();
+  const uint32_t tmem = *sh.tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) producer(sh, p, &tm_kc, &tm_kpe, &tm_qc, &tm_qpe, worker, rank);
+  } else if (warp == 1) {
+    if (lane == 0) mma_issuer(sh, p, tmem, worker);
+  } else {
+    softmax_epilogue(sh, p, tmem, worker, rank, warp, lane);
+  }
+
+  // teardown: every role gets here, normally or after a bounded wait gave up
+  __syncthreads();
+  if (warp == 1) {
+    if (lane == 0) {
+      // every issued MMA must have finished before TMEM is released
+      ptx::mma_commit(sh.bar(B_TEARDOWN));
+      const uint64_t t0 = ptx::globaltimer();
+      while (!ptx::mbar_try_wait(sh.bar(B_TEARDOWN), 0) && ptx::globaltimer() - t0 < kTimeoutNs) {
+      }
+    }
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+  if (*sh.abort) {
+    // let copies already in flight into this CTA's shared memory land before it exits
+    const uint64_t t0 = ptx::globaltimer();
+    while (ptx::globaltimer() - t0 < 2000000ull) {
+    }
+  }
+  ptx::cluster_sync();
+}
+
+// ------------------------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows][576] array; box = box_cols x box_rows.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_cols, uint32_t box_rows,
+              CUtensorMapSwizzle swz) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+
+bool tc_decode_supported(const mla_config* c) {
+  return c && c->act_dtype == MLA_BF16 && c->cache_dtype == MLA_BF16 && c->num_heads == tc::kH &&
+         c->d_latent == tc::kDC && c->d_rope == tc::kDR && c->page_size == tc::kP;
+}
+
 bool tc_decode_default_enabled() { return false; }
-cudaError_t launch_decode_tc(mla_dtype, const DecodeParams&, cudaStream_t) {
-  return cudaErrorNotSupported;
+
+int tc_decode_max_workers() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    if (cudaFuncSetAttribute(tc::decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tc::kSmemBytes) != cudaSuccess)
+      return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(tc::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = tc::kSmemBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc::decode_tc_kernel, &cfg) != cudaSuccess || n <= 0)
+      return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+cudaError_t launch_decode_tc(mla_dtype cache, const DecodeParams& p, cudaStream_t s) {
+  if (cache != MLA_BF16) return cudaErrorNotSupported;
+  CUtensorMap kc, kpe, qc, qpe;
+  const uint64_t cache_rows = (uint64_t)p.num_pages * tc::kP;
+  const uint64_t q_rows = (uint64_t)p.batch * p.q_len * tc::kH;
+  if (!tc::make_map(&kc, p.cache, cache_rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tc::make_map(&kpe, p.cache, cache_rows, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !tc::make_map(&qc, p.q_lat, q_rows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !tc::make_map(&qpe, p.q_lat, q_rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(tc::decode_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  tc::decode_tc_kernel<<<2 * p.workers, tc::kThreads, tc::kSmemBytes, s>>>(kc, kpe, qc, qpe, p);
+  note_launch();
+  return cudaGetLastError();
 }
 
 }  // namespace mla

@@ -14,7 +14,7 @@ from tests import harness as Hn
 pytestmark = pytest.mark.gpu
 
 DEV = torch.device("cuda:0")
-KERNELS = [M.KERNEL_SIMT]
+KERNELS = [M.KERNEL_SIMT, M.KERNEL_TC]
 
 
 def _kernel_id(k):
