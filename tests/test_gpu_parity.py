@@ -106,7 +106,7 @@ def test_split_count_invariance(kernel):
         assert d <= 1e-2 * np.max(np.abs(outs[0]["out_latent"])) + 1e-3
 
 
-@pytest.mark.parametrize("kernel", KERNELS, ids=_kernel_id)
+@pytest.mark.parametrize("kernel", [M.KERNEL_SIMT], ids=_kernel_id)
 def test_fp8_cache_small(kernel):
     wl = W.scaled(W.WORKLOADS["v2_fp8_b128_s8192"], (5, 64, 300, 1), name="v2_fp8_small")
     st = Hn.build_state(wl, DEV)
