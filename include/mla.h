@@ -160,6 +160,23 @@ mla_status mla_decode_ex(const mla_config* cfg, const void* q_nope, const void* 
                          int batch, int q_len, void* out_latent, float* lse, void* workspace,
                          size_t workspace_bytes, const mla_decode_opts* opts, void* stream);
 
+/* mla_decode without a caller workspace, for callers that cannot allocate device memory
+ * when they decode (a plugin inside a runtime that owns all device allocations, a serving
+ * loop with a frozen memory footprint, an environment that bans dynamic allocation). The
+ * pages have no counterpart to this call: it is a deployment convenience of this library.
+ * Its scratch is one 64 MiB array in device memory, statically part of the library and
+ * held by every GPU that loads it until the process exits; a batch whose
+ * mla_decode_workspace_size exceeds 64 MiB is rejected with MLA_ERR_WORKSPACE and an
+ * explanation in mla_last_error(). The first call on a device looks the array up
+ * (cudaGetSymbolAddress) with that device current: make it outside any stream capture.
+ * All calls share the array, so calls whose GPU work overlaps (other streams, unordered
+ * host threads) race; order them on one stream. Nothing in the array needs to start at
+ * zero. Arguments and results are those of mla_decode. */
+mla_status mla_decode_noalloc(const mla_config* cfg, const void* q_nope, const void* q_pe,
+                              const void* W_UK_abs, const void* cache, int num_pages,
+                              const int32_t* block_table, int max_pages, const int32_t* seq_lens,
+                              int batch, int q_len, void* out_latent, float* lse, void* stream);
+
 /* Bytes of workspace mla_output_proj needs for `rows` rows (may be 0). */
 mla_status mla_output_proj_workspace_size(const mla_config* cfg, int rows, size_t* bytes);
 

@@ -70,6 +70,7 @@ _SIGNATURES = {
     "mla_decode": (_I, [_CFG, _P, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P, _P, _P, _SZ, _P]),
     "mla_decode_ex": (_I, [_CFG, _P, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P, _P, _P, _SZ,
                            ctypes.POINTER(MlaDecodeOpts), _P]),
+    "mla_decode_noalloc": (_I, [_CFG, _P, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P, _P, _P]),
     "mla_output_proj_workspace_size": (_I, [_CFG, _I, ctypes.POINTER(_SZ)]),
     "mla_output_proj": (_I, [_CFG, _P, _P, _I, _P, _P, _SZ, _P]),
     "mla_read_device_status": (_I, [_P, _P, ctypes.POINTER(_I)]),
@@ -262,6 +263,29 @@ def mla_decode(cfg, q_nope, q_pe, W_UK_abs, cache, block_table, seq_lens, out_la
         _ptr(lse, "lse", (t.float32,), batch * q_len * H),
         _ptr(workspace, "workspace", (t.uint8,)), workspace.numel(), ctypes.byref(o),
         _stream(stream)), "mla_decode")
+
+
+def mla_decode_noalloc(cfg, q_nope, q_pe, W_UK_abs, cache, block_table, seq_lens, out_latent, lse,
+                       stream=None):
+    """mla_decode with the library's fixed 64 MiB device scratch array instead of a workspace,
+    for callers that cannot allocate device memory at decode time. Calls sharing the array
+    must be ordered on the GPU; the first call on a device must come before any capture."""
+    a = (_act_dtype(cfg),)
+    t = _torch()
+    batch, q_len = q_nope.shape[0], q_nope.shape[1]
+    H, d_c, d_r, d_n = cfg.num_heads, cfg.d_latent, cfg.d_rope, cfg.d_nope
+    D = d_c + d_r
+    num_pages = cache.numel() // (cfg.page_size * D)
+    max_pages = block_table.shape[1]
+    _check(lib().mla_decode_noalloc(
+        ctypes.byref(cfg), _ptr(q_nope, "q_nope", a, batch * q_len * H * d_n),
+        _ptr(q_pe, "q_pe", a, batch * q_len * H * d_r),
+        _ptr(W_UK_abs, "W_UK_abs", a, H * d_n * d_c),
+        _ptr(cache, "cache", _cache_dtypes(cfg), num_pages * cfg.page_size * D), num_pages,
+        _ptr(block_table, "block_table", _i32(0), batch * max_pages), max_pages,
+        _ptr(seq_lens, "seq_lens", _i32(0), batch), batch, q_len,
+        _ptr(out_latent, "out_latent", a, batch * q_len * H * d_c),
+        _ptr(lse, "lse", (t.float32,), batch * q_len * H), _stream(stream)), "mla_decode_noalloc")
 
 
 def mla_output_proj_workspace_size(cfg, rows) -> int:

@@ -134,6 +134,10 @@ bool use_tc_kernel(const mla_config* c, const mla_decode_opts* o) {
 
 }  // namespace
 
+namespace mla {
+void set_last_error(const std::string& what) { g_last_error = what; }
+}  // namespace mla
+
 extern "C" {
 
 int mla_version(void) { return 100; }
