@@ -187,11 +187,14 @@ def setup(wl, dev):
     out = torch.empty(rows * d.d_model, dtype=act, device=dev)
     ws = torch.zeros(M.mla_decode_workspace_size(cfg, B, q), dtype=torch.uint8, device=dev)
     ws_o = torch.zeros(M.mla_output_proj_workspace_size(cfg, rows), dtype=torch.uint8, device=dev)
+    n_a = M.mla_append_cache_workspace_size(cfg, rows)
+    ws_a = torch.zeros(n_a, dtype=torch.uint8, device=dev) if n_a else None
     torch.cuda.synchronize()
     return {"cfg": cfg, "dw": dw, "cache": cache, "bt_d": bt_d, "W_UK_abs": W_UK_abs,
             "W_comb": W_comb, "host": host, "dev_in": dev_in,
             "new_req": up(new_req, torch.int32), "new_pos": up(new_pos, torch.int32),
-            "out_lat": out_lat, "lse": lse, "out": out, "ws": ws, "ws_o": ws_o, "status": status}
+            "out_lat": out_lat, "lse": lse, "out": out, "ws": ws, "ws_o": ws_o, "ws_a": ws_a,
+            "status": status}
 
 
 def step(st, inp, ev=None):
@@ -202,7 +205,7 @@ def step(st, inp, ev=None):
     if ev:
         ev["append"][0].record()
     M.mla_append_cache(cfg, inp["h"], st["dw"]["W_DKV_KR"], st["new_req"], st["new_pos"], st["bt_d"],
-                       st["cache"], dev_status=st["status"])
+                       st["cache"], dev_status=st["status"], workspace=st["ws_a"])
     if ev:
         ev["append"][1].record()
         ev["decode"][0].record()

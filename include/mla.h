@@ -100,11 +100,18 @@ mla_status mla_absorb_weights(const mla_config* cfg, const void* W_UK, const voi
  *   cache [num_pages][P][d_c + d_r]     cache dtype, updated in place
  *   dev_status                          optional int32 device word (may be NULL):
  *                                       MLA_ERR_DEVICE_GUARD is OR-ed in for skipped rows.
+ *   workspace                           device buffer of mla_append_cache_workspace_size
+ *                                       bytes (256-byte aligned; may be NULL when that is 0)
+ *                                       holding the fp32 projection before encoding.
  * Rows must not share a (request, position); T == 0 is a no-op. */
 mla_status mla_append_cache(const mla_config* cfg, const void* h, const void* W_DKV_KR, int T,
                             const int32_t* req_ids, const int32_t* positions,
                             const int32_t* block_table, int batch, int max_pages, void* cache,
-                            int num_pages, int32_t* dev_status, void* stream);
+                            int num_pages, int32_t* dev_status, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace mla_append_cache needs for T rows (0 for fp32 activations). */
+mla_status mla_append_cache_workspace_size(const mla_config* cfg, int T, size_t* bytes);
 
 /* Append T tokens given their latent c_kv [T][d_c] and raw k_pe [T][d_r] (act dtype).
  * rotate != 0 applies RoPE at `positions` to k_pe before encoding; rotate == 0 stores
@@ -183,7 +190,8 @@ mla_status mla_output_proj_workspace_size(const mla_config* cfg, int rows, size_
 /* Output projection through the folded weights (huny.dev §3-2):
  *   out[r] = sum_i out_latent[r][i] W_comb[i*d_c : (i+1)*d_c]
  *   out_latent [rows][H*d_c], W_comb [H*d_c][d], out [rows][d]  (act dtype),
- *   fp32 accumulation. workspace as for mla_decode (may be NULL when its size is 0). */
+ *   fp32 accumulation. workspace: 256-byte aligned device buffer of
+ *   mla_output_proj_workspace_size bytes (an fp32 accumulator plus a status word). */
 mla_status mla_output_proj(const mla_config* cfg, const void* out_latent, const void* W_comb,
                            int rows, void* out, void* workspace, size_t workspace_bytes,
                            void* stream);

@@ -63,7 +63,8 @@ _CFG = ctypes.POINTER(MlaConfig)
 
 _SIGNATURES = {
     "mla_absorb_weights": (_I, [_CFG, _P, _P, _P, _P, _P, _P]),
-    "mla_append_cache": (_I, [_CFG, _P, _P, _I, _P, _P, _P, _I, _I, _P, _I, _P, _P]),
+    "mla_append_cache": (_I, [_CFG, _P, _P, _I, _P, _P, _P, _I, _I, _P, _I, _P, _P, _SZ, _P]),
+    "mla_append_cache_workspace_size": (_I, [_CFG, _I, ctypes.POINTER(_SZ)]),
     "mla_append_cache_latent": (_I, [_CFG, _P, _P, _I, _P, _P, _P, _I, _I, _P, _I, _I, _P, _P]),
     "mla_decode_workspace_size": (_I, [_CFG, _I, _I, ctypes.POINTER(MlaDecodeOpts),
                                        ctypes.POINTER(_SZ)]),
@@ -201,8 +202,16 @@ def _i32(t):
     return (_torch().int32,)
 
 
+def mla_append_cache_workspace_size(cfg, T) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().mla_append_cache_workspace_size(ctypes.byref(cfg), int(T), ctypes.byref(n)),
+           "mla_append_cache_workspace_size")
+    return int(n.value)
+
+
 def mla_append_cache(cfg, h, W_DKV_KR, req_ids, positions, block_table, cache, dev_status=None,
-                     stream=None):
+                     workspace=None, stream=None):
+    """workspace: uint8 device tensor of mla_append_cache_workspace_size bytes (None if 0)."""
     a = (_act_dtype(cfg),)
     T = req_ids.numel()
     D = cfg.d_latent + cfg.d_rope
@@ -213,7 +222,9 @@ def mla_append_cache(cfg, h, W_DKV_KR, req_ids, positions, block_table, cache, d
         T, _ptr(req_ids, "req_ids", _i32(0), T), _ptr(positions, "positions", _i32(0), T),
         _ptr(block_table, "block_table", _i32(0)), batch, max_pages,
         _ptr(cache, "cache", _cache_dtypes(cfg), num_pages * cfg.page_size * D), num_pages,
-        _ptr(dev_status, "dev_status", _i32(0), allow_none=True), _stream(stream)),
+        _ptr(dev_status, "dev_status", _i32(0), allow_none=True),
+        _ptr(workspace, "workspace", (_torch().uint8,), allow_none=True),
+        0 if workspace is None else workspace.numel(), _stream(stream)),
         "mla_append_cache")
 
 

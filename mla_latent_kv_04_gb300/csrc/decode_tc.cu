@@ -472,7 +472,7 @@ bool tc_decode_supported(const mla_config* c) {
          c->d_latent == tc::kDC && c->d_rope == tc::kDR && c->page_size == tc::kP;
 }
 
-bool tc_decode_default_enabled() { return false; }
+bool tc_decode_default_enabled() { return true; }
 
 int tc_decode_max_workers() {
   static int cached[64] = {0};

@@ -102,6 +102,23 @@ cudaError_t launch_absorb(mla_dtype act, const void* W_UK, const void* W_UV, con
                           void* W_UK_abs, void* W_comb, int H, int d_c, int d_n, int d_v, int d,
                           cudaStream_t s);
 
+// Tensor-core GEMMs (bf16 in, fp32 accumulate), gemm_tc.cu.
+cudaError_t launch_output_proj_tc(const void* o_lat, const void* W_comb, int rows, int K, int N,
+                                  void* out, float* acc, int32_t* status, cudaStream_t s);
+cudaError_t launch_query_absorb_tc(const void* q_nope, const void* W_UK_abs, int groups, int H,
+                                   int d_n, int d_c, int D, void* q_lat, int32_t* status,
+                                   cudaStream_t s);
+cudaError_t launch_append_proj_tc(const void* h, const void* W, int T, int d, int Dc, float* acc,
+                                  int32_t* status, cudaStream_t s);
+cudaError_t launch_append_finish(mla_dtype cache, const float* acc, int T, const int32_t* req_ids,
+                                 const int32_t* positions, const int32_t* block_table, int batch,
+                                 int max_pages, void* cache_ptr, int num_pages, int P, int d_c,
+                                 int d_r, const RopeTable& rt, float cache_scale, int32_t* status,
+                                 cudaStream_t s);
+cudaError_t launch_q_rope(mla_dtype act, const void* q_pe, const int32_t* seq_lens, int batch,
+                          int q_len, int H, int d_c, int d_r, const RopeTable& rt, void* q_lat,
+                          cudaStream_t s);
+
 // out = o_lat . W_comb; `acc` is an fp32 [rows][N] accumulator in the caller's workspace.
 cudaError_t launch_output_proj_simt_ws(mla_dtype act, const void* o_lat, const void* W_comb,
                                        int rows, int K, int N, void* out, float* acc,

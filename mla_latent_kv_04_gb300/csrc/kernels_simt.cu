@@ -129,10 +129,10 @@ __device__ __forceinline__ long long append_slot(const int32_t* req_ids, const i
 // One block per token row: [c_kv | RoPE(k_pe)] encoded into its page slot.
 template <typename AT, typename CT>
 __global__ void __launch_bounds__(128) append_latent_kernel(
-    const AT* __restrict__ c_kv, const AT* __restrict__ k_pe, const int32_t* req_ids,
-    const int32_t* positions, const int32_t* block_table, int batch, int max_pages,
-    CT* __restrict__ cache, int num_pages, int P, int d_c, int d_r, int rotate, RopeTable rt,
-    float cache_scale, int32_t* status) {
+    const AT* __restrict__ c_kv, const AT* __restrict__ k_pe, long long ld_c, long long ld_k,
+    const int32_t* req_ids, const int32_t* positions, const int32_t* block_table, int batch,
+    int max_pages, CT* __restrict__ cache, int num_pages, int P, int d_c, int d_r, int rotate,
+    RopeTable rt, float cache_scale, int32_t* status) {
   const int r = blockIdx.x;
   int pos = 0;
   const long long slot = append_slot(req_ids, positions, block_table, batch, max_pages, num_pages,
@@ -144,12 +144,12 @@ __global__ void __launch_bounds__(128) append_latent_kernel(
     const int col = 2 * e;
     float x0, x1;
     if (col < d_c) {
-      x0 = to_f32(c_kv[(long long)r * d_c + col]);
-      x1 = to_f32(c_kv[(long long)r * d_c + col + 1]);
+      x0 = to_f32(c_kv[(long long)r * ld_c + col]);
+      x1 = to_f32(c_kv[(long long)r * ld_c + col + 1]);
     } else {
       const int kc = col - d_c;
-      x0 = to_f32(k_pe[(long long)r * d_r + kc]);
-      x1 = to_f32(k_pe[(long long)r * d_r + kc + 1]);
+      x0 = to_f32(k_pe[(long long)r * ld_k + kc]);
+      x1 = to_f32(k_pe[(long long)r * ld_k + kc + 1]);
       if (rotate) {
         float sn, cs;
         rope_sincos(rt, kc / 2, pos, &sn, &cs);
@@ -571,6 +571,22 @@ static cudaError_t query_prologue_t(const void* q_nope, const void* q_pe, const 
   return cudaGetLastError();
 }
 
+cudaError_t launch_q_rope(mla_dtype act, const void* q_pe, const int32_t* seq_lens, int batch,
+                          int q_len, int H, int d_c, int d_r, const RopeTable& rt, void* q_lat,
+                          cudaStream_t s) {
+  const long long pairs = (long long)batch * q_len * H * (d_r / 2);
+  const int blocks = (int)min((pairs + 255) / 256, 4096LL);
+  if (blocks <= 0) return cudaSuccess;
+  if (act == MLA_F32)
+    q_rope_kernel<float><<<blocks, 256, 0, s>>>(reinterpret_cast<const float*>(q_pe), seq_lens, batch,
+                                               q_len, H, d_c, d_r, rt, reinterpret_cast<float*>(q_lat));
+  else
+    q_rope_kernel<bf16><<<blocks, 256, 0, s>>>(reinterpret_cast<const bf16*>(q_pe), seq_lens, batch,
+                                              q_len, H, d_c, d_r, rt, reinterpret_cast<bf16*>(q_lat));
+  note_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t launch_query_prologue(mla_dtype act, const void* q_nope, const void* q_pe,
                                   const void* W_UK_abs, const int32_t* seq_lens, int batch,
                                   int q_len, int H, int d_n, int d_c, int d_r,
@@ -632,7 +648,8 @@ static cudaError_t append_latent_t(const void* c_kv, const void* k_pe, int T,
                                    int32_t* status, cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   append_latent_kernel<AT, CT><<<T, 128, 0, s>>>(
-      reinterpret_cast<const AT*>(c_kv), reinterpret_cast<const AT*>(k_pe), req_ids, positions,
+      reinterpret_cast<const AT*>(c_kv), reinterpret_cast<const AT*>(k_pe), (long long)d_c,
+      (long long)d_r, req_ids, positions,
       block_table, batch, max_pages, reinterpret_cast<CT*>(cache_ptr), num_pages, P, d_c, d_r,
       rotate, rt, cache_scale, status);
   note_launch();
@@ -656,6 +673,27 @@ cudaError_t launch_append_latent(mla_dtype act, mla_dtype cache, const void* c_k
   return append_latent_t<bf16, uint8_t>(c_kv, k_pe, T, req_ids, positions, block_table, batch,
                                         max_pages, cache_ptr, num_pages, P, d_c, d_r, rotate, rt,
                                         cache_scale, status, s);
+}
+
+// RoPE + encode + scatter of append rows already projected into fp32 acc[T][d_c + d_r].
+cudaError_t launch_append_finish(mla_dtype cache, const float* acc, int T, const int32_t* req_ids,
+                                 const int32_t* positions, const int32_t* block_table, int batch,
+                                 int max_pages, void* cache_ptr, int num_pages, int P, int d_c,
+                                 int d_r, const RopeTable& rt, float cache_scale, int32_t* status,
+                                 cudaStream_t s) {
+  if (T <= 0) return cudaSuccess;
+  const long long ld = d_c + d_r;
+  if (cache == MLA_BF16)
+    append_latent_kernel<float, bf16><<<T, 128, 0, s>>>(acc, acc + d_c, ld, ld, req_ids, positions,
+                                                        block_table, batch, max_pages,
+                                                        reinterpret_cast<bf16*>(cache_ptr), num_pages,
+                                                        P, d_c, d_r, 1, rt, cache_scale, status);
+  else
+    append_latent_kernel<float, uint8_t><<<T, 128, 0, s>>>(
+        acc, acc + d_c, ld, ld, req_ids, positions, block_table, batch, max_pages,
+        reinterpret_cast<uint8_t*>(cache_ptr), num_pages, P, d_c, d_r, 1, rt, cache_scale, status);
+  note_launch();
+  return cudaGetLastError();
 }
 
 template <typename AT, typename CT>

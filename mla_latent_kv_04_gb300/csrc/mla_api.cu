@@ -183,21 +183,49 @@ static mla_status check_append(const mla_config* cfg, int T, const int32_t* req_
   return MLA_OK;
 }
 
+mla_status mla_append_cache_workspace_size(const mla_config* cfg, int T, size_t* bytes) {
+  mla_status st = check_config(cfg);
+  if (st != MLA_OK) return st;
+  if (T < 0 || !bytes) return invalid("T must be >= 0 and bytes non-NULL");
+  *bytes = cfg->act_dtype == MLA_BF16
+               ? align256((size_t)T * (cfg->d_latent + cfg->d_rope) * sizeof(float))
+               : 0;
+  return MLA_OK;
+}
+
 mla_status mla_append_cache(const mla_config* cfg, const void* h, const void* W_DKV_KR, int T,
                             const int32_t* req_ids, const int32_t* positions,
                             const int32_t* block_table, int batch, int max_pages, void* cache,
-                            int num_pages, int32_t* dev_status, void* stream) {
+                            int num_pages, int32_t* dev_status, void* workspace,
+                            size_t workspace_bytes, void* stream) {
   mla_status st = check_append(cfg, T, req_ids, positions, block_table, batch, max_pages, cache,
                                num_pages);
   if (st != MLA_OK) return st;
   if (T == 0) return MLA_OK;
   if (!h || !W_DKV_KR) return invalid("null h or W_DKV_KR");
   const RopeTable rt = rope_table(cfg);
-  cudaError_t e = launch_append_from_h(cfg->act_dtype, cfg->cache_dtype, h, W_DKV_KR, T,
-                                       cfg->d_model, req_ids, positions, block_table, batch,
-                                       max_pages, cache, num_pages, cfg->page_size, cfg->d_latent,
-                                       cfg->d_rope, rt, cfg->cache_scale, dev_status,
-                                       (cudaStream_t)stream);
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e;
+  if (cfg->act_dtype == MLA_BF16) {
+    const int Dc = cfg->d_latent + cfg->d_rope;
+    const size_t need = align256((size_t)T * Dc * sizeof(float));
+    if (!workspace || workspace_bytes < need) {
+      g_last_error = "workspace smaller than mla_append_cache_workspace_size";
+      return MLA_ERR_WORKSPACE;
+    }
+    if (((uintptr_t)workspace & 255) != 0) return invalid("workspace must be 256-byte aligned");
+    float* acc = (float*)workspace;
+    e = launch_append_proj_tc(h, W_DKV_KR, T, cfg->d_model, Dc, acc, dev_status, s);
+    if (e != cudaSuccess) return cuda_fail(e, "mla_append_cache (projection)");
+    e = launch_append_finish(cfg->cache_dtype, acc, T, req_ids, positions, block_table, batch,
+                             max_pages, cache, num_pages, cfg->page_size, cfg->d_latent,
+                             cfg->d_rope, rt, cfg->cache_scale, dev_status, s);
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_append_cache (encode)");
+  }
+  e = launch_append_from_h(cfg->act_dtype, cfg->cache_dtype, h, W_DKV_KR, T, cfg->d_model, req_ids,
+                           positions, block_table, batch, max_pages, cache, num_pages,
+                           cfg->page_size, cfg->d_latent, cfg->d_rope, rt, cfg->cache_scale,
+                           dev_status, s);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_append_cache");
 }
 
@@ -283,9 +311,17 @@ mla_status mla_decode_ex(const mla_config* cfg, const void* q_nope, const void* 
   cudaError_t e = launch_plan(pp, s);
   if (e != cudaSuccess) return cuda_fail(e, "mla_decode (plan)");
 
-  e = launch_query_prologue(cfg->act_dtype, q_nope, q_pe, W_UK_abs, seq_lens, batch, q_len,
-                            cfg->num_heads, cfg->d_nope, cfg->d_latent, cfg->d_rope, rt,
-                            ws + w.q_lat, s);
+  if (cfg->act_dtype == MLA_BF16) {
+    e = launch_query_absorb_tc(q_nope, W_UK_abs, batch * q_len, cfg->num_heads, cfg->d_nope,
+                               cfg->d_latent, D, ws + w.q_lat, pp.status, s);
+    if (e == cudaSuccess)
+      e = launch_q_rope(cfg->act_dtype, q_pe, seq_lens, batch, q_len, cfg->num_heads,
+                        cfg->d_latent, cfg->d_rope, rt, ws + w.q_lat, s);
+  } else {
+    e = launch_query_prologue(cfg->act_dtype, q_nope, q_pe, W_UK_abs, seq_lens, batch, q_len,
+                              cfg->num_heads, cfg->d_nope, cfg->d_latent, cfg->d_rope, rt,
+                              ws + w.q_lat, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "mla_decode (query prologue)");
 
   DecodeParams dp;
@@ -345,7 +381,7 @@ mla_status mla_output_proj_workspace_size(const mla_config* cfg, int rows, size_
   mla_status st = check_config(cfg);
   if (st != MLA_OK) return st;
   if (rows < 0 || !bytes) return invalid("rows must be >= 0 and bytes non-NULL");
-  *bytes = align256((size_t)rows * cfg->d_model * 4);
+  *bytes = align256((size_t)rows * cfg->d_model * 4) + 256;
   return MLA_OK;
 }
 
@@ -357,14 +393,21 @@ mla_status mla_output_proj(const mla_config* cfg, const void* out_latent, const 
   if (rows < 0) return invalid("rows must be >= 0");
   if (rows == 0) return MLA_OK;
   if (!out_latent || !W_comb || !out) return invalid("null pointer");
-  const size_t need = align256((size_t)rows * cfg->d_model * 4);
-  if (!workspace || workspace_bytes < need) {
+  const size_t acc_bytes = align256((size_t)rows * cfg->d_model * 4);
+  if (!workspace || workspace_bytes < acc_bytes + 256) {
     g_last_error = "workspace smaller than mla_output_proj_workspace_size";
     return MLA_ERR_WORKSPACE;
   }
-  cudaError_t e = launch_output_proj_simt_ws(cfg->act_dtype, out_latent, W_comb, rows,
-                                             cfg->num_heads * cfg->d_latent, cfg->d_model, out,
-                                             (float*)workspace, (cudaStream_t)stream);
+  if (((uintptr_t)workspace & 255) != 0) return invalid("workspace must be 256-byte aligned");
+  cudaError_t e;
+  if (cfg->act_dtype == MLA_BF16)
+    e = launch_output_proj_tc(out_latent, W_comb, rows, cfg->num_heads * cfg->d_latent,
+                              cfg->d_model, out, (float*)workspace,
+                              (int32_t*)((char*)workspace + acc_bytes), (cudaStream_t)stream);
+  else
+    e = launch_output_proj_simt_ws(cfg->act_dtype, out_latent, W_comb, rows,
+                                   cfg->num_heads * cfg->d_latent, cfg->d_model, out,
+                                   (float*)workspace, (cudaStream_t)stream);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_output_proj");
 }
 

@@ -73,8 +73,10 @@ def build_state(wl, dev, cfg=None, chunk_tokens=1 << 16):
         if n_h:
             h = W.hidden(wl, b, n_h)
             req, pos = W.append_batch(wl, b, n_lat, n_h)
+            aws = torch.empty(M.mla_append_cache_workspace_size(cfg, n_h), dtype=torch.uint8, device=dev)
             M.mla_append_cache(cfg, to_dev(h, act, dev), dw["W_DKV_KR"], to_dev(req, torch.int32, dev),
-                               to_dev(pos, torch.int32, dev), bt_d, cache, dev_status=status)
+                               to_dev(pos, torch.int32, dev), bt_d, cache, dev_status=status,
+                               workspace=aws if aws.numel() else None)
     H, d_c, d_n, d = wl.dims.num_heads, wl.dims.d_latent, wl.dims.d_nope, wl.dims.d_model
     W_UK_abs = torch.empty(H * d_n * d_c, dtype=act, device=dev)
     W_comb = torch.empty(H * d_c * d, dtype=act, device=dev)

@@ -118,4 +118,5 @@ def test_workspace_grows_with_batch(lib):
     a = M.mla_decode_workspace_size(c, 4, 1, num_workers=8)
     b = M.mla_decode_workspace_size(c, 64, 2, num_workers=8)
     assert b > a > 0
-    assert M.mla_output_proj_workspace_size(c, 32) == 32 * 5120 * 4
+    assert M.mla_output_proj_workspace_size(c, 32) == 32 * 5120 * 4 + 256
+    assert M.mla_append_cache_workspace_size(c, 32) == 32 * 576 * 4
