@@ -10,15 +10,19 @@
 // the latent dimensions: CTA r owns c_kv dims [256r, 256r+256) and k_pe dims
 // [512+32r, 512+32r+32). Per 64-token page each CTA
 //   1. TMA-loads only its 288-column slice of the page (36 KB; the pair reads each byte of
-//      the page once),
+//      the page once) into a 3-stage ring,
 //   2. computes a partial score S_r = Q_r K_r^T (M = 128 heads, N = 64 tokens, K = 288)
 //      into TMEM,
 //   3. sends S_r to the peer over distributed shared memory (st.async, counted on the
 //      peer's mbarrier) and adds the peer's partial: both CTAs hold the same full S,
-//   4. runs the online softmax (one thread per head row, exp2, lazy rescaling of O
-//      only when the running maximum grows by more than 2^8),
-//   5. writes P (bf16) to shared memory and accumulates O_r += P C_r (M = 128, N = 256,
-//      K = 64) in TMEM.
+//   4. runs the online softmax (one thread per head row, exp2, O rescaled lazily, only
+//      when the running maximum grows by more than 2^8),
+//   5. writes P (bf16) into TMEM and accumulates O_r += P C_r (M = 128, N = 256, K = 64;
+//      A = P from TMEM, B = the staged page slice) in TMEM.
+// The softmax threads pipeline pages: for page n they first take the peer's partial,
+// then read and ship their own partial of page n+1 (whose scores the MMA warp computed
+// one page ahead), and only then do page n's softmax, so the cluster exchange of one page
+// overlaps the arithmetic of the previous one.
 // Roles: warp 0 issues TMA, warp 1 issues MMAs (one thread) and owns the TMEM
 // allocation, warps 2-5 run the softmax and the epilogue (thread = head row = TMEM lane).
 // Every mbarrier wait is bounded (2 s): on timeout the kernel records MLA_ERR_TIMEOUT,
@@ -34,24 +38,23 @@ namespace mla {
 namespace tc {
 
 constexpr int kH = 128, kDC = 512, kDR = 64, kD = 576, kP = 64;
-constexpr int kNS = 2;                                   // cache-page pipeline stages
+constexpr int kNS = 3;                                   // cache-page pipeline stages
 constexpr int kQTileC = 128 * 64 * 2;                    // one 64-dim SW128 chunk of Q_r
 constexpr int kQTilePE = 128 * 32 * 2;                   // the 32-dim SW64 k_pe half of Q_r
 constexpr int kQBytes = 4 * kQTileC + kQTilePE;          // 73728
 constexpr int kKTileC = 64 * 64 * 2;                     // one 64-dim SW128 chunk of a page
 constexpr int kKTilePE = 64 * 32 * 2;                    // the 32-dim SW64 k_pe half
 constexpr int kStageBytes = 4 * kKTileC + kKTilePE;      // 36864
-constexpr int kPBytes = 128 * 64 * 2;                    // P: 128 heads x 64 tokens bf16
 constexpr int kXBytes = 128 * 64 * 4;                    // peer partial scores, fp32
 constexpr int kOffQ = 0;
 constexpr int kOffStage = kOffQ + kQBytes;
-constexpr int kOffP = kOffStage + kNS * kStageBytes;
-constexpr int kOffX = kOffP + kPBytes;
+constexpr int kOffX = kOffStage + kNS * kStageBytes;
 constexpr int kOffBar = kOffX + kXBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;         // + slack to align the base to 1 KB
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0;                            // O_r: 256 columns
-constexpr uint32_t kColS = 256;                          // S: 64 columns
+constexpr uint32_t kColO = 0;                            // O_r: 256 fp32 columns
+constexpr uint32_t kColS = 256;                          // S: 64 fp32 columns
+constexpr uint32_t kColP = 320;                          // P: 64 bf16 = 32 columns
 constexpr int kThreads = 192;
 constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, 256, false, true);
@@ -72,7 +75,6 @@ struct Shared {
   __device__ uint32_t bar(int i) const { return base_u32 + kOffBar + 8 * i; }
   __device__ uint32_t q() const { return base_u32 + kOffQ; }
   __device__ uint32_t stage(int s) const { return base_u32 + kOffStage + s * kStageBytes; }
-  __device__ uint32_t pbuf() const { return base_u32 + kOffP; }
   __device__ uint32_t xbuf() const { return base_u32 + kOffX; }
 };
 
@@ -129,15 +131,37 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
   }
 }
 
+// O_r += P C_r for global page m (stage `st`); `first` = the item's first page.
+__device__ __forceinline__ bool issue_pv(const Shared& sh, const DecodeParams& p, uint32_t tmem,
+                                         uint32_t m, int st, bool first, uint32_t item_idx) {
+  if (!wait_bar(sh, sh.bar(B_PFULL), m & 1, p.status)) return false;
+  if (first && !wait_bar(sh, sh.bar(B_OFREE), (item_idx & 1) ^ 1, p.status)) return false;
+  ptx::tc_fence_after();
+  const uint32_t sb = sh.stage(st);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint64_t bd = ptx::smem_desc(sb + 2048 * k, kKTileC, 1024, ptx::kSwizzle128);
+    ptx::mma_bf16_ts(tmem + kColO, tmem + kColP + 8 * k, bd, kIdescPV, (!first || k) ? 1u : 0u);
+  }
+  ptx::mma_commit(sh.bar(B_EMPTY0 + st));
+  ptx::mma_commit(sh.bar(B_PVDONE));
+  return true;
+}
+
+// MMA order: QK(0), QK(1), PV(0), QK(2), PV(1), ...: the scores of page n+1 exist before
+// the softmax of page n finishes, which the softmax pipeline relies on.
 __device__ void mma_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker) {
   const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
   int stage = 0;
   uint32_t wrap = 0, n = 0, q_iter = 0, item_idx = 0;
+  int prev_stage = 0;
+  bool prev_first = false;
+  uint32_t prev_item = 0;
   for (int it = it0; it < it1; ++it) {
     const WorkItem item = p.items[it];
-    if (!wait_bar(sh, sh.bar(B_QFULL), q_iter & 1, p.status)) return;
     for (int pg = item.page_begin; pg < item.page_end; ++pg) {
       const bool first = (pg == item.page_begin);
+      if (first && !wait_bar(sh, sh.bar(B_QFULL), q_iter & 1, p.status)) return;
       if (!wait_bar(sh, sh.bar(B_FULL0 + stage), wrap & 1, p.status)) return;
       if (!wait_bar(sh, sh.bar(B_SFREE), (n & 1) ^ 1, p.status)) return;
       ptx::tc_fence_after();
@@ -159,34 +183,57 @@ __device__ void mma_issuer(const Shared& sh, const DecodeParams& p, uint32_t tme
         ptx::mma_bf16_ss(tmem + kColS, a, bd, kIdescQK, 1u);
       }
       ptx::mma_commit(sh.bar(B_SFULL));
-      if (!wait_bar(sh, sh.bar(B_PFULL), n & 1, p.status)) return;
-      if (first && !wait_bar(sh, sh.bar(B_OFREE), (item_idx & 1) ^ 1, p.status)) return;
-      ptx::tc_fence_after();
-      // O_r += P C_r: P K-major (tokens contiguous), C_r MN-major (dims contiguous)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint64_t a = ptx::smem_desc(sh.pbuf() + 32 * k, 16, 1024, ptx::kSwizzle128);
-        const uint64_t bd = ptx::smem_desc(st + 2048 * k, kKTileC, 1024, ptx::kSwizzle128);
-        ptx::mma_bf16_ss(tmem + kColO, a, bd, kIdescPV, (!first || k) ? 1u : 0u);
+      if (pg == item.page_end - 1) {
+        ptx::mma_commit(sh.bar(B_QEMPTY));               // Q_r free once this QK is done
+        ++q_iter;
       }
-      ptx::mma_commit(sh.bar(B_EMPTY0 + stage));
-      ptx::mma_commit(sh.bar(B_PVDONE));
+      if (n > 0 && !issue_pv(sh, p, tmem, n - 1, prev_stage, prev_first, prev_item)) return;
+      prev_stage = stage;
+      prev_first = first;
+      prev_item = item_idx;
       ++n;
       if (++stage == kNS) {
         stage = 0;
         ++wrap;
       }
     }
-    ptx::mma_commit(sh.bar(B_QEMPTY));
-    ++q_iter;
     ++item_idx;
   }
+  if (n > 0) issue_pv(sh, p, tmem, n - 1, prev_stage, prev_first, prev_item);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b, float* sum) {
-  const bf16 x = __float2bfloat16_rn(a), y = __float2bfloat16_rn(b);
-  *sum += __bfloat162float(x) + __bfloat162float(y);
-  return (uint32_t)__bfloat16_as_ushort(x) | ((uint32_t)__bfloat16_as_ushort(y) << 16);
+// The softmax threads' view of this worker's pages, in processing order.
+struct PageCursor {
+  const DecodeParams* p;
+  int it, it1, pg;
+  WorkItem item;
+  __device__ void init(const DecodeParams& pp, int it0, int it_end) {
+    p = &pp;
+    it = it0;
+    it1 = it_end;
+    if (it < it1) {
+      item = p->items[it];
+      pg = item.page_begin;
+    }
+  }
+  __device__ bool valid() const { return it < it1; }
+  __device__ bool first() const { return pg == item.page_begin; }
+  __device__ bool last() const { return pg == item.page_end - 1; }
+  __device__ void next() {
+    if (++pg >= item.page_end) {
+      if (++it < it1) {
+        item = p->items[it];
+        pg = item.page_begin;
+      }
+    }
+  }
+};
+
+__device__ __forceinline__ void load_scores(const Shared& sh, uint32_t t_row, uint32_t (&sr)[64]) {
+  uint32_t* a = sr;
+  ptx::tmem_ld32(t_row + kColS, *reinterpret_cast<uint32_t(*)[32]>(a));
+  ptx::tmem_ld32(t_row + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
+  ptx::tmem_wait_ld();
 }
 
 __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker,
@@ -195,162 +242,189 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
   const int row = 32 * quarter + lane;                   // head index = TMEM lane
   const uint32_t t_row = tmem + ((uint32_t)(32 * quarter) << 16);
   const uint32_t peer = (uint32_t)(rank ^ 1);
-  const uint32_t peer_x = ptx::map_to_rank(sh.xbuf(), peer);
+  const uint32_t peer_xrow = ptx::map_to_rank(sh.xbuf(), peer) + row * 256;
   const uint32_t peer_xfull = ptx::map_to_rank(sh.bar(B_XFULL), peer);
   const uint32_t peer_xempty = ptx::map_to_rank(sh.bar(B_XEMPTY), peer);
   const float* xrow = reinterpret_cast<const float*>(sh.base + kOffX + row * 256);
-  uint8_t* prow = sh.base + kOffP + row * 128;
-  const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
+  const int sw = row & 7;
+  PageCursor cur, ahead;
+  cur.init(p, p.worker_off[worker], p.worker_off[worker + 1]);
+  ahead = cur;
+  if (!cur.valid()) return;
+  uint32_t sr[64];
+
+  // own partial of page 0 -> registers -> peer
+  auto fetch_and_send = [&](uint32_t n) -> bool {
+    if (!wait_bar(sh, sh.bar(B_SFULL), n & 1, p.status)) return false;
+    ptx::tc_fence_after();
+    load_scores(sh, t_row, sr);
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(sh.bar(B_SFREE));
+    if (!wait_bar(sh, sh.bar(B_XEMPTY), (n & 1) ^ 1, p.status, true)) return false;
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      ptx::st_async_v4(peer_xrow + (uint32_t)((c ^ sw) * 16), __uint_as_float(sr[4 * c]),
+                       __uint_as_float(sr[4 * c + 1]), __uint_as_float(sr[4 * c + 2]),
+                       __uint_as_float(sr[4 * c + 3]), peer_xfull);
+    return true;
+  };
+  if (!fetch_and_send(0)) return;
+  ahead.next();
+
   uint32_t n = 0;
-  for (int it = it0; it < it1; ++it) {
-    const WorkItem item = p.items[it];
-    const int g = item.group, b = g / p.q_len, kv = p.group_kv[g];
-    float m_used = -INFINITY, l = 0.f;
-    for (int pg = item.page_begin; pg < item.page_end; ++pg) {
-      const int page = p.block_table[(long long)b * p.max_pages + pg];
-      const bool valid = page >= 0 && page < p.num_pages;
-      if (!valid && row == 0 && rank == 0) flag_status(p.status, MLA_ERR_DEVICE_GUARD);
-      const int ntok = valid ? min(kP, kv - pg * kP) : 0;
-      // 1. own partial scores out of TMEM
-      if (!wait_bar(sh, sh.bar(B_SFULL), n & 1, p.status)) return;
-      ptx::tc_fence_after();
-      uint32_t sa[32], sb[32];
-      ptx::tmem_ld32(t_row + kColS, sa);
-      ptx::tmem_ld32(t_row + kColS + 32, sb);
-      ptx::tmem_wait_ld();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(sh.bar(B_SFREE));
-      // 2. swap partials with the peer CTA
-      if (!wait_bar(sh, sh.bar(B_XEMPTY), (n & 1) ^ 1, p.status, true)) return;
+  float m_used = -INFINITY, l = 0.f;
+  while (cur.valid()) {
+    const WorkItem item = cur.item;
+    const int pg = cur.pg;
+    const int g = item.group, b = g / p.q_len;
+    if (cur.first()) {
+      m_used = -INFINITY;
+      l = 0.f;
+    }
+    const int page = p.block_table[(long long)b * p.max_pages + pg];
+    const bool valid = page >= 0 && page < p.num_pages;
+    if (!valid && row == 0 && rank == 0) flag_status(p.status, MLA_ERR_DEVICE_GUARD);
+    const int ntok = valid ? min(kP, p.group_kv[g] - pg * kP) : 0;
+
+    // 1. the peer's partial of page n: s = own + peer
+    if (!wait_bar(sh, sh.bar(B_XFULL), n & 1, p.status, true)) return;
+    if (warp == 2 && lane == 0) ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL), kXBytes);
+    float s[64];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint32_t* src = (c < 8) ? &sa[4 * c] : &sb[4 * (c - 8)];
-        const uint32_t pos = (uint32_t)(c ^ (row & 7));
-        ptx::st_async_v4(peer_x + row * 256 + pos * 16, __uint_as_float(src[0]),
-                         __uint_as_float(src[1]), __uint_as_float(src[2]), __uint_as_float(src[3]),
-                         peer_xfull);
+    for (int c = 0; c < 16; ++c) {
+      const float4 v = *reinterpret_cast<const float4*>(xrow + 4 * (c ^ sw));
+      s[4 * c + 0] = __uint_as_float(sr[4 * c + 0]) + v.x;
+      s[4 * c + 1] = __uint_as_float(sr[4 * c + 1]) + v.y;
+      s[4 * c + 2] = __uint_as_float(sr[4 * c + 2]) + v.z;
+      s[4 * c + 3] = __uint_as_float(sr[4 * c + 3]) + v.w;
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive_remote(peer_xempty);
+
+    // 2. own partial of page n+1 (computed one page ahead by the MMA warp) -> peer
+    if (ahead.valid()) {
+      if (!fetch_and_send(n + 1)) return;
+      ahead.next();
+    }
+
+    // 3. softmax of page n. Rows past the last token (or a whole skipped page) may hold
+    // anything, NaN included, and 0 * NaN would poison O: zero them in the staged c_kv
+    // tiles before the P . C product reads them (the QK product that read them is done).
+    bool zeroed = false;
+    if (ntok < kP) {
+      uint8_t* stg = sh.base + kOffStage + (int)(n % kNS) * kStageBytes;
+      const int nrows = kP - ntok;
+      const int per_tile = nrows * 8;
+      for (int i = 32 * (warp - 2) + lane; i < 4 * per_tile; i += 128) {
+        const int tile = i / per_tile, rem = i % per_tile;
+        *reinterpret_cast<uint4*>(stg + tile * kKTileC + (ntok + rem / 8) * 128 + (rem % 8) * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
       }
-      if (!wait_bar(sh, sh.bar(B_XFULL), n & 1, p.status, true)) return;
-      if (warp == 2 && lane == 0) ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL), kXBytes);
-      float s[64];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const uint32_t pos = (uint32_t)(c ^ (row & 7));
-        const float4 v = *reinterpret_cast<const float4*>(xrow + pos * 4);
-        const uint32_t* src = (c < 8) ? &sa[4 * c] : &sb[4 * (c - 8)];
-        s[4 * c + 0] = __uint_as_float(src[0]) + v.x;
-        s[4 * c + 1] = __uint_as_float(src[1]) + v.y;
-        s[4 * c + 2] = __uint_as_float(src[2]) + v.z;
-        s[4 * c + 3] = __uint_as_float(src[3]) + v.w;
-      }
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive_remote(peer_xempty);
-      // Rows past the request's last token (or a whole skipped page) may hold anything,
-      // NaN included, and 0 * NaN would poison O: zero them in the staged c_kv tiles
-      // before the P . C product reads them (the QK product that read them is done).
-      if (ntok < kP) {
-        uint8_t* stg = sh.base + kOffStage + (int)(n % kNS) * kStageBytes;
-        const int nrows = kP - ntok;
-        const int per_tile = nrows * 8;                    // 16-byte chunks per tile
-        for (int i = 32 * (warp - 2) + lane; i < 4 * per_tile; i += 128) {
-          const int tile = i / per_tile, rem = i % per_tile;
-          *reinterpret_cast<uint4*>(stg + tile * kKTileC + (ntok + rem / 8) * 128 + (rem % 8) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-      // 3. online softmax in the log2 domain
-      float mx = -INFINITY;
+      for (int i = 0; i < 64; ++i)
+        if (i >= ntok) s[i] = -INFINITY;
+      zeroed = true;
+    }
+    float mx = s[0];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        s[i] = (i < ntok) ? s[i] * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[i]);
+    for (int i = 1; i < 64; ++i) mx = fmaxf(mx, s[i]);
+    mx *= p.scale_log2;
+    bool rescale = false;
+    float alpha = 1.f;
+    if (mx > -INFINITY) {
+      if (m_used == -INFINITY) {
+        m_used = mx;
+      } else if (mx > m_used + 8.f) {
+        alpha = ptx::ex2(m_used - mx);
+        m_used = mx;
+        l *= alpha;
+        rescale = true;
       }
-      bool rescale = false;
-      float alpha = 1.f;
-      if (mx > -INFINITY) {
-        if (m_used == -INFINITY) {
-          m_used = mx;
-        } else if (mx > m_used + 8.f) {
-          alpha = exp2f(m_used - mx);
-          m_used = mx;
-          l *= alpha;
-          rescale = true;
-        }
-      }
-      uint32_t packed[32];
+    }
+    uint32_t packed[32];
+    if (m_used == -INFINITY) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) packed[i] = 0u;
+    } else {
+      const float neg_m = -m_used;
       float psum = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float p0 = (s[2 * i] == -INFINITY) ? 0.f : exp2f(s[2 * i] - m_used);
-        const float p1 = (s[2 * i + 1] == -INFINITY) ? 0.f : exp2f(s[2 * i + 1] - m_used);
-        packed[i] = pack_bf16(p0, p1, &psum);
+        const float p0 = ptx::ex2(fmaf(s[2 * i], p.scale_log2, neg_m));
+        const float p1 = ptx::ex2(fmaf(s[2 * i + 1], p.scale_log2, neg_m));
+        psum += p0 + p1;
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+        packed[i] = *reinterpret_cast<const uint32_t*>(&h2);
       }
       l += psum;
-      // 4. the previous P . C product must be done before P or O are touched
-      if (n > 0 && !wait_bar(sh, sh.bar(B_PVDONE), (n - 1) & 1, p.status)) return;
-      ptx::tc_fence_after();
-      if (rescale) {
-#pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t v[32];
-          ptx::tmem_ld32(t_row + kColO + 32 * c, v);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-          ptx::tmem_st32(t_row + kColO + 32 * c, v);
-        }
-        ptx::tmem_wait_st();
-      }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t pos = (uint32_t)(c ^ (row & 7));
-        *reinterpret_cast<uint4*>(prow + pos * 16) =
-            make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-      }
-      ptx::fence_proxy_async_smem();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(sh.bar(B_PFULL));
-      ++n;
     }
-    // 5. epilogue: normalise O_r and write it (final output or split partial)
-    if (!wait_bar(sh, sh.bar(B_PVDONE), (n - 1) & 1, p.status)) return;
+    // the previous P . C product must be done before P or O are touched
+    if (n > 0 && !wait_bar(sh, sh.bar(B_PVDONE), (n - 1) & 1, p.status)) return;
     ptx::tc_fence_after();
-    const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
-    const float lse_v = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+    if (rescale) {
 #pragma unroll 1
-    for (int c = 0; c < 8; ++c) {
-      uint32_t v[32];
-      ptx::tmem_ld32(t_row + kColO + 32 * c, v);
-      ptx::tmem_wait_ld();
-      const int col = 256 * rank + 32 * c;
-      if (item.single) {
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out_latent) +
-                                              ((long long)g * kH + row) * kDC + col);
+      for (int c = 0; c < 8; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld32(t_row + kColO + 32 * c, v);
+        ptx::tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float dummy = 0.f;
-          dst[q] = make_uint4(pack_bf16(__uint_as_float(v[8 * q + 0]) * inv, __uint_as_float(v[8 * q + 1]) * inv, &dummy),
-                              pack_bf16(__uint_as_float(v[8 * q + 2]) * inv, __uint_as_float(v[8 * q + 3]) * inv, &dummy),
-                              pack_bf16(__uint_as_float(v[8 * q + 4]) * inv, __uint_as_float(v[8 * q + 5]) * inv, &dummy),
-                              pack_bf16(__uint_as_float(v[8 * q + 6]) * inv, __uint_as_float(v[8 * q + 7]) * inv, &dummy));
-        }
-      } else {
-        float4* dst = reinterpret_cast<float4*>(p.part_o + ((long long)it * kH + row) * kDC + col);
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
-                               __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+        ptx::tmem_st32(t_row + kColO + 32 * c, v);
       }
     }
+    ptx::tmem_st32(t_row + kColP, packed);
+    ptx::tmem_wait_st();
+    if (zeroed) ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(sh.bar(B_OFREE));
-    if (rank == 0) {
-      if (item.single) p.lse[(long long)g * kH + row] = lse_v;
-      else p.part_lse[(long long)it * kH + row] = lse_v;
+    if (lane == 0) ptx::mbar_arrive(sh.bar(B_PFULL));
+
+    // 4. after the item's last page: normalise O_r and write it (output or split partial)
+    if (cur.last()) {
+      const int it = cur.it;
+      if (!wait_bar(sh, sh.bar(B_PVDONE), n & 1, p.status)) return;
+      ptx::tc_fence_after();
+      const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
+      const float lse_v = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 8; ++c) {
+        uint32_t v[32];
+        ptx::tmem_ld32(t_row + kColO + 32 * c, v);
+        ptx::tmem_wait_ld();
+        const int col = 256 * rank + 32 * c;
+        if (item.single) {
+          uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out_latent) +
+                                                ((long long)g * kH + row) * kDC + col);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * j]) * inv,
+                                                              __uint_as_float(v[8 * q + 2 * j + 1]) * inv);
+              w[j] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(p.part_o + ((long long)it * kH + row) * kDC + col);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
+                                 __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(sh.bar(B_OFREE));
+      if (rank == 0) {
+        if (item.single) p.lse[(long long)g * kH + row] = lse_v;
+        else p.part_lse[(long long)it * kH + row] = lse_v;
+      }
     }
+    ++n;
+    cur.next();
   }
 }
 
@@ -372,10 +446,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int worker = blockIdx.x >> 1;
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(sh.bar(B_FULL0 + 0), 1);
-    ptx::mbar_init(sh.bar(B_FULL0 + 1), 1);
-    ptx::mbar_init(sh.bar(B_EMPTY0 + 0), 1);
-    ptx::mbar_init(sh.bar(B_EMPTY0 + 1), 1);
+    for (int s = 0; s < kNS; ++s) {
+      ptx::mbar_init(sh.bar(B_FULL0 + s), 1);
+      ptx::mbar_init(sh.bar(B_EMPTY0 + s), 1);
+    }
     ptx::mbar_init(sh.bar(B_QFULL), 1);
     ptx::mbar_init(sh.bar(B_QEMPTY), 1);
     ptx::mbar_init(sh.bar(B_SFULL), 1);
