@@ -11,20 +11,26 @@
 // [512+32r, 512+32r+32). Per 64-token page each CTA
 //   1. TMA-loads only its 288-column slice of the page (36 KB; the pair reads each byte of
 //      the page once) into a 3-stage ring,
-//   2. computes a partial score S_r = Q_r K_r^T (M = 128 heads, N = 64 tokens, K = 288)
-//      into TMEM,
-//   3. sends S_r to the peer over distributed shared memory (st.async, counted on the
-//      peer's mbarrier) and adds the peer's partial: both CTAs hold the same full S,
+//   2. computes a partial score S_r = Q_r K_r^T (M = 128 heads, N = 64 tokens, K = 288;
+//      A = Q_r held in TMEM, B = the staged page slice) into TMEM,
+//   3. sends S_r to the peer over distributed shared memory (each softmax warp writes its
+//      32 rows to a local staging buffer and one bulk copy per warp moves them into one of
+//      the peer's two receive buffers, counted on the peer's mbarrier) and adds the peer's
+//      partial: both CTAs hold the same full S,
 //   4. runs the online softmax (one thread per head row, exp2, O rescaled lazily, only
 //      when the running maximum grows by more than 2^8),
 //   5. writes P (bf16) into TMEM and accumulates O_r += P C_r (M = 128, N = 256, K = 64;
 //      A = P from TMEM, B = the staged page slice) in TMEM.
+// TMEM: O_r 256 columns, S 64, P 32, Q_r 144 (288 bf16 per head row).
 // The softmax threads pipeline pages: for page n they first take the peer's partial,
 // then read and ship their own partial of page n+1 (whose scores the MMA warp computed
-// one page ahead), and only then do page n's softmax, so the cluster exchange of one page
-// overlaps the arithmetic of the previous one.
-// Roles: warp 0 issues TMA, warp 1 issues MMAs (one thread) and owns the TMEM
-// allocation, warps 2-5 run the softmax and the epilogue (thread = head row = TMEM lane).
+// one page ahead), and only then do page n's softmax; with two receive buffers a send
+// waits only for the peer to have read the partial of two pages before, so the cluster
+// exchange overlaps the arithmetic of the previous page.
+// Roles: warp 0 issues TMA; warp 1 issues the score MMAs (one thread, running ahead as
+// soon as a page lands) and owns the TMEM allocation; warp 6 issues the P.C MMAs; warps
+// 2-5 run the softmax, load Q_r into TMEM at each work item's start and write the outputs
+// (thread = head row = TMEM lane).
 // Every mbarrier wait is bounded (2 s): on timeout the kernel records MLA_ERR_TIMEOUT,
 // every role leaves its loop, TMEM is freed and the pair meets at a final cluster
 // barrier before exit.
@@ -39,33 +45,31 @@ namespace tc {
 
 constexpr int kH = 128, kDC = 512, kDR = 64, kD = 576, kP = 64;
 constexpr int kNS = 3;                                   // cache-page pipeline stages
-constexpr int kQTileC = 128 * 64 * 2;                    // one 64-dim SW128 chunk of Q_r
-constexpr int kQTilePE = 128 * 32 * 2;                   // the 32-dim SW64 k_pe half of Q_r
-constexpr int kQBytes = 4 * kQTileC + kQTilePE;          // 73728
 constexpr int kKTileC = 64 * 64 * 2;                     // one 64-dim SW128 chunk of a page
 constexpr int kKTilePE = 64 * 32 * 2;                    // the 32-dim SW64 k_pe half
 constexpr int kStageBytes = 4 * kKTileC + kKTilePE;      // 36864
-constexpr int kXBytes = 128 * 64 * 4;                    // peer partial scores, fp32
-constexpr int kOffQ = 0;
-constexpr int kOffStage = kOffQ + kQBytes;
-constexpr int kOffX = kOffStage + kNS * kStageBytes;
-constexpr int kOffBar = kOffX + kXBytes;
+constexpr int kXBytes = 128 * 64 * 4;                    // one partial-score buffer, fp32
+constexpr int kOffStage = 0;
+constexpr int kOffX = kOffStage + kNS * kStageBytes;     // two receive buffers
+constexpr int kOffStg = kOffX + 2 * kXBytes;             // own partial, staged for the copy
+constexpr int kOffBar = kOffStg + kXBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;         // + slack to align the base to 1 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;                            // O_r: 256 fp32 columns
 constexpr uint32_t kColS = 256;                          // S: 64 fp32 columns
 constexpr uint32_t kColP = 320;                          // P: 64 bf16 = 32 columns
-constexpr int kThreads = 192;
+constexpr uint32_t kColQ = 352;                          // Q_r: 288 bf16 = 144 columns
+constexpr int kThreads = 224;
 constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, 256, false, true);
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 // mbarrier slots (8 bytes each) at kOffBar
 enum {
-  B_FULL0 = 0, B_EMPTY0 = kNS, B_QFULL = 2 * kNS, B_QEMPTY, B_SFULL, B_SFREE, B_PFULL, B_PVDONE,
-  B_XFULL, B_XEMPTY, B_OFREE, B_TEARDOWN, B_COUNT
+  B_FULL0 = 0, B_EMPTY0 = kNS, B_QFULL = 2 * kNS, B_SFULL, B_SFREE, B_PFULL, B_PVDONE,
+  B_XFULL0, B_XFULL1, B_XEMPTY0, B_XEMPTY1, B_OFREE, B_TEARDOWN, B_COUNT
 };
-static_assert(B_COUNT * 8 <= 128, "barrier area");
+static_assert(B_COUNT * 8 <= 160, "barrier area");
 
 struct Shared {
   uint8_t* base;       // 1 KB aligned
@@ -73,9 +77,9 @@ struct Shared {
   volatile int* abort;
   uint32_t* tmem_slot;
   __device__ uint32_t bar(int i) const { return base_u32 + kOffBar + 8 * i; }
-  __device__ uint32_t q() const { return base_u32 + kOffQ; }
   __device__ uint32_t stage(int s) const { return base_u32 + kOffStage + s * kStageBytes; }
-  __device__ uint32_t xbuf() const { return base_u32 + kOffX; }
+  __device__ uint32_t xbuf(int j) const { return base_u32 + kOffX + j * kXBytes; }
+  __device__ uint32_t stg() const { return base_u32 + kOffStg; }
 };
 
 __device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_t parity,
@@ -98,21 +102,13 @@ __device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_
 
 // ------------------------------------------------------------------------------- roles
 __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensorMap* tm_kc,
-                         const CUtensorMap* tm_kpe, const CUtensorMap* tm_qc,
-                         const CUtensorMap* tm_qpe, int worker, int rank) {
+                         const CUtensorMap* tm_kpe, int worker, int rank) {
   const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
   int stage = 0;
-  uint32_t wrap = 0, q_iter = 0;
+  uint32_t wrap = 0;
   for (int it = it0; it < it1; ++it) {
     const WorkItem item = p.items[it];
-    const int g = item.group, b = g / p.q_len;
-    if (!wait_bar(sh, sh.bar(B_QEMPTY), (q_iter & 1) ^ 1, p.status)) return;
-    ptx::mbar_arrive_expect_tx(sh.bar(B_QFULL), kQBytes);
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      ptx::tma_load_2d(sh.q() + c * kQTileC, tm_qc, 256 * rank + 64 * c, g * kH, sh.bar(B_QFULL));
-    ptx::tma_load_2d(sh.q() + 4 * kQTileC, tm_qpe, kDC + 32 * rank, g * kH, sh.bar(B_QFULL));
-    ++q_iter;
+    const int b = item.group / p.q_len;
     for (int pg = item.page_begin; pg < item.page_end; ++pg) {
       int page = p.block_table[(long long)b * p.max_pages + pg];
       if (page < 0 || page >= p.num_pages) page = 0;      // masked by the softmax side
@@ -131,66 +127,33 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
   }
 }
 
-// O_r += P C_r for global page m (stage `st`); `first` = the item's first page.
-__device__ __forceinline__ bool issue_pv(const Shared& sh, const DecodeParams& p, uint32_t tmem,
-                                         uint32_t m, int st, bool first, uint32_t item_idx) {
-  if (!wait_bar(sh, sh.bar(B_PFULL), m & 1, p.status)) return false;
-  if (first && !wait_bar(sh, sh.bar(B_OFREE), (item_idx & 1) ^ 1, p.status)) return false;
-  ptx::tc_fence_after();
-  const uint32_t sb = sh.stage(st);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint64_t bd = ptx::smem_desc(sb + 2048 * k, kKTileC, 1024, ptx::kSwizzle128);
-    ptx::mma_bf16_ts(tmem + kColO, tmem + kColP + 8 * k, bd, kIdescPV, (!first || k) ? 1u : 0u);
-  }
-  ptx::mma_commit(sh.bar(B_EMPTY0 + st));
-  ptx::mma_commit(sh.bar(B_PVDONE));
-  return true;
-}
-
-// MMA order: QK(0), QK(1), PV(0), QK(2), PV(1), ...: the scores of page n+1 exist before
-// the softmax of page n finishes, which the softmax pipeline relies on.
-__device__ void mma_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker) {
+// Score MMAs: S = Q_r K_r^T for every page in order, as soon as the page has landed and the
+// softmax has read the previous scores (S has one TMEM buffer).
+__device__ void qk_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker) {
   const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
   int stage = 0;
-  uint32_t wrap = 0, n = 0, q_iter = 0, item_idx = 0;
-  int prev_stage = 0;
-  bool prev_first = false;
-  uint32_t prev_item = 0;
+  uint32_t wrap = 0, n = 0, item_idx = 0;
   for (int it = it0; it < it1; ++it) {
     const WorkItem item = p.items[it];
     for (int pg = item.page_begin; pg < item.page_end; ++pg) {
-      const bool first = (pg == item.page_begin);
-      if (first && !wait_bar(sh, sh.bar(B_QFULL), q_iter & 1, p.status)) return;
+      if (pg == item.page_begin && !wait_bar(sh, sh.bar(B_QFULL), item_idx & 1, p.status)) return;
       if (!wait_bar(sh, sh.bar(B_FULL0 + stage), wrap & 1, p.status)) return;
       if (!wait_bar(sh, sh.bar(B_SFREE), (n & 1) ^ 1, p.status)) return;
       ptx::tc_fence_after();
       const uint32_t st = sh.stage(stage);
-      // S = Q_r K_r^T over the CTA's 256 c_kv dims (SW128) and 32 k_pe dims (SW64)
+      // Q_r from TMEM; the CTA's 256 c_kv dims (SW128) and 32 k_pe dims (SW64) from the page
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t a = ptx::smem_desc(sh.q() + c * kQTileC + 32 * k, 16, 1024, ptx::kSwizzle128);
-          const uint64_t bd = ptx::smem_desc(st + c * kKTileC + 32 * k, 16, 1024, ptx::kSwizzle128);
-          ptx::mma_bf16_ss(tmem + kColS, a, bd, kIdescQK, (c | k) ? 1u : 0u);
-        }
+      for (int j = 0; j < 16; ++j) {
+        const uint64_t bd = ptx::smem_desc(st + (j >> 2) * kKTileC + 32 * (j & 3), 16, 1024,
+                                           ptx::kSwizzle128);
+        ptx::mma_bf16_ts(tmem + kColS, tmem + kColQ + 8 * j, bd, kIdescQK, j ? 1u : 0u);
       }
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const uint64_t a = ptx::smem_desc(sh.q() + 4 * kQTileC + 32 * k, 16, 512, ptx::kSwizzle64);
         const uint64_t bd = ptx::smem_desc(st + 4 * kKTileC + 32 * k, 16, 512, ptx::kSwizzle64);
-        ptx::mma_bf16_ss(tmem + kColS, a, bd, kIdescQK, 1u);
+        ptx::mma_bf16_ts(tmem + kColS, tmem + kColQ + 128 + 8 * k, bd, kIdescQK, 1u);
       }
       ptx::mma_commit(sh.bar(B_SFULL));
-      if (pg == item.page_end - 1) {
-        ptx::mma_commit(sh.bar(B_QEMPTY));               // Q_r free once this QK is done
-        ++q_iter;
-      }
-      if (n > 0 && !issue_pv(sh, p, tmem, n - 1, prev_stage, prev_first, prev_item)) return;
-      prev_stage = stage;
-      prev_first = first;
-      prev_item = item_idx;
       ++n;
       if (++stage == kNS) {
         stage = 0;
@@ -199,7 +162,34 @@ __device__ void mma_issuer(const Shared& sh, const DecodeParams& p, uint32_t tme
     }
     ++item_idx;
   }
-  if (n > 0) issue_pv(sh, p, tmem, n - 1, prev_stage, prev_first, prev_item);
+}
+
+// Output MMAs: O_r += P C_r for every page once its P is in TMEM. The page's score MMA
+// finished before its P existed, so the stage is free once this product is done.
+__device__ void pv_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker) {
+  const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
+  int stage = 0;
+  uint32_t n = 0, item_idx = 0;
+  for (int it = it0; it < it1; ++it) {
+    const WorkItem item = p.items[it];
+    for (int pg = item.page_begin; pg < item.page_end; ++pg) {
+      const bool first = (pg == item.page_begin);
+      if (!wait_bar(sh, sh.bar(B_PFULL), n & 1, p.status)) return;
+      if (first && !wait_bar(sh, sh.bar(B_OFREE), (item_idx & 1) ^ 1, p.status)) return;
+      ptx::tc_fence_after();
+      const uint32_t sb = sh.stage(stage);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint64_t bd = ptx::smem_desc(sb + 2048 * k, kKTileC, 1024, ptx::kSwizzle128);
+        ptx::mma_bf16_ts(tmem + kColO, tmem + kColP + 8 * k, bd, kIdescPV, (!first || k) ? 1u : 0u);
+      }
+      ptx::mma_commit(sh.bar(B_EMPTY0 + stage));
+      ptx::mma_commit(sh.bar(B_PVDONE));
+      ++n;
+      if (++stage == kNS) stage = 0;
+    }
+    ++item_idx;
+  }
 }
 
 // The softmax threads' view of this worker's pages, in processing order.
@@ -236,16 +226,51 @@ __device__ __forceinline__ void load_scores(const Shared& sh, uint32_t t_row, ui
   ptx::tmem_wait_ld();
 }
 
+// Q_r of one head row (group g) into TMEM: 256 c dims then 32 k_pe dims, two bf16 per column.
+__device__ __forceinline__ void store_q(const DecodeParams& p, uint32_t t_row, int g, int row,
+                                        int rank) {
+  const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(p.q_lat) +
+                                                    ((long long)g * kH + row) * kD);
+  uint4 cur[8], nxt[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) cur[i] = src[32 * rank + i];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    if (c < 3) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) nxt[i] = src[32 * rank + 8 * (c + 1) + i];
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) nxt[i] = src[64 + 4 * rank + i];
+    }
+    uint32_t v[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[4 * i] = cur[i].x; v[4 * i + 1] = cur[i].y; v[4 * i + 2] = cur[i].z; v[4 * i + 3] = cur[i].w;
+    }
+    ptx::tmem_st32(t_row + kColQ + 32 * c, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
+  }
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    w[4 * i] = cur[i].x; w[4 * i + 1] = cur[i].y; w[4 * i + 2] = cur[i].z; w[4 * i + 3] = cur[i].w;
+  }
+  ptx::tmem_st16(t_row + kColQ + 128, w);
+  ptx::tmem_wait_st();
+}
+
 __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker,
                                  int rank, int warp, int lane) {
   const int quarter = warp & 3;
   const int row = 32 * quarter + lane;                   // head index = TMEM lane
   const uint32_t t_row = tmem + ((uint32_t)(32 * quarter) << 16);
   const uint32_t peer = (uint32_t)(rank ^ 1);
-  const uint32_t peer_xrow = ptx::map_to_rank(sh.xbuf(), peer) + row * 256;
-  const uint32_t peer_xfull = ptx::map_to_rank(sh.bar(B_XFULL), peer);
-  const uint32_t peer_xempty = ptx::map_to_rank(sh.bar(B_XEMPTY), peer);
-  const float* xrow = reinterpret_cast<const float*>(sh.base + kOffX + row * 256);
+  const uint32_t peer_x0 = ptx::map_to_rank(sh.xbuf(0), peer);
+  uint8_t* stg_row = sh.base + kOffStg + row * 256;
+  const uint32_t peer_xfull0 = ptx::map_to_rank(sh.bar(B_XFULL0), peer);
+  const uint32_t peer_xempty0 = ptx::map_to_rank(sh.bar(B_XEMPTY0), peer);
   const int sw = row & 7;
   PageCursor cur, ahead;
   cur.init(p, p.worker_off[worker], p.worker_off[worker + 1]);
@@ -253,22 +278,52 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
   if (!cur.valid()) return;
   uint32_t sr[64];
 
-  // own partial of page 0 -> registers -> peer
+  auto publish_q = [&](int g) {
+    store_q(p, t_row, g, row, rank);
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(sh.bar(B_QFULL));
+  };
+  // own partial of page n -> registers -> local staging -> (bulk copy) the peer's receive
+  // buffer n & 1
   auto fetch_and_send = [&](uint32_t n) -> bool {
     if (!wait_bar(sh, sh.bar(B_SFULL), n & 1, p.status)) return false;
     ptx::tc_fence_after();
     load_scores(sh, t_row, sr);
     ptx::tc_fence_before();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(sh.bar(B_SFREE));
-    if (!wait_bar(sh, sh.bar(B_XEMPTY), (n & 1) ^ 1, p.status, true)) return false;
+    if (lane == 0) {
+      ptx::mbar_arrive(sh.bar(B_SFREE));
+      ptx::bulk_wait_read_all();                 // the previous copy has read the staging rows
+    }
+    __syncwarp();
 #pragma unroll
     for (int c = 0; c < 16; ++c)
-      ptx::st_async_v4(peer_xrow + (uint32_t)((c ^ sw) * 16), __uint_as_float(sr[4 * c]),
-                       __uint_as_float(sr[4 * c + 1]), __uint_as_float(sr[4 * c + 2]),
-                       __uint_as_float(sr[4 * c + 3]), peer_xfull);
-    return true;
+      *reinterpret_cast<uint4*>(stg_row + ((c ^ sw) * 16)) =
+          make_uint4(sr[4 * c], sr[4 * c + 1], sr[4 * c + 2], sr[4 * c + 3]);
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    const uint32_t j = n & 1;
+    int ok = 1;
+    if (lane == 0) {
+      ok = wait_bar(sh, sh.bar(B_XEMPTY0 + j), ((n >> 1) & 1) ^ 1, p.status, true) ? 1 : 0;
+      if (ok) {
+        ptx::bulk_s2s(peer_x0 + j * kXBytes + quarter * 8192, sh.stg() + quarter * 8192, 8192,
+                      peer_xfull0 + 8 * j);
+        ptx::bulk_commit();
+      }
+    }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
   };
+  // block-table entry and key count of a page, loaded one page before they are used
+  auto load_meta = [&](const PageCursor& c, int* page, int* kv) {
+    const int gg = c.item.group;
+    *page = p.block_table[(long long)(gg / p.q_len) * p.max_pages + c.pg];
+    *kv = p.group_kv[gg];
+  };
+  int page_cur = 0, kv_cur = 0, page_nxt = 0, kv_nxt = 0;
+  load_meta(cur, &page_cur, &kv_cur);
+  publish_q(cur.item.group);
   if (!fetch_and_send(0)) return;
   ahead.next();
 
@@ -277,19 +332,19 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
   while (cur.valid()) {
     const WorkItem item = cur.item;
     const int pg = cur.pg;
-    const int g = item.group, b = g / p.q_len;
+    const int g = item.group;
     if (cur.first()) {
       m_used = -INFINITY;
       l = 0.f;
     }
-    const int page = p.block_table[(long long)b * p.max_pages + pg];
-    const bool valid = page >= 0 && page < p.num_pages;
-    if (!valid && row == 0 && rank == 0) flag_status(p.status, MLA_ERR_DEVICE_GUARD);
-    const int ntok = valid ? min(kP, p.group_kv[g] - pg * kP) : 0;
+    const bool valid = page_cur >= 0 && page_cur < p.num_pages;
+    const int ntok = valid ? min(kP, kv_cur - pg * kP) : 0;
 
-    // 1. the peer's partial of page n: s = own + peer
-    if (!wait_bar(sh, sh.bar(B_XFULL), n & 1, p.status, true)) return;
-    if (warp == 2 && lane == 0) ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL), kXBytes);
+    // 1. the peer's partial of page n (receive buffer n & 1): s = own + peer
+    const uint32_t jx = n & 1;
+    if (!wait_bar(sh, sh.bar(B_XFULL0 + jx), (n >> 1) & 1, p.status, true)) return;
+    if (warp == 2 && lane == 0) ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL0 + jx), kXBytes);
+    const float* xrow = reinterpret_cast<const float*>(sh.base + kOffX + jx * kXBytes + row * 256);
     float s[64];
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
@@ -299,14 +354,25 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
       s[4 * c + 2] = __uint_as_float(sr[4 * c + 2]) + v.z;
       s[4 * c + 3] = __uint_as_float(sr[4 * c + 3]) + v.w;
     }
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive_remote(peer_xempty);
+    {
+      // every lane's buffer reads have returned before lane 0 tells the peer it may refill
+      uint32_t dep = 0;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) dep ^= __float_as_uint(s[4 * c]);
+      const uint32_t all = __ballot_sync(0xffffffffu, dep != 0x7fc00001u);
+      if (lane == 0) ptx::mbar_arrive_remote_relaxed(peer_xempty0 + 8 * jx, all);
+    }
 
-    // 2. own partial of page n+1 (computed one page ahead by the MMA warp) -> peer
+    // 2. own partial of page n+1 (computed one page ahead by the MMA warp) -> peer; a page
+    // that opens the next work item needs that item's Q_r in TMEM first (every QK of the
+    // current item is done: its last scores, page n's, are already read)
     if (ahead.valid()) {
+      if (ahead.first()) publish_q(ahead.item.group);
+      load_meta(ahead, &page_nxt, &kv_nxt);
       if (!fetch_and_send(n + 1)) return;
       ahead.next();
     }
+    if (!valid && row == 0 && rank == 0) flag_status(p.status, MLA_ERR_DEVICE_GUARD);
 
     // 3. softmax of page n. Rows past the last token (or a whole skipped page) may hold
     // anything, NaN included, and 0 * NaN would poison O: zero them in the staged c_kv
@@ -425,22 +491,22 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
     }
     ++n;
     cur.next();
+    page_cur = page_nxt;
+    kv_cur = kv_nxt;
   }
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
-                     const __grid_constant__ CUtensorMap tm_kpe,
-                     const __grid_constant__ CUtensorMap tm_qc,
-                     const __grid_constant__ CUtensorMap tm_qpe, const DecodeParams p) {
+                     const __grid_constant__ CUtensorMap tm_kpe, const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   Shared sh;
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t aligned = (raw + 1023u) & ~1023u;
   sh.base = smem_raw + (aligned - raw);
   sh.base_u32 = aligned;
-  sh.abort = reinterpret_cast<volatile int*>(sh.base + kOffBar + 128);
-  sh.tmem_slot = reinterpret_cast<uint32_t*>(sh.base + kOffBar + 136);
+  sh.abort = reinterpret_cast<volatile int*>(sh.base + kOffBar + 160);
+  sh.tmem_slot = reinterpret_cast<uint32_t*>(sh.base + kOffBar + 168);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (int)ptx::cluster_ctarank();
   const int worker = blockIdx.x >> 1;
@@ -450,23 +516,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_init(sh.bar(B_FULL0 + s), 1);
       ptx::mbar_init(sh.bar(B_EMPTY0 + s), 1);
     }
-    ptx::mbar_init(sh.bar(B_QFULL), 1);
-    ptx::mbar_init(sh.bar(B_QEMPTY), 1);
+    ptx::mbar_init(sh.bar(B_QFULL), 4);
     ptx::mbar_init(sh.bar(B_SFULL), 1);
     ptx::mbar_init(sh.bar(B_SFREE), 4);
     ptx::mbar_init(sh.bar(B_PFULL), 4);
     ptx::mbar_init(sh.bar(B_PVDONE), 1);
-    ptx::mbar_init(sh.bar(B_XFULL), 1);
-    ptx::mbar_init(sh.bar(B_XEMPTY), 4);
+    ptx::mbar_init(sh.bar(B_XFULL0), 1);
+    ptx::mbar_init(sh.bar(B_XFULL1), 1);
+    ptx::mbar_init(sh.bar(B_XEMPTY0), 4);
+    ptx::mbar_init(sh.bar(B_XEMPTY1), 4);
     ptx::mbar_init(sh.bar(B_OFREE), 4);
-    ptx::mbar_init(sh.bar(B_TEARDOWN), 1);
+    ptx::mbar_init(sh.bar(B_TEARDOWN), 2);
     *sh.abort = 0;
     ptx::fence_mbar_init();
-    ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL), kXBytes);   // phase 0 of the peer's sends
+    // first phase of each receive buffer (the peer's partials of pages 0 and 1)
+    ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL0), kXBytes);
+    ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL1), kXBytes);
     ptx::prefetch_tensormap(&tm_kc);
     ptx::prefetch_tensormap(&tm_kpe);
-    ptx::prefetch_tensormap(&tm_qc);
-    ptx::prefetch_tensormap(&tm_qpe);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(sh.tmem_slot), kTmemCols);
@@ -479,19 +546,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *sh.tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) producer(sh, p, &tm_kc, &tm_kpe, &tm_qc, &tm_qpe, worker, rank);
+    if (lane == 0) producer(sh, p, &tm_kc, &tm_kpe, worker, rank);
   } else if (warp == 1) {
-    if (lane == 0) mma_issuer(sh, p, tmem, worker);
+    if (lane == 0) qk_issuer(sh, p, tmem, worker);
+  } else if (warp == 6) {
+    if (lane == 0) pv_issuer(sh, p, tmem, worker);
   } else {
     softmax_epilogue(sh, p, tmem, worker, rank, warp, lane);
   }
 
   // teardown: every role gets here, normally or after a bounded wait gave up
+  // both MMA issuers commit: every issued MMA must have finished before TMEM is released
+  if ((warp == 1 || warp == 6) && lane == 0) ptx::mma_commit(sh.bar(B_TEARDOWN));
+  if (warp >= 2 && warp <= 5 && lane == 0) ptx::bulk_wait_read_all();
   __syncthreads();
   if (warp == 1) {
     if (lane == 0) {
-      // every issued MMA must have finished before TMEM is released
-      ptx::mma_commit(sh.bar(B_TEARDOWN));
       const uint64_t t0 = ptx::globaltimer();
       while (!ptx::mbar_try_wait(sh.bar(B_TEARDOWN), 0) && ptx::globaltimer() - t0 < kTimeoutNs) {
       }
@@ -577,18 +647,15 @@ int tc_decode_max_workers() {
 
 cudaError_t launch_decode_tc(mla_dtype cache, const DecodeParams& p, cudaStream_t s) {
   if (cache != MLA_BF16) return cudaErrorNotSupported;
-  CUtensorMap kc, kpe, qc, qpe;
+  CUtensorMap kc, kpe;
   const uint64_t cache_rows = (uint64_t)p.num_pages * tc::kP;
-  const uint64_t q_rows = (uint64_t)p.batch * p.q_len * tc::kH;
   if (!tc::make_map(&kc, p.cache, cache_rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tc::make_map(&kpe, p.cache, cache_rows, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !tc::make_map(&qc, p.q_lat, q_rows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tc::make_map(&qpe, p.q_lat, q_rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+      !tc::make_map(&kpe, p.cache, cache_rows, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(tc::decode_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
   if (e != cudaSuccess) return e;
-  tc::decode_tc_kernel<<<2 * p.workers, tc::kThreads, tc::kSmemBytes, s>>>(kc, kpe, qc, qpe, p);
+  tc::decode_tc_kernel<<<2 * p.workers, tc::kThreads, tc::kSmemBytes, s>>>(kc, kpe, p);
   note_launch();
   return cudaGetLastError();
 }
