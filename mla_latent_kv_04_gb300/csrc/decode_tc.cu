@@ -10,13 +10,15 @@
 // the latent dimensions: CTA r owns c_kv dims [256r, 256r+256) and k_pe dims
 // [512+32r, 512+32r+32). Per 64-token page each CTA
 //   1. TMA-loads only its 288-column slice of the page (36 KB; the pair reads each byte of
-//      the page once) into a 3-stage ring,
+//      the page once) into a 4-stage ring,
 //   2. computes a partial score S_r = Q_r K_r^T (M = 128 heads, N = 64 tokens, K = 288;
 //      A = Q_r held in TMEM, B = the staged page slice) into TMEM,
-//   3. sends S_r to the peer over distributed shared memory (each softmax warp writes its
-//      32 rows to a local staging buffer and one bulk copy per warp moves them into one of
-//      the peer's two receive buffers, counted on the peer's mbarrier) and adds the peer's
-//      partial: both CTAs hold the same full S,
+//   3. sends S_r, rounded to fp16, to the peer over distributed shared memory (each
+//      softmax warp writes its 32 half-rows to a local staging buffer and one 2 KB bulk
+//      copy per warp moves them into one of the peer's two receive buffers, counted on the
+//      peer's mbarrier); both CTAs then use the same S = f16(S_0) + f16(S_1) in fp32.
+//      The fp16 rounding of a partial (relative 2^-11) is below the bf16 rounding of P,
+//      and halves the cluster traffic and the buffers, which buys the 4th page stage,
 //   4. runs the online softmax (one thread per head row, exp2, O rescaled lazily, only
 //      when the running maximum grows by more than 2^8),
 //   5. writes P (bf16) into TMEM and accumulates O_r += P C_r (M = 128, N = 256, K = 64;
@@ -28,12 +30,16 @@
 // waits only for the peer to have read the partial of two pages before, so the cluster
 // exchange overlaps the arithmetic of the previous page.
 // Roles: warp 0 issues TMA; warp 1 issues the score MMAs (one thread, running ahead as
-// soon as a page lands) and owns the TMEM allocation; warp 6 issues the P.C MMAs; warps
-// 2-5 run the softmax, load Q_r into TMEM at each work item's start and write the outputs
-// (thread = head row = TMEM lane).
+// soon as a page lands) and owns the TMEM allocation; warp 10 issues the P.C MMAs; warps
+// 2-9 run the softmax, load Q_r into TMEM at each work item's start and write the
+// outputs. Each head row (= TMEM lane) has two softmax threads, in warps w and w+4 (same
+// TMEM quarter): one owns score columns 0-31 and output dims 0-127 of the CTA's slice,
+// the other columns 32-63 and dims 128-255; they combine the row maximum every page and
+// the row sum once per work item through shared memory.
 // Every mbarrier wait is bounded (2 s): on timeout the kernel records MLA_ERR_TIMEOUT,
 // every role leaves its loop, TMEM is freed and the pair meets at a final cluster
 // barrier before exit.
+#include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -44,22 +50,25 @@ namespace mla {
 namespace tc {
 
 constexpr int kH = 128, kDC = 512, kDR = 64, kD = 576, kP = 64;
-constexpr int kNS = 3;                                   // cache-page pipeline stages
+constexpr int kNS = 4;                                   // cache-page pipeline stages
 constexpr int kKTileC = 64 * 64 * 2;                     // one 64-dim SW128 chunk of a page
 constexpr int kKTilePE = 64 * 32 * 2;                    // the 32-dim SW64 k_pe half
 constexpr int kStageBytes = 4 * kKTileC + kKTilePE;      // 36864
-constexpr int kXBytes = 128 * 64 * 4;                    // one partial-score buffer, fp32
+constexpr int kXBytes = 128 * 64 * 2;                    // one partial-score buffer, fp16
+constexpr int kXHalf = kXBytes / 2;                      // [half][128 rows][32 scores]
 constexpr int kOffStage = 0;
 constexpr int kOffX = kOffStage + kNS * kStageBytes;     // two receive buffers
 constexpr int kOffStg = kOffX + 2 * kXBytes;             // own partial, staged for the copy
-constexpr int kOffBar = kOffStg + kXBytes;
+constexpr int kOffRed = kOffStg + kXBytes;               // row max halves [2][2][128] fp32
+constexpr int kOffLsum = kOffRed + 2048;                 // row sum halves [2][2][128] fp32
+constexpr int kOffBar = kOffLsum + 2048;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;         // + slack to align the base to 1 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;                            // O_r: 256 fp32 columns
 constexpr uint32_t kColS = 256;                          // S: 64 fp32 columns
 constexpr uint32_t kColP = 320;                          // P: 64 bf16 = 32 columns
 constexpr uint32_t kColQ = 352;                          // Q_r: 288 bf16 = 144 columns
-constexpr int kThreads = 224;
+constexpr int kThreads = 352;                            // 11 warps
 constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, 256, false, true);
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -67,9 +76,11 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 // mbarrier slots (8 bytes each) at kOffBar
 enum {
   B_FULL0 = 0, B_EMPTY0 = kNS, B_QFULL = 2 * kNS, B_SFULL, B_SFREE, B_PFULL, B_PVDONE,
-  B_XFULL0, B_XFULL1, B_XEMPTY0, B_XEMPTY1, B_OFREE, B_TEARDOWN, B_COUNT
+  B_XFULL0, B_XFULL1, B_XEMPTY0, B_XEMPTY1, B_OFREE, B_TEARDOWN, B_RMAX0, B_RMAX1, B_LSUM0,
+  B_LSUM1, B_COUNT
 };
-static_assert(B_COUNT * 8 <= 160, "barrier area");
+static_assert(B_COUNT * 8 <= 192, "barrier area");
+constexpr int kSoftmaxWarps = 8;                         // warps 2..9: two per TMEM quarter
 
 struct Shared {
   uint8_t* base;       // 1 KB aligned
@@ -219,77 +230,94 @@ struct PageCursor {
   }
 };
 
-__device__ __forceinline__ void load_scores(const Shared& sh, uint32_t t_row, uint32_t (&sr)[64]) {
-  uint32_t* a = sr;
-  ptx::tmem_ld32(t_row + kColS, *reinterpret_cast<uint32_t(*)[32]>(a));
-  ptx::tmem_ld32(t_row + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(a + 32));
-  ptx::tmem_wait_ld();
-}
-
-// Q_r of one head row (group g) into TMEM: 256 c dims then 32 k_pe dims, two bf16 per column.
+// Q_r of one head row (group g) into TMEM: 256 c dims then 32 k_pe dims, two bf16 per
+// column; the row's two softmax threads store columns [0, 64) and [64, 144).
 __device__ __forceinline__ void store_q(const DecodeParams& p, uint32_t t_row, int g, int row,
-                                        int rank) {
+                                        int rank, int half) {
   const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(p.q_lat) +
                                                     ((long long)g * kH + row) * kD);
-  uint4 cur[8], nxt[8];
+  if (half == 0) {
+    uint4 a[8], b[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) cur[i] = src[32 * rank + i];
+    for (int i = 0; i < 8; ++i) a[i] = src[32 * rank + i];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    if (c < 3) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) nxt[i] = src[32 * rank + 8 * (c + 1) + i];
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) nxt[i] = src[64 + 4 * rank + i];
-    }
+    for (int i = 0; i < 8; ++i) b[i] = src[32 * rank + 8 + i];
     uint32_t v[32];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      v[4 * i] = cur[i].x; v[4 * i + 1] = cur[i].y; v[4 * i + 2] = cur[i].z; v[4 * i + 3] = cur[i].w;
+      v[4 * i] = a[i].x; v[4 * i + 1] = a[i].y; v[4 * i + 2] = a[i].z; v[4 * i + 3] = a[i].w;
     }
-    ptx::tmem_st32(t_row + kColQ + 32 * c, v);
+    ptx::tmem_st32(t_row + kColQ, v);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
-  }
-  uint32_t w[16];
+    for (int i = 0; i < 8; ++i) {
+      v[4 * i] = b[i].x; v[4 * i + 1] = b[i].y; v[4 * i + 2] = b[i].z; v[4 * i + 3] = b[i].w;
+    }
+    ptx::tmem_st32(t_row + kColQ + 32, v);
+  } else {
+    uint4 a[8], b[8], c[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    w[4 * i] = cur[i].x; w[4 * i + 1] = cur[i].y; w[4 * i + 2] = cur[i].z; w[4 * i + 3] = cur[i].w;
+    for (int i = 0; i < 8; ++i) a[i] = src[32 * rank + 16 + i];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b[i] = src[32 * rank + 24 + i];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = src[64 + 4 * rank + i];
+    uint32_t v[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[4 * i] = a[i].x; v[4 * i + 1] = a[i].y; v[4 * i + 2] = a[i].z; v[4 * i + 3] = a[i].w;
+    }
+    ptx::tmem_st32(t_row + kColQ + 64, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      v[4 * i] = b[i].x; v[4 * i + 1] = b[i].y; v[4 * i + 2] = b[i].z; v[4 * i + 3] = b[i].w;
+    }
+    ptx::tmem_st32(t_row + kColQ + 96, v);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      w[4 * i] = c[i].x; w[4 * i + 1] = c[i].y; w[4 * i + 2] = c[i].z; w[4 * i + 3] = c[i].w;
+    }
+    ptx::tmem_st16(t_row + kColQ + 128, w);
   }
-  ptx::tmem_st16(t_row + kColQ + 128, w);
   ptx::tmem_wait_st();
 }
 
 __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker,
                                  int rank, int warp, int lane) {
   const int quarter = warp & 3;
+  const int half = (warp - 2) >> 2;                      // 0: score cols 0-31, 1: cols 32-63
   const int row = 32 * quarter + lane;                   // head index = TMEM lane
+  const int tid = 32 * (warp - 2) + lane;                // 0..255 over the softmax warps
   const uint32_t t_row = tmem + ((uint32_t)(32 * quarter) << 16);
   const uint32_t peer = (uint32_t)(rank ^ 1);
-  const uint32_t peer_x0 = ptx::map_to_rank(sh.xbuf(0), peer);
-  uint8_t* stg_row = sh.base + kOffStg + row * 256;
+  const uint32_t hoff = (uint32_t)(half * kXHalf);
+  const uint32_t peer_x_warp = ptx::map_to_rank(sh.xbuf(0), peer) + hoff + quarter * 2048;
   const uint32_t peer_xfull0 = ptx::map_to_rank(sh.bar(B_XFULL0), peer);
   const uint32_t peer_xempty0 = ptx::map_to_rank(sh.bar(B_XEMPTY0), peer);
-  const int sw = row & 7;
+  const uint32_t stg_warp = sh.stg() + hoff + quarter * 2048;
+  uint8_t* stg_row = sh.base + kOffStg + hoff + row * 64;
+  float* red = reinterpret_cast<float*>(sh.base + kOffRed);      // [parity][half][row]
+  float* lsum = reinterpret_cast<float*>(sh.base + kOffLsum);    // [parity][half][row]
+  const int sw = (row >> 1) & 3;                         // 16-byte chunk swizzle of 64-byte rows
   PageCursor cur, ahead;
   cur.init(p, p.worker_off[worker], p.worker_off[worker + 1]);
   ahead = cur;
   if (!cur.valid()) return;
-  uint32_t sr[64];
+  uint32_t sr[32];
 
   auto publish_q = [&](int g) {
-    store_q(p, t_row, g, row, rank);
+    store_q(p, t_row, g, row, rank, half);
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(sh.bar(B_QFULL));
   };
-  // own partial of page n -> registers -> local staging -> (bulk copy) the peer's receive
-  // buffer n & 1
+  // own half-row of page n's partial scores -> registers -> local staging -> (one bulk copy
+  // per warp) the peer's receive buffer n & 1
   auto fetch_and_send = [&](uint32_t n) -> bool {
     if (!wait_bar(sh, sh.bar(B_SFULL), n & 1, p.status)) return false;
     ptx::tc_fence_after();
-    load_scores(sh, t_row, sr);
+    ptx::tmem_ld32(t_row + kColS + 32 * half, sr);
+    ptx::tmem_wait_ld();
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) {
@@ -297,10 +325,21 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
       ptx::bulk_wait_read_all();                 // the previous copy has read the staging rows
     }
     __syncwarp();
+    // own partial rounded to fp16 (kept in sr as the same rounded values, for the sum)
 #pragma unroll
-    for (int c = 0; c < 16; ++c)
-      *reinterpret_cast<uint4*>(stg_row + ((c ^ sw) * 16)) =
-          make_uint4(sr[4 * c], sr[4 * c + 1], sr[4 * c + 2], sr[4 * c + 3]);
+    for (int c = 0; c < 4; ++c) {
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __half2 h2 = __floats2half2_rn(__uint_as_float(sr[8 * c + 2 * k]),
+                                             __uint_as_float(sr[8 * c + 2 * k + 1]));
+        w[k] = *reinterpret_cast<const uint32_t*>(&h2);
+        const float2 back = __half22float2(h2);
+        sr[8 * c + 2 * k] = __float_as_uint(back.x);
+        sr[8 * c + 2 * k + 1] = __float_as_uint(back.y);
+      }
+      *reinterpret_cast<uint4*>(stg_row + ((c ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
     ptx::fence_proxy_async_smem();
     __syncwarp();
     const uint32_t j = n & 1;
@@ -308,8 +347,7 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
     if (lane == 0) {
       ok = wait_bar(sh, sh.bar(B_XEMPTY0 + j), ((n >> 1) & 1) ^ 1, p.status, true) ? 1 : 0;
       if (ok) {
-        ptx::bulk_s2s(peer_x0 + j * kXBytes + quarter * 8192, sh.stg() + quarter * 8192, 8192,
-                      peer_xfull0 + 8 * j);
+        ptx::bulk_s2s(peer_x_warp + j * kXBytes, stg_warp, 2048, peer_xfull0 + 8 * j);
         ptx::bulk_commit();
       }
     }
@@ -327,8 +365,8 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
   if (!fetch_and_send(0)) return;
   ahead.next();
 
-  uint32_t n = 0;
-  float m_used = -INFINITY, l = 0.f;
+  uint32_t n = 0, item_idx = 0;
+  float m_used = -INFINITY, l = 0.f;                     // l: this half's share of the row sum
   while (cur.valid()) {
     const WorkItem item = cur.item;
     const int pg = cur.pg;
@@ -344,35 +382,38 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
     const uint32_t jx = n & 1;
     if (!wait_bar(sh, sh.bar(B_XFULL0 + jx), (n >> 1) & 1, p.status, true)) return;
     if (warp == 2 && lane == 0) ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL0 + jx), kXBytes);
-    const float* xrow = reinterpret_cast<const float*>(sh.base + kOffX + jx * kXBytes + row * 256);
-    float s[64];
+    const uint8_t* xrow = sh.base + kOffX + jx * kXBytes + hoff + row * 64;
+    float s[32];
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const float4 v = *reinterpret_cast<const float4*>(xrow + 4 * (c ^ sw));
-      s[4 * c + 0] = __uint_as_float(sr[4 * c + 0]) + v.x;
-      s[4 * c + 1] = __uint_as_float(sr[4 * c + 1]) + v.y;
-      s[4 * c + 2] = __uint_as_float(sr[4 * c + 2]) + v.z;
-      s[4 * c + 3] = __uint_as_float(sr[4 * c + 3]) + v.w;
+    for (int c = 0; c < 4; ++c) {
+      const uint4 v = *reinterpret_cast<const uint4*>(xrow + ((c ^ sw) * 16));
+      const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&vv[k]));
+        s[8 * c + 2 * k] = __uint_as_float(sr[8 * c + 2 * k]) + f.x;
+        s[8 * c + 2 * k + 1] = __uint_as_float(sr[8 * c + 2 * k + 1]) + f.y;
+      }
     }
     {
       // every lane's buffer reads have returned before lane 0 tells the peer it may refill
       uint32_t dep = 0;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) dep ^= __float_as_uint(s[4 * c]);
+      for (int c = 0; c < 4; ++c) dep ^= __float_as_uint(s[8 * c]);
       const uint32_t all = __ballot_sync(0xffffffffu, dep != 0x7fc00001u);
       if (lane == 0) ptx::mbar_arrive_remote_relaxed(peer_xempty0 + 8 * jx, all);
     }
 
-    // 2. own partial of page n+1 (computed one page ahead by the MMA warp) -> peer; a page
-    // that opens the next work item needs that item's Q_r in TMEM first (every QK of the
-    // current item is done: its last scores, page n's, are already read)
+    // 2. own partial of page n+1 (computed one page ahead by the score MMAs) -> peer; a page
+    // that opens the next work item needs that item's Q_r in TMEM first (every score MMA of
+    // the current item is done: its last scores, page n's, are already read)
     if (ahead.valid()) {
       if (ahead.first()) publish_q(ahead.item.group);
       load_meta(ahead, &page_nxt, &kv_nxt);
       if (!fetch_and_send(n + 1)) return;
       ahead.next();
     }
-    if (!valid && row == 0 && rank == 0) flag_status(p.status, MLA_ERR_DEVICE_GUARD);
+    if (!valid && row == 0 && half == 0 && rank == 0) flag_status(p.status, MLA_ERR_DEVICE_GUARD);
 
     // 3. softmax of page n. Rows past the last token (or a whole skipped page) may hold
     // anything, NaN included, and 0 * NaN would poison O: zero them in the staged c_kv
@@ -382,20 +423,26 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
       uint8_t* stg = sh.base + kOffStage + (int)(n % kNS) * kStageBytes;
       const int nrows = kP - ntok;
       const int per_tile = nrows * 8;
-      for (int i = 32 * (warp - 2) + lane; i < 4 * per_tile; i += 128) {
+      for (int i = tid; i < 4 * per_tile; i += 32 * kSoftmaxWarps) {
         const int tile = i / per_tile, rem = i % per_tile;
         *reinterpret_cast<uint4*>(stg + tile * kKTileC + (ntok + rem / 8) * 128 + (rem % 8) * 16) =
             make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int i = 0; i < 64; ++i)
-        if (i >= ntok) s[i] = -INFINITY;
+      for (int i = 0; i < 32; ++i)
+        if (32 * half + i >= ntok) s[i] = -INFINITY;
       zeroed = true;
     }
-    float mx = s[0];
+    float hm = s[0];
 #pragma unroll
-    for (int i = 1; i < 64; ++i) mx = fmaxf(mx, s[i]);
-    mx *= p.scale_log2;
+    for (int i = 1; i < 32; ++i) hm = fmaxf(hm, s[i]);
+    // combine the two halves' maxima of this row
+    float* redp = red + (int)(n & 1) * 256;
+    redp[half * 128 + row] = hm;
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(sh.bar(B_RMAX0 + (n & 1)));
+    if (!wait_bar(sh, sh.bar(B_RMAX0 + (n & 1)), (n >> 1) & 1, p.status)) return;
+    const float mx = fmaxf(hm, redp[(half ^ 1) * 128 + row]) * p.scale_log2;
     bool rescale = false;
     float alpha = 1.f;
     if (mx > -INFINITY) {
@@ -408,15 +455,15 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
         rescale = true;
       }
     }
-    uint32_t packed[32];
+    uint32_t packed[16];
     if (m_used == -INFINITY) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) packed[i] = 0u;
+      for (int i = 0; i < 16; ++i) packed[i] = 0u;
     } else {
       const float neg_m = -m_used;
       float psum = 0.f;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < 16; ++i) {
         const float p0 = ptx::ex2(fmaf(s[2 * i], p.scale_log2, neg_m));
         const float p1 = ptx::ex2(fmaf(s[2 * i + 1], p.scale_log2, neg_m));
         psum += p0 + p1;
@@ -430,35 +477,42 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
     ptx::tc_fence_after();
     if (rescale) {
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
-        ptx::tmem_ld32(t_row + kColO + 32 * c, v);
+        const uint32_t a = t_row + kColO + 128 * half + 32 * c;
+        ptx::tmem_ld32(a, v);
         ptx::tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-        ptx::tmem_st32(t_row + kColO + 32 * c, v);
+        ptx::tmem_st32(a, v);
       }
     }
-    ptx::tmem_st32(t_row + kColP, packed);
+    ptx::tmem_st16(t_row + kColP + 16 * half, packed);
     ptx::tmem_wait_st();
     if (zeroed) ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(sh.bar(B_PFULL));
 
-    // 4. after the item's last page: normalise O_r and write it (output or split partial)
+    // 4. after the item's last page: normalise this half of O_r and write it
     if (cur.last()) {
       const int it = cur.it;
+      float* ls = lsum + (int)(item_idx & 1) * 256;
+      ls[half * 128 + row] = l;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(sh.bar(B_LSUM0 + (item_idx & 1)));
+      if (!wait_bar(sh, sh.bar(B_LSUM0 + (item_idx & 1)), (item_idx >> 1) & 1, p.status)) return;
+      const float lt = l + ls[(half ^ 1) * 128 + row];
       if (!wait_bar(sh, sh.bar(B_PVDONE), n & 1, p.status)) return;
       ptx::tc_fence_after();
-      const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
-      const float lse_v = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      const float inv = (lt > 0.f) ? p.out_scale / lt : 0.f;
+      const float lse_v = (lt > 0.f) ? (m_used + log2f(lt)) * kLn2 : -INFINITY;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
-        ptx::tmem_ld32(t_row + kColO + 32 * c, v);
+        ptx::tmem_ld32(t_row + kColO + 128 * half + 32 * c, v);
         ptx::tmem_wait_ld();
-        const int col = 256 * rank + 32 * c;
+        const int col = 256 * rank + 128 * half + 32 * c;
         if (item.single) {
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out_latent) +
                                                 ((long long)g * kH + row) * kDC + col);
@@ -466,10 +520,10 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
           for (int q = 0; q < 4; ++q) {
             uint32_t w[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * j]) * inv,
-                                                              __uint_as_float(v[8 * q + 2 * j + 1]) * inv);
-              w[j] = *reinterpret_cast<const uint32_t*>(&h2);
+            for (int jj = 0; jj < 4; ++jj) {
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * jj]) * inv,
+                                                              __uint_as_float(v[8 * q + 2 * jj + 1]) * inv);
+              w[jj] = *reinterpret_cast<const uint32_t*>(&h2);
             }
             dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
           }
@@ -484,10 +538,11 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(sh.bar(B_OFREE));
-      if (rank == 0) {
+      if (rank == 0 && half == 0) {
         if (item.single) p.lse[(long long)g * kH + row] = lse_v;
         else p.part_lse[(long long)it * kH + row] = lse_v;
       }
+      ++item_idx;
     }
     ++n;
     cur.next();
@@ -505,8 +560,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t aligned = (raw + 1023u) & ~1023u;
   sh.base = smem_raw + (aligned - raw);
   sh.base_u32 = aligned;
-  sh.abort = reinterpret_cast<volatile int*>(sh.base + kOffBar + 160);
-  sh.tmem_slot = reinterpret_cast<uint32_t*>(sh.base + kOffBar + 168);
+  sh.abort = reinterpret_cast<volatile int*>(sh.base + kOffBar + 192);
+  sh.tmem_slot = reinterpret_cast<uint32_t*>(sh.base + kOffBar + 200);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (int)ptx::cluster_ctarank();
   const int worker = blockIdx.x >> 1;
@@ -516,17 +571,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_init(sh.bar(B_FULL0 + s), 1);
       ptx::mbar_init(sh.bar(B_EMPTY0 + s), 1);
     }
-    ptx::mbar_init(sh.bar(B_QFULL), 4);
+    ptx::mbar_init(sh.bar(B_QFULL), kSoftmaxWarps);
     ptx::mbar_init(sh.bar(B_SFULL), 1);
-    ptx::mbar_init(sh.bar(B_SFREE), 4);
-    ptx::mbar_init(sh.bar(B_PFULL), 4);
+    ptx::mbar_init(sh.bar(B_SFREE), kSoftmaxWarps);
+    ptx::mbar_init(sh.bar(B_PFULL), kSoftmaxWarps);
     ptx::mbar_init(sh.bar(B_PVDONE), 1);
     ptx::mbar_init(sh.bar(B_XFULL0), 1);
     ptx::mbar_init(sh.bar(B_XFULL1), 1);
-    ptx::mbar_init(sh.bar(B_XEMPTY0), 4);
-    ptx::mbar_init(sh.bar(B_XEMPTY1), 4);
-    ptx::mbar_init(sh.bar(B_OFREE), 4);
+    ptx::mbar_init(sh.bar(B_XEMPTY0), kSoftmaxWarps);
+    ptx::mbar_init(sh.bar(B_XEMPTY1), kSoftmaxWarps);
+    ptx::mbar_init(sh.bar(B_OFREE), kSoftmaxWarps);
     ptx::mbar_init(sh.bar(B_TEARDOWN), 2);
+    ptx::mbar_init(sh.bar(B_RMAX0), kSoftmaxWarps);
+    ptx::mbar_init(sh.bar(B_RMAX1), kSoftmaxWarps);
+    ptx::mbar_init(sh.bar(B_LSUM0), kSoftmaxWarps);
+    ptx::mbar_init(sh.bar(B_LSUM1), kSoftmaxWarps);
     *sh.abort = 0;
     ptx::fence_mbar_init();
     // first phase of each receive buffer (the peer's partials of pages 0 and 1)
@@ -549,7 +608,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) producer(sh, p, &tm_kc, &tm_kpe, worker, rank);
   } else if (warp == 1) {
     if (lane == 0) qk_issuer(sh, p, tmem, worker);
-  } else if (warp == 6) {
+  } else if (warp == 10) {
     if (lane == 0) pv_issuer(sh, p, tmem, worker);
   } else {
     softmax_epilogue(sh, p, tmem, worker, rank, warp, lane);
@@ -557,8 +616,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   // teardown: every role gets here, normally or after a bounded wait gave up
   // both MMA issuers commit: every issued MMA must have finished before TMEM is released
-  if ((warp == 1 || warp == 6) && lane == 0) ptx::mma_commit(sh.bar(B_TEARDOWN));
-  if (warp >= 2 && warp <= 5 && lane == 0) ptx::bulk_wait_read_all();
+  if ((warp == 1 || warp == 10) && lane == 0) ptx::mma_commit(sh.bar(B_TEARDOWN));
+  if (warp >= 2 && warp <= 9 && lane == 0) ptx::bulk_wait_read_all();
   __syncthreads();
   if (warp == 1) {
     if (lane == 0) {
