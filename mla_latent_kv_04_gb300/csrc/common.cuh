@@ -28,7 +28,8 @@ struct RopeTable {
 __device__ __forceinline__ void rope_sincos(const RopeTable& rt, int k, int pos, float* s, float* c) {
   double a = (double)pos * rt.inv_freq[k];
   const double two_pi = 6.283185307179586476925286766559;
-  a -= two_pi * rint(a / two_pi);
+  const double inv_two_pi = 0.15915494309189533576888376337251;
+  a = fma(-two_pi, rint(a * inv_two_pi), a);
   sincosf((float)a, s, c);
 }
 

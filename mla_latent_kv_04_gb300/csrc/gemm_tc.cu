@@ -30,13 +30,12 @@ struct Params {
   int32_t* status;
 };
 
-template <int BN>
+template <int BN, int NS>
 struct Cfg {
   static constexpr int kABytes = kBM * kBK * 2;          // 16 KB: two 64x64 MN-major boxes
   static constexpr int kBBytes = BN * kBK * 2;            // BN rows of 128 bytes
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = (BN <= 64) ? 4 : (BN <= 128 ? 5 : 4);
-  static constexpr int kCtasPerSm = (BN <= 64) ? 2 : 1;
+  static constexpr int kStages = NS;
   static constexpr int kBarOff = kStages * kStageBytes;
   static constexpr int kSmem = kBarOff + 256 + 1024;
   static constexpr uint32_t kTmemCols = (BN <= 32) ? 32 : (BN <= 64 ? 64 : (BN <= 128 ? 128 : 256));
@@ -60,11 +59,11 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 
 // D^T[z][m][n] = sum_k A[z][k][m] * B[z][n][k]; A is the MN-major weight, B the K-major
 // token matrix. Work unit = (z, m tile, n tile, k split), one per CTA.
-template <int BN, class Epi>
+template <int BN, int NS, class Epi>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const Params gp, const Epi epi) {
-  using C = Cfg<BN>;
+  using C = Cfg<BN, NS>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = ptx::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -222,11 +221,11 @@ static int sm_count() {
   return cached[dev];
 }
 
-template <int BN, class Epi>
+template <int BN, int NS, class Epi>
 static cudaError_t run(const CUtensorMap& A, const CUtensorMap& B, Params gp, const Epi& epi,
                        cudaStream_t s) {
-  using C = Cfg<BN>;
-  auto kern = tc_gemm_kernel<BN, Epi>;
+  using C = Cfg<BN, NS>;
+  auto kern = tc_gemm_kernel<BN, NS, Epi>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   const long long units = (long long)gp.batch * gp.m_tiles * gp.n_tiles * gp.k_splits;
@@ -246,16 +245,20 @@ static cudaError_t dispatch(const CUtensorMap& A, const CUtensorMap& Bmap32, con
   gp.k_blocks = (gp.K + kBK - 1) / kBK;
   gp.k_splits = 1;
   if (allow_split) {
+    // about two CTAs per SM, each with at least 4 K blocks
     const long long base_units = (long long)gp.batch * gp.m_tiles * gp.n_tiles;
     const int per_sm = bn <= 64 ? 2 : 1;
-    const int want = (int)(((long long)per_sm * sm_count()) / (base_units > 0 ? base_units : 1));
-    gp.k_splits = want < 1 ? 1 : (want > gp.k_blocks ? gp.k_blocks : want);
+    int want = (int)(((long long)per_sm * sm_count()) / (base_units > 0 ? base_units : 1));
+    const int max_splits = gp.k_blocks / 4 > 0 ? gp.k_blocks / 4 : 1;
+    if (want > max_splits) want = max_splits;
+    gp.k_splits = want < 1 ? 1 : want;
   }
+  const bool shallow = (gp.k_blocks + gp.k_splits - 1) / gp.k_splits <= 2;   // ring of 2 is enough
   switch (bn) {
-    case 32: return run<32>(A, Bmap32, gp, epi, s);
-    case 64: return run<64>(A, Bmap64, gp, epi, s);
-    case 128: return run<128>(A, Bmap128, gp, epi, s);
-    default: return run<256>(A, Bmap256, gp, epi, s);
+    case 32: return shallow ? run<32, 2>(A, Bmap32, gp, epi, s) : run<32, 4>(A, Bmap32, gp, epi, s);
+    case 64: return shallow ? run<64, 2>(A, Bmap64, gp, epi, s) : run<64, 4>(A, Bmap64, gp, epi, s);
+    case 128: return shallow ? run<128, 2>(A, Bmap128, gp, epi, s) : run<128, 5>(A, Bmap128, gp, epi, s);
+    default: return shallow ? run<256, 2>(A, Bmap256, gp, epi, s) : run<256, 4>(A, Bmap256, gp, epi, s);
   }
 }
 

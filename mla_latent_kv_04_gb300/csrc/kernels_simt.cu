@@ -215,26 +215,36 @@ __global__ void transpose_heads_kernel(const T* __restrict__ W_UK, T* __restrict
 }
 
 // ======================================================================== query prologue
+// One block per (group, 16 heads): the d_r/2 rotation angles of the group's position are
+// computed once into shared memory, then applied to those heads' q_pe.
 template <typename T>
-__global__ void q_rope_kernel(const T* __restrict__ q_pe, const int32_t* seq_lens, int batch,
-                              int q_len, int H, int d_c, int d_r, RopeTable rt, T* __restrict__ q_lat) {
-  const long long pairs = (long long)batch * q_len * H * (d_r / 2);
+__global__ void __launch_bounds__(256) q_rope_kernel(const T* __restrict__ q_pe,
+                                                     const int32_t* seq_lens, int batch, int q_len,
+                                                     int H, int d_c, int d_r, RopeTable rt,
+                                                     T* __restrict__ q_lat) {
+  __shared__ float cs[kMaxRopePairs], sn[kMaxRopePairs];
+  const int g = blockIdx.x;
+  const int h0 = blockIdx.y * 16, h1 = min(H, h0 + 16);
+  const int b = g / q_len, t = g % q_len;
+  const int pos = seq_lens[b] - q_len + t;
+  const int pairs = d_r / 2;
+  if (threadIdx.x < pairs) {
+    float s_ = 0.f, c_ = 0.f;
+    if (pos >= 0) rope_sincos(rt, threadIdx.x, pos, &s_, &c_);
+    sn[threadIdx.x] = s_;
+    cs[threadIdx.x] = c_;
+  }
+  __syncthreads();
   const int D = d_c + d_r;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < pairs;
-       i += (long long)gridDim.x * blockDim.x) {
-    const int k = (int)(i % (d_r / 2));
-    const long long gh = i / (d_r / 2);           // (b * q_len + t) * H + h
-    const long long g = gh / H;
-    const int b = (int)(g / q_len), t = (int)(g % q_len);
-    const int pos = seq_lens[b] - q_len + t;
+  for (int i = threadIdx.x; i < (h1 - h0) * pairs; i += blockDim.x) {
+    const int h = h0 + i / pairs, k = i % pairs;
+    const long long gh = (long long)g * H + h;
     const float x0 = to_f32(q_pe[gh * d_r + 2 * k]);
     const float x1 = to_f32(q_pe[gh * d_r + 2 * k + 1]);
     float y0 = 0.f, y1 = 0.f;
     if (pos >= 0) {
-      float sn, cs;
-      rope_sincos(rt, k, pos, &sn, &cs);
-      y0 = x0 * cs - x1 * sn;
-      y1 = x0 * sn + x1 * cs;
+      y0 = x0 * cs[k] - x1 * sn[k];
+      y1 = x0 * sn[k] + x1 * cs[k];
     }
     q_lat[gh * D + d_c + 2 * k] = from_f32<T>(y0);
     q_lat[gh * D + d_c + 2 * k + 1] = from_f32<T>(y1);
@@ -291,7 +301,7 @@ __device__ __forceinline__ int group_of(const int* cu, int n, long long x) {
 // worker w processes its range as one work item per group it touches. An item that
 // covers a whole group writes the final output, the others write partials merged by
 // the combine kernel.
-__global__ void __launch_bounds__(1024) plan_kernel(PlanParams p) {
+__global__ void __launch_bounds__(256) plan_kernel(PlanParams p) {
   extern __shared__ int sm[];
   const int groups = p.batch * p.q_len;
   int* cu = sm;                             // [groups + 1]
@@ -494,39 +504,63 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeParams p) {
 // ======================================================================== LSE combine
 // out = sum_s exp(lse_s - L) o_s with L = log sum_s exp(lse_s) over a group's items;
 // groups with no item (empty requests) get out = 0, lse = -inf.
+// One warp per (group, head): the warp merges the group's split partials over the d_c
+// latent dims with 16-byte loads.
 template <typename QT>
-__global__ void __launch_bounds__(128) combine_kernel(DecodeParams p) {
-  const int gh = blockIdx.x;
-  const int g = gh / p.H, h = gh % p.H;
-  const int k = blockIdx.y * blockDim.x + threadIdx.x;
+__global__ void __launch_bounds__(256) combine_kernel(DecodeParams p, int groups) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long gh = (long long)blockIdx.x * 8 + warp;
+  if (gh >= (long long)groups * p.H) return;
+  const int g = (int)(gh / p.H), h = (int)(gh % p.H);
   const int first = p.group_first[g], last = p.group_last[g];
   const int n = (first >= 0 && last >= first) ? last - first + 1 : 0;
-  QT* out = reinterpret_cast<QT*>(p.out_latent) + (long long)gh * p.d_c;
-  if (n == 1) return;
-  if (n == 0) {
-    if (k < p.d_c) out[k] = from_f32<QT>(0.f);
-    if (k == 0) p.lse[gh] = -INFINITY;
-    return;
-  }
+  QT* out = reinterpret_cast<QT*>(p.out_latent) + gh * p.d_c;
+  if (n == 1) return;                          // written directly by the attention kernel
   float m = -INFINITY;
   for (int s = 0; s < n; ++s) m = fmaxf(m, p.part_lse[(long long)(first + s) * p.H + h]);
-  if (m == -INFINITY) {
-    if (k < p.d_c) out[k] = from_f32<QT>(0.f);
-    if (k == 0) p.lse[gh] = -INFINITY;
+  if (n == 0 || m == -INFINITY) {
+    for (int k = lane; k < p.d_c; k += 32) out[k] = from_f32<QT>(0.f);
+    if (lane == 0) p.lse[gh] = -INFINITY;
     return;
   }
   float sum = 0.f;
   for (int s = 0; s < n; ++s) sum += expf(p.part_lse[(long long)(first + s) * p.H + h] - m);
   const float L = m + logf(sum);
-  if (k < p.d_c) {
-    float acc = 0.f;
-    for (int s = 0; s < n; ++s) {
-      const long long slot = (long long)(first + s) * p.H + h;
-      acc = fmaf(expf(p.part_lse[slot] - L), p.part_o[slot * p.d_c + k], acc);
+  // weights of the first 8 splits kept in registers; any further split is streamed
+  constexpr int kW = 8;
+  float w[kW];
+#pragma unroll
+  for (int s = 0; s < kW; ++s)
+    w[s] = (s < n) ? expf(p.part_lse[(long long)(first + s) * p.H + h] - L) : 0.f;
+  const float* base = p.part_o + ((long long)first * p.H + h) * p.d_c;
+  const long long stride = (long long)p.H * p.d_c;     // from one split slot to the next
+  for (int k = 4 * lane; k < p.d_c; k += 128) {
+    float4 v[kW];
+#pragma unroll
+    for (int s = 0; s < kW; ++s)
+      v[s] = (s < n) ? *reinterpret_cast<const float4*>(base + s * stride + k) : make_float4(0, 0, 0, 0);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < kW; ++s) {
+      acc.x = fmaf(w[s], v[s].x, acc.x);
+      acc.y = fmaf(w[s], v[s].y, acc.y);
+      acc.z = fmaf(w[s], v[s].z, acc.z);
+      acc.w = fmaf(w[s], v[s].w, acc.w);
     }
-    out[k] = from_f32<QT>(acc);
+    for (int s = kW; s < n; ++s) {
+      const float ws = expf(p.part_lse[(long long)(first + s) * p.H + h] - L);
+      const float4 x = *reinterpret_cast<const float4*>(base + s * stride + k);
+      acc.x = fmaf(ws, x.x, acc.x);
+      acc.y = fmaf(ws, x.y, acc.y);
+      acc.z = fmaf(ws, x.z, acc.z);
+      acc.w = fmaf(ws, x.w, acc.w);
+    }
+    out[k] = from_f32<QT>(acc.x);
+    out[k + 1] = from_f32<QT>(acc.y);
+    out[k + 2] = from_f32<QT>(acc.z);
+    out[k + 3] = from_f32<QT>(acc.w);
   }
-  if (k == 0) p.lse[gh] = L;
+  if (lane == 0) p.lse[gh] = L;
 }
 
 template <typename T>
@@ -544,7 +578,7 @@ cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
-  plan_kernel<<<1, 1024, smem, s>>>(p);
+  plan_kernel<<<1, 256, smem, s>>>(p);
   note_launch();
   return cudaGetLastError();
 }
@@ -561,10 +595,8 @@ static cudaError_t query_prologue_t(const void* q_nope, const void* q_pe, const 
                             reinterpret_cast<const T*>(W_UK_abs), (long long)d_c,
                             (long long)d_n * d_c, groups, d_c, d_n, H, 1, epi, s);
   if (e != cudaSuccess) return e;
-  const long long pairs = (long long)groups * H * (d_r / 2);
-  const int blocks = (int)min((pairs + 255) / 256, 4096LL);
-  if (blocks > 0) {
-    q_rope_kernel<T><<<blocks, 256, 0, s>>>(reinterpret_cast<const T*>(q_pe), seq_lens, batch, q_len,
+  if (groups > 0) {
+    q_rope_kernel<T><<<dim3(groups, (H + 15) / 16), 256, 0, s>>>(reinterpret_cast<const T*>(q_pe), seq_lens, batch, q_len,
                                            H, d_c, d_r, rt, reinterpret_cast<T*>(q_lat));
     note_launch();
   }
@@ -574,9 +606,9 @@ static cudaError_t query_prologue_t(const void* q_nope, const void* q_pe, const 
 cudaError_t launch_q_rope(mla_dtype act, const void* q_pe, const int32_t* seq_lens, int batch,
                           int q_len, int H, int d_c, int d_r, const RopeTable& rt, void* q_lat,
                           cudaStream_t s) {
-  const long long pairs = (long long)batch * q_len * H * (d_r / 2);
-  const int blocks = (int)min((pairs + 255) / 256, 4096LL);
-  if (blocks <= 0) return cudaSuccess;
+  const int groups = batch * q_len;
+  if (groups <= 0) return cudaSuccess;
+  const dim3 blocks(groups, (H + 15) / 16);
   if (act == MLA_F32)
     q_rope_kernel<float><<<blocks, 256, 0, s>>>(reinterpret_cast<const float*>(q_pe), seq_lens, batch,
                                                q_len, H, d_c, d_r, rt, reinterpret_cast<float*>(q_lat));
@@ -632,9 +664,9 @@ cudaError_t launch_decode_simt(mla_dtype act, mla_dtype cache, const DecodeParam
 
 cudaError_t launch_combine(mla_dtype act, const DecodeParams& p, int groups, cudaStream_t s) {
   if (groups <= 0) return cudaSuccess;
-  dim3 grid(groups * p.H, (p.d_c + 127) / 128);
-  if (act == MLA_F32) combine_kernel<float><<<grid, 128, 0, s>>>(p);
-  else combine_kernel<bf16><<<grid, 128, 0, s>>>(p);
+  const int blocks = (int)(((long long)groups * p.H + 7) / 8);
+  if (act == MLA_F32) combine_kernel<float><<<blocks, 256, 0, s>>>(p, groups);
+  else combine_kernel<bf16><<<blocks, 256, 0, s>>>(p, groups);
   note_launch();
   return cudaGetLastError();
 }
