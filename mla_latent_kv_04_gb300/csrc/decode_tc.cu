@@ -11,31 +11,26 @@
 // [512+32r, 512+32r+32). Per 64-token page each CTA
 //   1. TMA-loads only its 288-column slice of the page (36 KB; the pair reads each byte of
 //      the page once) into a 4-stage ring,
-//   2. computes a partial score S_r = Q_r K_r^T (M = 128 heads, N = 64 tokens, K = 288;
-//      A = Q_r held in TMEM, B = the staged page slice) into TMEM,
-//   3. sends S_r, rounded to fp16, to the peer over distributed shared memory (each
-//      softmax warp writes its 32 half-rows to a local staging buffer and one 2 KB bulk
-//      copy per warp moves them into one of the peer's two receive buffers, counted on the
-//      peer's mbarrier); both CTAs then use the same S = f16(S_0) + f16(S_1) in fp32.
-//      The fp16 rounding of a partial (relative 2^-11) is below the bf16 rounding of P,
-//      and halves the cluster traffic and the buffers, which buys the 4th page stage,
-//   4. runs the online softmax (one thread per head row, exp2, O rescaled lazily, only
-//      when the running maximum grows by more than 2^8),
-//   5. writes P (bf16) into TMEM and accumulates O_r += P C_r (M = 128, N = 256, K = 64;
-//      A = P from TMEM, B = the staged page slice) in TMEM.
-// TMEM: O_r 256 columns, S 64, P 32, Q_r 144 (288 bf16 per head row).
-// The softmax threads pipeline pages: for page n they first take the peer's partial,
-// then read and ship their own partial of page n+1 (whose scores the MMA warp computed
-// one page ahead), and only then do page n's softmax; with two receive buffers a send
-// waits only for the peer to have read the partial of two pages before, so the cluster
-// exchange overlaps the arithmetic of the previous page.
-// Roles: warp 0 issues TMA; warp 1 issues the score MMAs (one thread, running ahead as
-// soon as a page lands) and owns the TMEM allocation; warp 10 issues the P.C MMAs; warps
-// 2-9 run the softmax, load Q_r into TMEM at each work item's start and write the
-// outputs. Each head row (= TMEM lane) has two softmax threads, in warps w and w+4 (same
-// TMEM quarter): one owns score columns 0-31 and output dims 0-127 of the CTA's slice,
-// the other columns 32-63 and dims 128-255; they combine the row maximum every page and
-// the row sum once per work item through shared memory.
+//   2. computes its partial score S_r = Q_r K_r^T (M = 128 heads, N = 64 tokens, K = 288)
+//      into TMEM (A = the latent part of Q_r held in TMEM, and the k_pe part from shared
+//      memory),
+//   3. exchange warps read S_r, round it to fp16, stage it in shared memory and move it
+//      with one bulk copy per warp into one of the peer's two receive buffers (counted
+//      on the peer's mbarrier); when the peer's partial arrives they write the combined
+//      scores f16(S_0) + f16(S_1) (identical in both CTAs; the fp16 rounding, relative
+//      2^-11, is below the bf16 rounding of P) into a second TMEM buffer,
+//   4. softmax warps read the combined scores, run the online softmax (one thread per
+//      head row, exp2, O rescaled lazily, only when the running maximum grows by more
+//      than 2^8) and write P (bf16) over the same TMEM buffer,
+//   5. O_r += P C_r (M = 128, N = 256, K = 64; A = P from TMEM, B = the staged page).
+// The exchange warps run one page ahead of the softmax warps (they ship page n+1's
+// partial before combining page n), so the cluster transfer, the score MMAs and the
+// softmax of consecutive pages overlap.
+// Roles: warp 0 issues TMA; warp 1 issues the score MMAs and owns the TMEM allocation;
+// warps 2-5 exchange scores and load Q_r into TMEM at each work item's start; warps 6-9
+// run the softmax and write the outputs; warp 10 issues the P.C MMAs. A thread of warps
+// 2-9 owns one head row = one TMEM lane.
+// TMEM: O_r 256 columns, raw S 64, combined S / P 64, Q_r latent part 128.
 // Every mbarrier wait is bounded (2 s): on timeout the kernel records MLA_ERR_TIMEOUT,
 // every role leaves its loop, TMEM is freed and the pair meets at a final cluster
 // barrier before exit.
@@ -54,20 +49,19 @@ constexpr int kNS = 4;                                   // cache-page pipeline 
 constexpr int kKTileC = 64 * 64 * 2;                     // one 64-dim SW128 chunk of a page
 constexpr int kKTilePE = 64 * 32 * 2;                    // the 32-dim SW64 k_pe half
 constexpr int kStageBytes = 4 * kKTileC + kKTilePE;      // 36864
-constexpr int kXBytes = 128 * 64 * 2;                    // one partial-score buffer, fp16
-constexpr int kXHalf = kXBytes / 2;                      // [half][128 rows][32 scores]
+constexpr int kXBytes = 128 * 64 * 2;                    // one fp16 partial-score buffer
+constexpr int kQPeBytes = 128 * 32 * 2;                  // Q_r k_pe part, SW64 [128][32]
 constexpr int kOffStage = 0;
 constexpr int kOffX = kOffStage + kNS * kStageBytes;     // two receive buffers
-constexpr int kOffStg = kOffX + 2 * kXBytes;             // own partial, staged for the copy
-constexpr int kOffRed = kOffStg + kXBytes;               // row max halves [2][2][128] fp32
-constexpr int kOffLsum = kOffRed + 2048;                 // row sum halves [2][2][128] fp32
-constexpr int kOffBar = kOffLsum + 2048;
+constexpr int kOffStg = kOffX + 2 * kXBytes;             // two staging buffers (own partial)
+constexpr int kOffQPe = kOffStg + 2 * kXBytes;
+constexpr int kOffBar = kOffQPe + kQPeBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;         // + slack to align the base to 1 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;                            // O_r: 256 fp32 columns
-constexpr uint32_t kColS = 256;                          // S: 64 fp32 columns
-constexpr uint32_t kColP = 320;                          // P: 64 bf16 = 32 columns
-constexpr uint32_t kColQ = 352;                          // Q_r: 288 bf16 = 144 columns
+constexpr uint32_t kColS = 256;                          // raw partial S: 64 fp32 columns
+constexpr uint32_t kColC = 320;                          // combined S (fp32), then P (bf16)
+constexpr uint32_t kColQ = 384;                          // Q_r latent part: 256 bf16 = 128
 constexpr int kThreads = 352;                            // 11 warps
 constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, 256, false, true);
@@ -75,12 +69,11 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 // mbarrier slots (8 bytes each) at kOffBar
 enum {
-  B_FULL0 = 0, B_EMPTY0 = kNS, B_QFULL = 2 * kNS, B_SFULL, B_SFREE, B_PFULL, B_PVDONE,
-  B_XFULL0, B_XFULL1, B_XEMPTY0, B_XEMPTY1, B_OFREE, B_TEARDOWN, B_RMAX0, B_RMAX1, B_LSUM0,
-  B_LSUM1, B_COUNT
+  B_FULL0 = 0, B_EMPTY0 = kNS, B_QFULL = 2 * kNS, B_QPEFULL, B_QPEEMPTY, B_SFULL, B_SFREE,
+  B_CFULL, B_PFULL, B_PVDONE, B_XFULL0, B_XFULL1, B_XEMPTY0, B_XEMPTY1, B_OFREE, B_TEARDOWN,
+  B_COUNT
 };
 static_assert(B_COUNT * 8 <= 192, "barrier area");
-constexpr int kSoftmaxWarps = 8;                         // warps 2..9: two per TMEM quarter
 
 struct Shared {
   uint8_t* base;       // 1 KB aligned
@@ -90,7 +83,8 @@ struct Shared {
   __device__ uint32_t bar(int i) const { return base_u32 + kOffBar + 8 * i; }
   __device__ uint32_t stage(int s) const { return base_u32 + kOffStage + s * kStageBytes; }
   __device__ uint32_t xbuf(int j) const { return base_u32 + kOffX + j * kXBytes; }
-  __device__ uint32_t stg() const { return base_u32 + kOffStg; }
+  __device__ uint32_t stg(int j) const { return base_u32 + kOffStg + j * kXBytes; }
+  __device__ uint32_t qpe() const { return base_u32 + kOffQPe; }
 };
 
 __device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_t parity,
@@ -111,99 +105,7 @@ __device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_
   }
 }
 
-// ------------------------------------------------------------------------------- roles
-__device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensorMap* tm_kc,
-                         const CUtensorMap* tm_kpe, int worker, int rank) {
-  const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
-  int stage = 0;
-  uint32_t wrap = 0;
-  for (int it = it0; it < it1; ++it) {
-    const WorkItem item = p.items[it];
-    const int b = item.group / p.q_len;
-    for (int pg = item.page_begin; pg < item.page_end; ++pg) {
-      int page = p.block_table[(long long)b * p.max_pages + pg];
-      if (page < 0 || page >= p.num_pages) page = 0;      // masked by the softmax side
-      if (!wait_bar(sh, sh.bar(B_EMPTY0 + stage), (wrap & 1) ^ 1, p.status)) return;
-      const uint32_t full = sh.bar(B_FULL0 + stage);
-      ptx::mbar_arrive_expect_tx(full, kStageBytes);
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        ptx::tma_load_2d(sh.stage(stage) + c * kKTileC, tm_kc, 256 * rank + 64 * c, page * kP, full);
-      ptx::tma_load_2d(sh.stage(stage) + 4 * kKTileC, tm_kpe, kDC + 32 * rank, page * kP, full);
-      if (++stage == kNS) {
-        stage = 0;
-        ++wrap;
-      }
-    }
-  }
-}
-
-// Score MMAs: S = Q_r K_r^T for every page in order, as soon as the page has landed and the
-// softmax has read the previous scores (S has one TMEM buffer).
-__device__ void qk_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker) {
-  const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
-  int stage = 0;
-  uint32_t wrap = 0, n = 0, item_idx = 0;
-  for (int it = it0; it < it1; ++it) {
-    const WorkItem item = p.items[it];
-    for (int pg = item.page_begin; pg < item.page_end; ++pg) {
-      if (pg == item.page_begin && !wait_bar(sh, sh.bar(B_QFULL), item_idx & 1, p.status)) return;
-      if (!wait_bar(sh, sh.bar(B_FULL0 + stage), wrap & 1, p.status)) return;
-      if (!wait_bar(sh, sh.bar(B_SFREE), (n & 1) ^ 1, p.status)) return;
-      ptx::tc_fence_after();
-      const uint32_t st = sh.stage(stage);
-      // Q_r from TMEM; the CTA's 256 c_kv dims (SW128) and 32 k_pe dims (SW64) from the page
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const uint64_t bd = ptx::smem_desc(st + (j >> 2) * kKTileC + 32 * (j & 3), 16, 1024,
-                                           ptx::kSwizzle128);
-        ptx::mma_bf16_ts(tmem + kColS, tmem + kColQ + 8 * j, bd, kIdescQK, j ? 1u : 0u);
-      }
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const uint64_t bd = ptx::smem_desc(st + 4 * kKTileC + 32 * k, 16, 512, ptx::kSwizzle64);
-        ptx::mma_bf16_ts(tmem + kColS, tmem + kColQ + 128 + 8 * k, bd, kIdescQK, 1u);
-      }
-      ptx::mma_commit(sh.bar(B_SFULL));
-      ++n;
-      if (++stage == kNS) {
-        stage = 0;
-        ++wrap;
-      }
-    }
-    ++item_idx;
-  }
-}
-
-// Output MMAs: O_r += P C_r for every page once its P is in TMEM. The page's score MMA
-// finished before its P existed, so the stage is free once this product is done.
-__device__ void pv_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker) {
-  const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
-  int stage = 0;
-  uint32_t n = 0, item_idx = 0;
-  for (int it = it0; it < it1; ++it) {
-    const WorkItem item = p.items[it];
-    for (int pg = item.page_begin; pg < item.page_end; ++pg) {
-      const bool first = (pg == item.page_begin);
-      if (!wait_bar(sh, sh.bar(B_PFULL), n & 1, p.status)) return;
-      if (first && !wait_bar(sh, sh.bar(B_OFREE), (item_idx & 1) ^ 1, p.status)) return;
-      ptx::tc_fence_after();
-      const uint32_t sb = sh.stage(stage);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint64_t bd = ptx::smem_desc(sb + 2048 * k, kKTileC, 1024, ptx::kSwizzle128);
-        ptx::mma_bf16_ts(tmem + kColO, tmem + kColP + 8 * k, bd, kIdescPV, (!first || k) ? 1u : 0u);
-      }
-      ptx::mma_commit(sh.bar(B_EMPTY0 + stage));
-      ptx::mma_commit(sh.bar(B_PVDONE));
-      ++n;
-      if (++stage == kNS) stage = 0;
-    }
-    ++item_idx;
-  }
-}
-
-// The softmax threads' view of this worker's pages, in processing order.
+// This worker's pages in processing order.
 struct PageCursor {
   const DecodeParams* p;
   int it, it1, pg;
@@ -230,129 +132,267 @@ struct PageCursor {
   }
 };
 
-// Q_r of one head row (group g) into TMEM: 256 c dims then 32 k_pe dims, two bf16 per
-// column; the row's two softmax threads store columns [0, 64) and [64, 144).
+// ------------------------------------------------------------------------------- roles
+// TMA: the k_pe part of Q_r once per work item, then the item's pages.
+__device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensorMap* tm_kc,
+                         const CUtensorMap* tm_kpe, const CUtensorMap* tm_qpe, int worker,
+                         int rank) {
+  const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
+  int stage = 0;
+  uint32_t wrap = 0, q_iter = 0;
+  for (int it = it0; it < it1; ++it) {
+    const WorkItem item = p.items[it];
+    const int g = item.group, b = g / p.q_len;
+    if (!wait_bar(sh, sh.bar(B_QPEEMPTY), (q_iter & 1) ^ 1, p.status)) return;
+    ptx::mbar_arrive_expect_tx(sh.bar(B_QPEFULL), kQPeBytes);
+    ptx::tma_load_2d(sh.qpe(), tm_qpe, kDC + 32 * rank, g * kH, sh.bar(B_QPEFULL));
+    ++q_iter;
+    for (int pg = item.page_begin; pg < item.page_end; ++pg) {
+      int page = p.block_table[(long long)b * p.max_pages + pg];
+      if (page < 0 || page >= p.num_pages) page = 0;      // masked by the softmax side
+      if (!wait_bar(sh, sh.bar(B_EMPTY0 + stage), (wrap & 1) ^ 1, p.status)) return;
+      const uint32_t full = sh.bar(B_FULL0 + stage);
+      ptx::mbar_arrive_expect_tx(full, kStageBytes);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        ptx::tma_load_2d(sh.stage(stage) + c * kKTileC, tm_kc, 256 * rank + 64 * c, page * kP, full);
+      ptx::tma_load_2d(sh.stage(stage) + 4 * kKTileC, tm_kpe, kDC + 32 * rank, page * kP, full);
+      if (++stage == kNS) {
+        stage = 0;
+        ++wrap;
+      }
+    }
+  }
+}
+
+// Score MMAs: S = Q_r K_r^T for every page, as soon as the page has landed and the
+// exchange warps have read the previous raw scores.
+__device__ void qk_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker) {
+  const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
+  int stage = 0;
+  uint32_t wrap = 0, n = 0, item_idx = 0;
+  for (int it = it0; it < it1; ++it) {
+    const WorkItem item = p.items[it];
+    for (int pg = item.page_begin; pg < item.page_end; ++pg) {
+      if (pg == item.page_begin) {
+        if (!wait_bar(sh, sh.bar(B_QFULL), item_idx & 1, p.status)) return;
+        if (!wait_bar(sh, sh.bar(B_QPEFULL), item_idx & 1, p.status)) return;
+      }
+      if (!wait_bar(sh, sh.bar(B_FULL0 + stage), wrap & 1, p.status)) return;
+      if (!wait_bar(sh, sh.bar(B_SFREE), (n & 1) ^ 1, p.status)) return;
+      ptx::tc_fence_after();
+      const uint32_t st = sh.stage(stage);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint64_t bd = ptx::smem_desc(st + (j >> 2) * kKTileC + 32 * (j & 3), 16, 1024,
+                                           ptx::kSwizzle128);
+        ptx::mma_bf16_ts(tmem + kColS, tmem + kColQ + 8 * j, bd, kIdescQK, j ? 1u : 0u);
+      }
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const uint64_t a = ptx::smem_desc(sh.qpe() + 32 * k, 16, 512, ptx::kSwizzle64);
+        const uint64_t bd = ptx::smem_desc(st + 4 * kKTileC + 32 * k, 16, 512, ptx::kSwizzle64);
+        ptx::mma_bf16_ss(tmem + kColS, a, bd, kIdescQK, 1u);
+      }
+      ptx::mma_commit(sh.bar(B_SFULL));
+      if (pg == item.page_end - 1) ptx::mma_commit(sh.bar(B_QPEEMPTY));
+      ++n;
+      if (++stage == kNS) {
+        stage = 0;
+        ++wrap;
+      }
+    }
+    ++item_idx;
+  }
+}
+
+// Output MMAs: O_r += P C_r once P is in TMEM. The page's score MMA finished before its P
+// existed, so the stage is free once this product is done.
+__device__ void pv_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker) {
+  const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
+  int stage = 0;
+  uint32_t n = 0, item_idx = 0;
+  for (int it = it0; it < it1; ++it) {
+    const WorkItem item = p.items[it];
+    for (int pg = item.page_begin; pg < item.page_end; ++pg) {
+      const bool first = (pg == item.page_begin);
+      if (!wait_bar(sh, sh.bar(B_PFULL), n & 1, p.status)) return;
+      if (first && !wait_bar(sh, sh.bar(B_OFREE), (item_idx & 1) ^ 1, p.status)) return;
+      ptx::tc_fence_after();
+      const uint32_t sb = sh.stage(stage);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint64_t bd = ptx::smem_desc(sb + 2048 * k, kKTileC, 1024, ptx::kSwizzle128);
+        ptx::mma_bf16_ts(tmem + kColO, tmem + kColC + 8 * k, bd, kIdescPV, (!first || k) ? 1u : 0u);
+      }
+      ptx::mma_commit(sh.bar(B_EMPTY0 + stage));
+      ptx::mma_commit(sh.bar(B_PVDONE));
+      ++n;
+      if (++stage == kNS) stage = 0;
+    }
+    ++item_idx;
+  }
+}
+
+// Q_r latent part of one head row (group g) into TMEM: 256 bf16, two per column.
 __device__ __forceinline__ void store_q(const DecodeParams& p, uint32_t t_row, int g, int row,
-                                        int rank, int half) {
+                                        int rank) {
   const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(p.q_lat) +
-                                                    ((long long)g * kH + row) * kD);
-  if (half == 0) {
-    uint4 a[8], b[8];
+                                                    ((long long)g * kH + row) * kD) + 32 * rank;
+  uint4 a[8], b[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) a[i] = src[32 * rank + i];
+  for (int half = 0; half < 2; ++half) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) b[i] = src[32 * rank + 8 + i];
+    for (int i = 0; i < 8; ++i) a[i] = src[16 * half + i];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b[i] = src[16 * half + 8 + i];
     uint32_t v[32];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       v[4 * i] = a[i].x; v[4 * i + 1] = a[i].y; v[4 * i + 2] = a[i].z; v[4 * i + 3] = a[i].w;
     }
-    ptx::tmem_st32(t_row + kColQ, v);
+    ptx::tmem_st32(t_row + kColQ + 64 * half, v);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       v[4 * i] = b[i].x; v[4 * i + 1] = b[i].y; v[4 * i + 2] = b[i].z; v[4 * i + 3] = b[i].w;
     }
-    ptx::tmem_st32(t_row + kColQ + 32, v);
-  } else {
-    uint4 a[8], b[8], c[4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) a[i] = src[32 * rank + 16 + i];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) b[i] = src[32 * rank + 24 + i];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) c[i] = src[64 + 4 * rank + i];
-    uint32_t v[32];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      v[4 * i] = a[i].x; v[4 * i + 1] = a[i].y; v[4 * i + 2] = a[i].z; v[4 * i + 3] = a[i].w;
-    }
-    ptx::tmem_st32(t_row + kColQ + 64, v);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      v[4 * i] = b[i].x; v[4 * i + 1] = b[i].y; v[4 * i + 2] = b[i].z; v[4 * i + 3] = b[i].w;
-    }
-    ptx::tmem_st32(t_row + kColQ + 96, v);
-    uint32_t w[16];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      w[4 * i] = c[i].x; w[4 * i + 1] = c[i].y; w[4 * i + 2] = c[i].z; w[4 * i + 3] = c[i].w;
-    }
-    ptx::tmem_st16(t_row + kColQ + 128, w);
+    ptx::tmem_st32(t_row + kColQ + 64 * half + 32, v);
   }
   ptx::tmem_wait_st();
 }
 
-__device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker,
-                                 int rank, int warp, int lane) {
+// Exchange warps: raw partial -> fp16 -> staging -> peer; peer's partial + own -> combined
+// scores in TMEM. One thread per head row, 64 scores.
+__device__ void exchange(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker, int rank,
+                         int warp, int lane) {
   const int quarter = warp & 3;
-  const int half = (warp - 2) >> 2;                      // 0: score cols 0-31, 1: cols 32-63
-  const int row = 32 * quarter + lane;                   // head index = TMEM lane
-  const int tid = 32 * (warp - 2) + lane;                // 0..255 over the softmax warps
+  const int row = 32 * quarter + lane;
   const uint32_t t_row = tmem + ((uint32_t)(32 * quarter) << 16);
   const uint32_t peer = (uint32_t)(rank ^ 1);
-  const uint32_t hoff = (uint32_t)(half * kXHalf);
-  const uint32_t peer_x_warp = ptx::map_to_rank(sh.xbuf(0), peer) + hoff + quarter * 2048;
+  const uint32_t peer_x_warp = ptx::map_to_rank(sh.xbuf(0), peer) + quarter * 4096;
   const uint32_t peer_xfull0 = ptx::map_to_rank(sh.bar(B_XFULL0), peer);
   const uint32_t peer_xempty0 = ptx::map_to_rank(sh.bar(B_XEMPTY0), peer);
-  const uint32_t stg_warp = sh.stg() + hoff + quarter * 2048;
-  uint8_t* stg_row = sh.base + kOffStg + hoff + row * 64;
-  float* red = reinterpret_cast<float*>(sh.base + kOffRed);      // [parity][half][row]
-  float* lsum = reinterpret_cast<float*>(sh.base + kOffLsum);    // [parity][half][row]
-  const int sw = (row >> 1) & 3;                         // 16-byte chunk swizzle of 64-byte rows
+  const int sw = row & 7;                                // 16-byte chunk swizzle of 128-byte rows
   PageCursor cur, ahead;
   cur.init(p, p.worker_off[worker], p.worker_off[worker + 1]);
   ahead = cur;
   if (!cur.valid()) return;
-  uint32_t sr[32];
 
   auto publish_q = [&](int g) {
-    store_q(p, t_row, g, row, rank, half);
+    store_q(p, t_row, g, row, rank);
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(sh.bar(B_QFULL));
   };
-  // own half-row of page n's partial scores -> registers -> local staging -> (one bulk copy
-  // per warp) the peer's receive buffer n & 1
-  auto fetch_and_send = [&](uint32_t n) -> bool {
+  // raw partial of page n -> fp16 staging buffer n & 1 -> (bulk copy) the peer's buffer n & 1
+  auto send = [&](uint32_t n) -> bool {
     if (!wait_bar(sh, sh.bar(B_SFULL), n & 1, p.status)) return false;
     ptx::tc_fence_after();
-    ptx::tmem_ld32(t_row + kColS + 32 * half, sr);
+    uint32_t r[64];
+    ptx::tmem_ld32(t_row + kColS, *reinterpret_cast<uint32_t(*)[32]>(r));
+    ptx::tmem_ld32(t_row + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(r + 32));
     ptx::tmem_wait_ld();
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) {
       ptx::mbar_arrive(sh.bar(B_SFREE));
-      ptx::bulk_wait_read_all();                 // the previous copy has read the staging rows
+      ptx::bulk_wait_read_le1();                 // staging buffer n & 1 (copy of n-2) is free
     }
     __syncwarp();
-    // own partial rounded to fp16 (kept in sr as the same rounded values, for the sum)
+    const uint32_t j = n & 1;
+    uint8_t* srow = sh.base + kOffStg + j * kXBytes + row * 128;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 8; ++c) {
       uint32_t w[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const __half2 h2 = __floats2half2_rn(__uint_as_float(sr[8 * c + 2 * k]),
-                                             __uint_as_float(sr[8 * c + 2 * k + 1]));
+        const __half2 h2 = __floats2half2_rn(__uint_as_float(r[8 * c + 2 * k]),
+                                             __uint_as_float(r[8 * c + 2 * k + 1]));
         w[k] = *reinterpret_cast<const uint32_t*>(&h2);
-        const float2 back = __half22float2(h2);
-        sr[8 * c + 2 * k] = __float_as_uint(back.x);
-        sr[8 * c + 2 * k + 1] = __float_as_uint(back.y);
       }
-      *reinterpret_cast<uint4*>(stg_row + ((c ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(srow + ((c ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
     ptx::fence_proxy_async_smem();
     __syncwarp();
-    const uint32_t j = n & 1;
     int ok = 1;
     if (lane == 0) {
       ok = wait_bar(sh, sh.bar(B_XEMPTY0 + j), ((n >> 1) & 1) ^ 1, p.status, true) ? 1 : 0;
       if (ok) {
-        ptx::bulk_s2s(peer_x_warp + j * kXBytes, stg_warp, 2048, peer_xfull0 + 8 * j);
+        ptx::bulk_s2s(peer_x_warp + j * kXBytes, sh.stg(j) + quarter * 4096, 4096,
+                      peer_xfull0 + 8 * j);
         ptx::bulk_commit();
       }
     }
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
   };
+
+  publish_q(cur.item.group);
+  if (!send(0)) return;
+  ahead.next();
+  uint32_t n = 0;
+  while (cur.valid()) {
+    // ship page n+1 first (a page that opens the next work item needs that item's Q_r:
+    // every score MMA of the current item is done, since page n's raw scores were read)
+    if (ahead.valid()) {
+      if (ahead.first()) publish_q(ahead.item.group);
+      if (!send(n + 1)) return;
+      ahead.next();
+    }
+    // combine page n: own fp16 partial (staging n & 1) + the peer's (receive buffer n & 1)
+    const uint32_t j = n & 1;
+    if (!wait_bar(sh, sh.bar(B_XFULL0 + j), (n >> 1) & 1, p.status, true)) return;
+    if (warp == 2 && lane == 0) ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL0 + j), kXBytes);
+    const uint8_t* xrow = sh.base + kOffX + j * kXBytes + row * 128;
+    const uint8_t* srow = sh.base + kOffStg + j * kXBytes + row * 128;
+    uint32_t cs[64];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 a = *reinterpret_cast<const uint4*>(xrow + ((c ^ sw) * 16));
+      const uint4 b = *reinterpret_cast<const uint4*>(srow + ((c ^ sw) * 16));
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&av[k]));
+        const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&bv[k]));
+        cs[8 * c + 2 * k] = __float_as_uint(fa.x + fb.x);
+        cs[8 * c + 2 * k + 1] = __float_as_uint(fa.y + fb.y);
+      }
+    }
+    {
+      // every lane's buffer reads have returned before lane 0 tells the peer it may refill
+      uint32_t dep = 0;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) dep ^= cs[8 * c];
+      const uint32_t all = __ballot_sync(0xffffffffu, dep != 0x7fc00001u);
+      if (lane == 0) ptx::mbar_arrive_remote_relaxed(peer_xempty0 + 8 * j, all);
+    }
+    // the combined-score buffer still holds P of page n-1 until its P.C product is done
+    if (n > 0 && !wait_bar(sh, sh.bar(B_PVDONE), (n - 1) & 1, p.status)) return;
+    ptx::tc_fence_after();
+    ptx::tmem_st32(t_row + kColC, *reinterpret_cast<uint32_t(*)[32]>(cs));
+    ptx::tmem_st32(t_row + kColC + 32, *reinterpret_cast<uint32_t(*)[32]>(cs + 32));
+    ptx::tmem_wait_st();
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(sh.bar(B_CFULL));
+    ++n;
+    cur.next();
+  }
+}
+
+// Softmax warps: combined scores -> online softmax -> P over the same TMEM columns; the
+// item's output at its last page.
+__device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker,
+                                 int rank, int warp, int lane) {
+  const int quarter = warp & 3;
+  const int row = 32 * quarter + lane;
+  const int tid = 32 * (warp - 6) + lane;                // 0..127 over the softmax warps
+  const uint32_t t_row = tmem + ((uint32_t)(32 * quarter) << 16);
+  PageCursor cur, ahead;
+  cur.init(p, p.worker_off[worker], p.worker_off[worker + 1]);
+  if (!cur.valid()) return;
+  ahead = cur;
+  ahead.next();
   // block-table entry and key count of a page, loaded one page before they are used
   auto load_meta = [&](const PageCursor& c, int* page, int* kv) {
     const int gg = c.item.group;
@@ -361,12 +401,8 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
   };
   int page_cur = 0, kv_cur = 0, page_nxt = 0, kv_nxt = 0;
   load_meta(cur, &page_cur, &kv_cur);
-  publish_q(cur.item.group);
-  if (!fetch_and_send(0)) return;
-  ahead.next();
-
-  uint32_t n = 0, item_idx = 0;
-  float m_used = -INFINITY, l = 0.f;                     // l: this half's share of the row sum
+  uint32_t n = 0;
+  float m_used = -INFINITY, l = 0.f;
   while (cur.valid()) {
     const WorkItem item = cur.item;
     const int pg = cur.pg;
@@ -375,74 +411,40 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
       m_used = -INFINITY;
       l = 0.f;
     }
+    if (ahead.valid()) load_meta(ahead, &page_nxt, &kv_nxt);
     const bool valid = page_cur >= 0 && page_cur < p.num_pages;
+    if (!valid && row == 0 && rank == 0) flag_status(p.status, MLA_ERR_DEVICE_GUARD);
     const int ntok = valid ? min(kP, kv_cur - pg * kP) : 0;
 
-    // 1. the peer's partial of page n (receive buffer n & 1): s = own + peer
-    const uint32_t jx = n & 1;
-    if (!wait_bar(sh, sh.bar(B_XFULL0 + jx), (n >> 1) & 1, p.status, true)) return;
-    if (warp == 2 && lane == 0) ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL0 + jx), kXBytes);
-    const uint8_t* xrow = sh.base + kOffX + jx * kXBytes + hoff + row * 64;
-    float s[32];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint4 v = *reinterpret_cast<const uint4*>(xrow + ((c ^ sw) * 16));
-      const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&vv[k]));
-        s[8 * c + 2 * k] = __uint_as_float(sr[8 * c + 2 * k]) + f.x;
-        s[8 * c + 2 * k + 1] = __uint_as_float(sr[8 * c + 2 * k + 1]) + f.y;
-      }
-    }
-    {
-      // every lane's buffer reads have returned before lane 0 tells the peer it may refill
-      uint32_t dep = 0;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) dep ^= __float_as_uint(s[8 * c]);
-      const uint32_t all = __ballot_sync(0xffffffffu, dep != 0x7fc00001u);
-      if (lane == 0) ptx::mbar_arrive_remote_relaxed(peer_xempty0 + 8 * jx, all);
-    }
-
-    // 2. own partial of page n+1 (computed one page ahead by the score MMAs) -> peer; a page
-    // that opens the next work item needs that item's Q_r in TMEM first (every score MMA of
-    // the current item is done: its last scores, page n's, are already read)
-    if (ahead.valid()) {
-      if (ahead.first()) publish_q(ahead.item.group);
-      load_meta(ahead, &page_nxt, &kv_nxt);
-      if (!fetch_and_send(n + 1)) return;
-      ahead.next();
-    }
-    if (!valid && row == 0 && half == 0 && rank == 0) flag_status(p.status, MLA_ERR_DEVICE_GUARD);
-
-    // 3. softmax of page n. Rows past the last token (or a whole skipped page) may hold
-    // anything, NaN included, and 0 * NaN would poison O: zero them in the staged c_kv
-    // tiles before the P . C product reads them (the QK product that read them is done).
+    if (!wait_bar(sh, sh.bar(B_CFULL), n & 1, p.status)) return;
+    ptx::tc_fence_after();
+    uint32_t sr[64];
+    ptx::tmem_ld32(t_row + kColC, *reinterpret_cast<uint32_t(*)[32]>(sr));
+    ptx::tmem_ld32(t_row + kColC + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+    ptx::tmem_wait_ld();
+    float* s = reinterpret_cast<float*>(sr);
+    // Rows past the last token (or a whole skipped page) may hold anything, NaN included,
+    // and 0 * NaN would poison O: zero them in the staged c_kv tiles before the P . C
+    // product reads them (the score MMA that read them is done).
     bool zeroed = false;
     if (ntok < kP) {
       uint8_t* stg = sh.base + kOffStage + (int)(n % kNS) * kStageBytes;
       const int nrows = kP - ntok;
       const int per_tile = nrows * 8;
-      for (int i = tid; i < 4 * per_tile; i += 32 * kSoftmaxWarps) {
+      for (int i = tid; i < 4 * per_tile; i += 128) {
         const int tile = i / per_tile, rem = i % per_tile;
         *reinterpret_cast<uint4*>(stg + tile * kKTileC + (ntok + rem / 8) * 128 + (rem % 8) * 16) =
             make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (32 * half + i >= ntok) s[i] = -INFINITY;
+      for (int i = 0; i < 64; ++i)
+        if (i >= ntok) s[i] = -INFINITY;
       zeroed = true;
     }
-    float hm = s[0];
+    float mx = s[0];
 #pragma unroll
-    for (int i = 1; i < 32; ++i) hm = fmaxf(hm, s[i]);
-    // combine the two halves' maxima of this row
-    float* redp = red + (int)(n & 1) * 256;
-    redp[half * 128 + row] = hm;
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(sh.bar(B_RMAX0 + (n & 1)));
-    if (!wait_bar(sh, sh.bar(B_RMAX0 + (n & 1)), (n >> 1) & 1, p.status)) return;
-    const float mx = fmaxf(hm, redp[(half ^ 1) * 128 + row]) * p.scale_log2;
+    for (int i = 1; i < 64; ++i) mx = fmaxf(mx, s[i]);
+    mx *= p.scale_log2;
     bool rescale = false;
     float alpha = 1.f;
     if (mx > -INFINITY) {
@@ -455,15 +457,15 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
         rescale = true;
       }
     }
-    uint32_t packed[16];
+    uint32_t packed[32];
     if (m_used == -INFINITY) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) packed[i] = 0u;
+      for (int i = 0; i < 32; ++i) packed[i] = 0u;
     } else {
       const float neg_m = -m_used;
       float psum = 0.f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < 32; ++i) {
         const float p0 = ptx::ex2(fmaf(s[2 * i], p.scale_log2, neg_m));
         const float p1 = ptx::ex2(fmaf(s[2 * i + 1], p.scale_log2, neg_m));
         psum += p0 + p1;
@@ -472,47 +474,39 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
       }
       l += psum;
     }
-    // the previous P . C product must be done before P or O are touched
-    if (n > 0 && !wait_bar(sh, sh.bar(B_PVDONE), (n - 1) & 1, p.status)) return;
-    ptx::tc_fence_after();
+    // O is stable here: the previous P . C product finished before these scores were
+    // written, and this page's product waits for P below
     if (rescale) {
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 8; ++c) {
         uint32_t v[32];
-        const uint32_t a = t_row + kColO + 128 * half + 32 * c;
-        ptx::tmem_ld32(a, v);
+        ptx::tmem_ld32(t_row + kColO + 32 * c, v);
         ptx::tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-        ptx::tmem_st32(a, v);
+        ptx::tmem_st32(t_row + kColO + 32 * c, v);
       }
     }
-    ptx::tmem_st16(t_row + kColP + 16 * half, packed);
+    ptx::tmem_st32(t_row + kColC, packed);
     ptx::tmem_wait_st();
     if (zeroed) ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(sh.bar(B_PFULL));
 
-    // 4. after the item's last page: normalise this half of O_r and write it
+    // after the item's last page: normalise O_r and write it (output or split partial)
     if (cur.last()) {
       const int it = cur.it;
-      float* ls = lsum + (int)(item_idx & 1) * 256;
-      ls[half * 128 + row] = l;
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(sh.bar(B_LSUM0 + (item_idx & 1)));
-      if (!wait_bar(sh, sh.bar(B_LSUM0 + (item_idx & 1)), (item_idx >> 1) & 1, p.status)) return;
-      const float lt = l + ls[(half ^ 1) * 128 + row];
       if (!wait_bar(sh, sh.bar(B_PVDONE), n & 1, p.status)) return;
       ptx::tc_fence_after();
-      const float inv = (lt > 0.f) ? p.out_scale / lt : 0.f;
-      const float lse_v = (lt > 0.f) ? (m_used + log2f(lt)) * kLn2 : -INFINITY;
+      const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
+      const float lse_v = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 8; ++c) {
         uint32_t v[32];
-        ptx::tmem_ld32(t_row + kColO + 128 * half + 32 * c, v);
+        ptx::tmem_ld32(t_row + kColO + 32 * c, v);
         ptx::tmem_wait_ld();
-        const int col = 256 * rank + 128 * half + 32 * c;
+        const int col = 256 * rank + 32 * c;
         if (item.single) {
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out_latent) +
                                                 ((long long)g * kH + row) * kDC + col);
@@ -538,14 +532,14 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(sh.bar(B_OFREE));
-      if (rank == 0 && half == 0) {
+      if (rank == 0) {
         if (item.single) p.lse[(long long)g * kH + row] = lse_v;
         else p.part_lse[(long long)it * kH + row] = lse_v;
       }
-      ++item_idx;
     }
     ++n;
     cur.next();
+    if (ahead.valid()) ahead.next();
     page_cur = page_nxt;
     kv_cur = kv_nxt;
   }
@@ -553,7 +547,8 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
-                     const __grid_constant__ CUtensorMap tm_kpe, const DecodeParams p) {
+                     const __grid_constant__ CUtensorMap tm_kpe,
+                     const __grid_constant__ CUtensorMap tm_qpe, const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   Shared sh;
   const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -571,21 +566,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ptx::mbar_init(sh.bar(B_FULL0 + s), 1);
       ptx::mbar_init(sh.bar(B_EMPTY0 + s), 1);
     }
-    ptx::mbar_init(sh.bar(B_QFULL), kSoftmaxWarps);
+    ptx::mbar_init(sh.bar(B_QFULL), 4);
+    ptx::mbar_init(sh.bar(B_QPEFULL), 1);
+    ptx::mbar_init(sh.bar(B_QPEEMPTY), 1);
     ptx::mbar_init(sh.bar(B_SFULL), 1);
-    ptx::mbar_init(sh.bar(B_SFREE), kSoftmaxWarps);
-    ptx::mbar_init(sh.bar(B_PFULL), kSoftmaxWarps);
+    ptx::mbar_init(sh.bar(B_SFREE), 4);
+    ptx::mbar_init(sh.bar(B_CFULL), 4);
+    ptx::mbar_init(sh.bar(B_PFULL), 4);
     ptx::mbar_init(sh.bar(B_PVDONE), 1);
     ptx::mbar_init(sh.bar(B_XFULL0), 1);
     ptx::mbar_init(sh.bar(B_XFULL1), 1);
-    ptx::mbar_init(sh.bar(B_XEMPTY0), kSoftmaxWarps);
-    ptx::mbar_init(sh.bar(B_XEMPTY1), kSoftmaxWarps);
-    ptx::mbar_init(sh.bar(B_OFREE), kSoftmaxWarps);
+    ptx::mbar_init(sh.bar(B_XEMPTY0), 4);
+    ptx::mbar_init(sh.bar(B_XEMPTY1), 4);
+    ptx::mbar_init(sh.bar(B_OFREE), 4);
     ptx::mbar_init(sh.bar(B_TEARDOWN), 2);
-    ptx::mbar_init(sh.bar(B_RMAX0), kSoftmaxWarps);
-    ptx::mbar_init(sh.bar(B_RMAX1), kSoftmaxWarps);
-    ptx::mbar_init(sh.bar(B_LSUM0), kSoftmaxWarps);
-    ptx::mbar_init(sh.bar(B_LSUM1), kSoftmaxWarps);
     *sh.abort = 0;
     ptx::fence_mbar_init();
     // first phase of each receive buffer (the peer's partials of pages 0 and 1)
@@ -593,6 +587,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL1), kXBytes);
     ptx::prefetch_tensormap(&tm_kc);
     ptx::prefetch_tensormap(&tm_kpe);
+    ptx::prefetch_tensormap(&tm_qpe);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(sh.tmem_slot), kTmemCols);
@@ -605,19 +600,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *sh.tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) producer(sh, p, &tm_kc, &tm_kpe, worker, rank);
+    if (lane == 0) producer(sh, p, &tm_kc, &tm_kpe, &tm_qpe, worker, rank);
   } else if (warp == 1) {
     if (lane == 0) qk_issuer(sh, p, tmem, worker);
-  } else if (warp == 10) {
-    if (lane == 0) pv_issuer(sh, p, tmem, worker);
-  } else {
+  } else if (warp <= 5) {
+    exchange(sh, p, tmem, worker, rank, warp, lane);
+  } else if (warp <= 9) {
     softmax_epilogue(sh, p, tmem, worker, rank, warp, lane);
+  } else {
+    if (lane == 0) pv_issuer(sh, p, tmem, worker);
   }
 
   // teardown: every role gets here, normally or after a bounded wait gave up
   // both MMA issuers commit: every issued MMA must have finished before TMEM is released
   if ((warp == 1 || warp == 10) && lane == 0) ptx::mma_commit(sh.bar(B_TEARDOWN));
-  if (warp >= 2 && warp <= 9 && lane == 0) ptx::bulk_wait_read_all();
+  if (warp >= 2 && warp <= 5 && lane == 0) ptx::bulk_wait_read_all();
   __syncthreads();
   if (warp == 1) {
     if (lane == 0) {
@@ -706,15 +703,17 @@ int tc_decode_max_workers() {
 
 cudaError_t launch_decode_tc(mla_dtype cache, const DecodeParams& p, cudaStream_t s) {
   if (cache != MLA_BF16) return cudaErrorNotSupported;
-  CUtensorMap kc, kpe;
+  CUtensorMap kc, kpe, qpe;
   const uint64_t cache_rows = (uint64_t)p.num_pages * tc::kP;
+  const uint64_t q_rows = (uint64_t)p.batch * p.q_len * tc::kH;
   if (!tc::make_map(&kc, p.cache, cache_rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tc::make_map(&kpe, p.cache, cache_rows, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))
+      !tc::make_map(&kpe, p.cache, cache_rows, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !tc::make_map(&qpe, p.q_lat, q_rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(tc::decode_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
   if (e != cudaSuccess) return e;
-  tc::decode_tc_kernel<<<2 * p.workers, tc::kThreads, tc::kSmemBytes, s>>>(kc, kpe, p);
+  tc::decode_tc_kernel<<<2 * p.workers, tc::kThreads, tc::kSmemBytes, s>>>(kc, kpe, qpe, p);
   note_launch();
   return cudaGetLastError();
 }
