@@ -23,13 +23,13 @@
 //      head row, exp2, O rescaled lazily, only when the running maximum grows by more
 //      than 2^8) and write P (bf16) over the same TMEM buffer,
 //   5. O_r += P C_r (M = 128, N = 256, K = 64; A = P from TMEM, B = the staged page).
-// The exchange warps run one page ahead of the softmax warps (they ship page n+1's
-// partial before combining page n), so the cluster transfer, the score MMAs and the
-// softmax of consecutive pages overlap.
+// Three 4-warp groups pipeline consecutive pages: send warps ship page n+1's partial
+// while combine warps merge page n and softmax warps process page n-1, so the cluster
+// transfer, the score MMAs and the softmax overlap.
 // Roles: warp 0 issues TMA; warp 1 issues the score MMAs and owns the TMEM allocation;
-// warps 2-5 exchange scores and load Q_r into TMEM at each work item's start; warps 6-9
-// run the softmax and write the outputs; warp 10 issues the P.C MMAs. A thread of warps
-// 2-9 owns one head row = one TMEM lane.
+// warps 2-5 send partial scores and load Q_r into TMEM at each work item's start; warps
+// 6-9 combine the partials; warps 10-13 run the softmax and write the outputs; warp 14
+// issues the P.C MMAs. A thread of warps 2-13 owns one head row = one TMEM lane.
 // TMEM: O_r 256 columns, raw S 64, combined S / P 64, Q_r latent part 128.
 // Every mbarrier wait is bounded (2 s): on timeout the kernel records MLA_ERR_TIMEOUT,
 // every role leaves its loop, TMEM is freed and the pair meets at a final cluster
@@ -56,13 +56,13 @@ constexpr int kOffX = kOffStage + kNS * kStageBytes;     // two receive buffers
 constexpr int kOffStg = kOffX + 2 * kXBytes;             // two staging buffers (own partial)
 constexpr int kOffQPe = kOffStg + 2 * kXBytes;
 constexpr int kOffBar = kOffQPe + kQPeBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;         // + slack to align the base to 1 KB
+constexpr int kSmemBytes = kOffBar + 320 + 1024;         // + slack to align the base to 1 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;                            // O_r: 256 fp32 columns
 constexpr uint32_t kColS = 256;                          // raw partial S: 64 fp32 columns
 constexpr uint32_t kColC = 320;                          // combined S (fp32), then P (bf16)
 constexpr uint32_t kColQ = 384;                          // Q_r latent part: 256 bf16 = 128
-constexpr int kThreads = 352;                            // 11 warps
+constexpr int kThreads = 480;                            // 15 warps
 constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, 256, false, true);
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -71,9 +71,9 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 enum {
   B_FULL0 = 0, B_EMPTY0 = kNS, B_QFULL = 2 * kNS, B_QPEFULL, B_QPEEMPTY, B_SFULL, B_SFREE,
   B_CFULL, B_PFULL, B_PVDONE, B_XFULL0, B_XFULL1, B_XEMPTY0, B_XEMPTY1, B_OFREE, B_TEARDOWN,
-  B_COUNT
+  B_STGREADY0, B_STGREADY1, B_STGFREE0, B_STGFREE1, B_COUNT
 };
-static_assert(B_COUNT * 8 <= 192, "barrier area");
+static_assert(B_COUNT * 8 <= 240, "barrier area");
 
 struct Shared {
   uint8_t* base;       // 1 KB aligned
@@ -261,32 +261,30 @@ __device__ __forceinline__ void store_q(const DecodeParams& p, uint32_t t_row, i
   ptx::tmem_wait_st();
 }
 
-// Exchange warps: raw partial -> fp16 -> staging -> peer; peer's partial + own -> combined
-// scores in TMEM. One thread per head row, 64 scores.
-__device__ void exchange(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker, int rank,
-                         int warp, int lane) {
+// Send warps: raw partial of every page -> fp16 -> staging buffer n & 1 -> (bulk copy)
+// the peer's receive buffer n & 1; Q_r's latent part into TMEM at each item's start.
+__device__ void send_warps(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker, int rank,
+                           int warp, int lane) {
   const int quarter = warp & 3;
   const int row = 32 * quarter + lane;
   const uint32_t t_row = tmem + ((uint32_t)(32 * quarter) << 16);
   const uint32_t peer = (uint32_t)(rank ^ 1);
   const uint32_t peer_x_warp = ptx::map_to_rank(sh.xbuf(0), peer) + quarter * 4096;
   const uint32_t peer_xfull0 = ptx::map_to_rank(sh.bar(B_XFULL0), peer);
-  const uint32_t peer_xempty0 = ptx::map_to_rank(sh.bar(B_XEMPTY0), peer);
   const int sw = row & 7;                                // 16-byte chunk swizzle of 128-byte rows
-  PageCursor cur, ahead;
+  PageCursor cur;
   cur.init(p, p.worker_off[worker], p.worker_off[worker + 1]);
-  ahead = cur;
-  if (!cur.valid()) return;
-
-  auto publish_q = [&](int g) {
-    store_q(p, t_row, g, row, rank);
-    ptx::tc_fence_before();
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(sh.bar(B_QFULL));
-  };
-  // raw partial of page n -> fp16 staging buffer n & 1 -> (bulk copy) the peer's buffer n & 1
-  auto send = [&](uint32_t n) -> bool {
-    if (!wait_bar(sh, sh.bar(B_SFULL), n & 1, p.status)) return false;
+  uint32_t n = 0;
+  while (cur.valid()) {
+    // a page that opens a work item needs that item's Q_r: every score MMA of the previous
+    // item is done, since the previous page's raw scores were read
+    if (cur.first()) {
+      store_q(p, t_row, cur.item.group, row, rank);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(sh.bar(B_QFULL));
+    }
+    if (!wait_bar(sh, sh.bar(B_SFULL), n & 1, p.status)) return;
     ptx::tc_fence_after();
     uint32_t r[64];
     ptx::tmem_ld32(t_row + kColS, *reinterpret_cast<uint32_t(*)[32]>(r));
@@ -294,12 +292,15 @@ __device__ void exchange(const Shared& sh, const DecodeParams& p, uint32_t tmem,
     ptx::tmem_wait_ld();
     ptx::tc_fence_before();
     __syncwarp();
+    const uint32_t j = n & 1;
+    int ok = 1;
     if (lane == 0) {
       ptx::mbar_arrive(sh.bar(B_SFREE));
-      ptx::bulk_wait_read_le1();                 // staging buffer n & 1 (copy of n-2) is free
+      // staging buffer j: the combine warps have read page n-2 and its copy has read it too
+      ok = wait_bar(sh, sh.bar(B_STGFREE0 + j), ((n >> 1) & 1) ^ 1, p.status) ? 1 : 0;
+      ptx::bulk_wait_read_le1();
     }
-    __syncwarp();
-    const uint32_t j = n & 1;
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
     uint8_t* srow = sh.base + kOffStg + j * kXBytes + row * 128;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
@@ -314,8 +315,8 @@ __device__ void exchange(const Shared& sh, const DecodeParams& p, uint32_t tmem,
     }
     ptx::fence_proxy_async_smem();
     __syncwarp();
-    int ok = 1;
     if (lane == 0) {
+      ptx::mbar_arrive(sh.bar(B_STGREADY0 + j));
       ok = wait_bar(sh, sh.bar(B_XEMPTY0 + j), ((n >> 1) & 1) ^ 1, p.status, true) ? 1 : 0;
       if (ok) {
         ptx::bulk_s2s(peer_x_warp + j * kXBytes, sh.stg(j) + quarter * 4096, 4096,
@@ -323,25 +324,30 @@ __device__ void exchange(const Shared& sh, const DecodeParams& p, uint32_t tmem,
         ptx::bulk_commit();
       }
     }
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
-  };
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+    ++n;
+    cur.next();
+  }
+}
 
-  publish_q(cur.item.group);
-  if (!send(0)) return;
-  ahead.next();
-  uint32_t n = 0;
-  while (cur.valid()) {
-    // ship page n+1 first (a page that opens the next work item needs that item's Q_r:
-    // every score MMA of the current item is done, since page n's raw scores were read)
-    if (ahead.valid()) {
-      if (ahead.first()) publish_q(ahead.item.group);
-      if (!send(n + 1)) return;
-      ahead.next();
-    }
-    // combine page n: own fp16 partial (staging n & 1) + the peer's (receive buffer n & 1)
+// Combine warps: own fp16 partial (staging n & 1) + the peer's (receive buffer n & 1) ->
+// combined scores in TMEM, once P of page n-1 (same columns) has been consumed.
+__device__ void combine_warps(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker,
+                              int rank, int warp, int lane) {
+  const int quarter = warp & 3;
+  const int row = 32 * quarter + lane;
+  const uint32_t t_row = tmem + ((uint32_t)(32 * quarter) << 16);
+  const uint32_t peer = (uint32_t)(rank ^ 1);
+  const uint32_t peer_xempty0 = ptx::map_to_rank(sh.bar(B_XEMPTY0), peer);
+  const int sw = row & 7;
+  const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
+  uint32_t total = 0;
+  for (int it = it0; it < it1; ++it) total += p.items[it].page_end - p.items[it].page_begin;
+  for (uint32_t n = 0; n < total; ++n) {
     const uint32_t j = n & 1;
     if (!wait_bar(sh, sh.bar(B_XFULL0 + j), (n >> 1) & 1, p.status, true)) return;
-    if (warp == 2 && lane == 0) ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL0 + j), kXBytes);
+    if (warp == 6 && lane == 0) ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL0 + j), kXBytes);
+    if (!wait_bar(sh, sh.bar(B_STGREADY0 + j), (n >> 1) & 1, p.status)) return;
     const uint8_t* xrow = sh.base + kOffX + j * kXBytes + row * 128;
     const uint8_t* srow = sh.base + kOffStg + j * kXBytes + row * 128;
     uint32_t cs[64];
@@ -359,12 +365,15 @@ __device__ void exchange(const Shared& sh, const DecodeParams& p, uint32_t tmem,
       }
     }
     {
-      // every lane's buffer reads have returned before lane 0 tells the peer it may refill
+      // every lane's buffer reads have returned before the buffers are released
       uint32_t dep = 0;
 #pragma unroll
       for (int c = 0; c < 8; ++c) dep ^= cs[8 * c];
       const uint32_t all = __ballot_sync(0xffffffffu, dep != 0x7fc00001u);
-      if (lane == 0) ptx::mbar_arrive_remote_relaxed(peer_xempty0 + 8 * j, all);
+      if (lane == 0) {
+        ptx::mbar_arrive_remote_relaxed(peer_xempty0 + 8 * j, all);
+        ptx::mbar_arrive(sh.bar(B_STGFREE0 + j));
+      }
     }
     // the combined-score buffer still holds P of page n-1 until its P.C product is done
     if (n > 0 && !wait_bar(sh, sh.bar(B_PVDONE), (n - 1) & 1, p.status)) return;
@@ -375,8 +384,6 @@ __device__ void exchange(const Shared& sh, const DecodeParams& p, uint32_t tmem,
     ptx::tc_fence_before();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(sh.bar(B_CFULL));
-    ++n;
-    cur.next();
   }
 }
 
@@ -386,7 +393,7 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
                                  int rank, int warp, int lane) {
   const int quarter = warp & 3;
   const int row = 32 * quarter + lane;
-  const int tid = 32 * (warp - 6) + lane;                // 0..127 over the softmax warps
+  const int tid = 32 * (warp - 10) + lane;               // 0..127 over the softmax warps
   const uint32_t t_row = tmem + ((uint32_t)(32 * quarter) << 16);
   PageCursor cur, ahead;
   cur.init(p, p.worker_off[worker], p.worker_off[worker + 1]);
@@ -555,8 +562,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t aligned = (raw + 1023u) & ~1023u;
   sh.base = smem_raw + (aligned - raw);
   sh.base_u32 = aligned;
-  sh.abort = reinterpret_cast<volatile int*>(sh.base + kOffBar + 192);
-  sh.tmem_slot = reinterpret_cast<uint32_t*>(sh.base + kOffBar + 200);
+  sh.abort = reinterpret_cast<volatile int*>(sh.base + kOffBar + 256);
+  sh.tmem_slot = reinterpret_cast<uint32_t*>(sh.base + kOffBar + 264);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (int)ptx::cluster_ctarank();
   const int worker = blockIdx.x >> 1;
@@ -580,6 +587,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::mbar_init(sh.bar(B_XEMPTY1), 4);
     ptx::mbar_init(sh.bar(B_OFREE), 4);
     ptx::mbar_init(sh.bar(B_TEARDOWN), 2);
+    ptx::mbar_init(sh.bar(B_STGREADY0), 4);
+    ptx::mbar_init(sh.bar(B_STGREADY1), 4);
+    ptx::mbar_init(sh.bar(B_STGFREE0), 4);
+    ptx::mbar_init(sh.bar(B_STGFREE1), 4);
     *sh.abort = 0;
     ptx::fence_mbar_init();
     // first phase of each receive buffer (the peer's partials of pages 0 and 1)
@@ -604,8 +615,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) qk_issuer(sh, p, tmem, worker);
   } else if (warp <= 5) {
-    exchange(sh, p, tmem, worker, rank, warp, lane);
+    send_warps(sh, p, tmem, worker, rank, warp, lane);
   } else if (warp <= 9) {
+    combine_warps(sh, p, tmem, worker, rank, warp, lane);
+  } else if (warp <= 13) {
     softmax_epilogue(sh, p, tmem, worker, rank, warp, lane);
   } else {
     if (lane == 0) pv_issuer(sh, p, tmem, worker);
@@ -613,7 +626,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   // teardown: every role gets here, normally or after a bounded wait gave up
   // both MMA issuers commit: every issued MMA must have finished before TMEM is released
-  if ((warp == 1 || warp == 10) && lane == 0) ptx::mma_commit(sh.bar(B_TEARDOWN));
+  if ((warp == 1 || warp == 14) && lane == 0) ptx::mma_commit(sh.bar(B_TEARDOWN));
   if (warp >= 2 && warp <= 5 && lane == 0) ptx::bulk_wait_read_all();
   __syncthreads();
   if (warp == 1) {
