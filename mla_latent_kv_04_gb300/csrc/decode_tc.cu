@@ -14,23 +14,28 @@
 //   2. computes its partial score S_r = Q_r K_r^T (M = 128 heads, N = 64 tokens, K = 288)
 //      into TMEM (A = the latent part of Q_r held in TMEM, and the k_pe part from shared
 //      memory),
-//   3. exchange warps read S_r, round it to fp16, stage it in shared memory and move it
-//      with one bulk copy per warp into one of the peer's two receive buffers (counted
-//      on the peer's mbarrier); when the peer's partial arrives they write the combined
-//      scores f16(S_0) + f16(S_1) (identical in both CTAs; the fp16 rounding, relative
-//      2^-11, is below the bf16 rounding of P) into a second TMEM buffer,
-//   4. softmax warps read the combined scores, run the online softmax (one thread per
-//      head row, exp2, O rescaled lazily, only when the running maximum grows by more
-//      than 2^8) and write P (bf16) over the same TMEM buffer,
+//   3. send warps read S_r, round it to fp16 (columns past the last token as 0, values
+//      beyond the fp16 range saturated), stage it in shared memory and move it with one
+//      bulk copy per warp into one of the peer's two receive buffers (counted on the peer's
+//      mbarrier),
+//   4. softmax warps combine the peer's fp16 partial with their own staged fp16 partial
+//      (identical combined scores f16(S_0) + f16(S_1) in both CTAs; the fp16 rounding,
+//      relative 2^-11, is below the bf16 rounding of P), run the online softmax (one thread
+//      per head row, exp2, O rescaled lazily, only when the running maximum grows by more
+//      than 2^8) and write P (bf16) into one of two TMEM buffers,
 //   5. O_r += P C_r (M = 128, N = 256, K = 64; A = P from TMEM, B = the staged page).
-// Three 4-warp groups pipeline consecutive pages: send warps ship page n+1's partial
-// while combine warps merge page n and softmax warps process page n-1, so the cluster
-// transfer, the score MMAs and the softmax overlap.
+// The query arrives pre-multiplied by softmax_scale * log2(e), so scores are already in
+// log2 units: the softmax forms each exponent as (f32) own half + (f32) peer half - m with
+// two mixed fp16/fp32 adds, and takes the running maximum on packed fp16 sums.
+// The send warps run ahead of the softmax warps, so the cluster transfer, the score MMAs
+// and the softmax of consecutive pages overlap.
 // Roles: warp 0 issues TMA; warp 1 issues the score MMAs and owns the TMEM allocation;
 // warps 2-5 send partial scores and load Q_r into TMEM at each work item's start; warps
-// 6-9 combine the partials; warps 10-13 run the softmax and write the outputs; warp 14
-// issues the P.C MMAs. A thread of warps 2-13 owns one head row = one TMEM lane.
-// TMEM: O_r 256 columns, raw S 64, combined S / P 64, Q_r latent part 128.
+// 6-9 combine the partials, run the softmax and write the outputs; warp 10 issues the P.C
+// MMAs. A thread of warps 2-9 owns one head row = one TMEM lane.
+// TMEM: O_r 256 columns, raw S 64, P 2 x 32, Q_r latent part 128.
+// Split partials are written [item][d_c / 4][128 heads][4] fp32, so the 32 threads of a
+// warp (32 consecutive heads) store one contiguous 512-byte run per instruction.
 // Every mbarrier wait is bounded (2 s): on timeout the kernel records MLA_ERR_TIMEOUT,
 // every role leaves its loop, TMEM is freed and the pair meets at a final cluster
 // barrier before exit.
@@ -60,9 +65,9 @@ constexpr int kSmemBytes = kOffBar + 320 + 1024;         // + slack to align the
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;                            // O_r: 256 fp32 columns
 constexpr uint32_t kColS = 256;                          // raw partial S: 64 fp32 columns
-constexpr uint32_t kColC = 320;                          // combined S (fp32), then P (bf16)
+constexpr uint32_t kColP = 320;                          // P: two buffers of 64 bf16 = 32
 constexpr uint32_t kColQ = 384;                          // Q_r latent part: 256 bf16 = 128
-constexpr int kThreads = 480;                            // 15 warps
+constexpr int kThreads = 352;                            // 11 warps
 constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, 256, false, true);
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -70,7 +75,7 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 // mbarrier slots (8 bytes each) at kOffBar
 enum {
   B_FULL0 = 0, B_EMPTY0 = kNS, B_QFULL = 2 * kNS, B_QPEFULL, B_QPEEMPTY, B_SFULL, B_SFREE,
-  B_CFULL, B_PFULL, B_PVDONE, B_XFULL0, B_XFULL1, B_XEMPTY0, B_XEMPTY1, B_OFREE, B_TEARDOWN,
+  B_PFULL0, B_PFULL1, B_PVDONE0, B_PVDONE1, B_XFULL0, B_XFULL1, B_XEMPTY0, B_XEMPTY1, B_OFREE, B_TEARDOWN,
   B_STGREADY0, B_STGREADY1, B_STGFREE0, B_STGFREE1, B_COUNT
 };
 static_assert(B_COUNT * 8 <= 240, "barrier area");
@@ -107,15 +112,15 @@ __device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_
 
 // This worker's pages in processing order.
 struct PageCursor {
-  const DecodeParams* p;
+  const WorkItem* items;
   int it, it1, pg;
   WorkItem item;
   __device__ void init(const DecodeParams& pp, int it0, int it_end) {
-    p = &pp;
+    items = pp.items;
     it = it0;
     it1 = it_end;
     if (it < it1) {
-      item = p->items[it];
+      item = items[it];
       pg = item.page_begin;
     }
   }
@@ -125,7 +130,7 @@ struct PageCursor {
   __device__ void next() {
     if (++pg >= item.page_end) {
       if (++it < it1) {
-        item = p->items[it];
+        item = items[it];
         pg = item.page_begin;
       }
     }
@@ -133,7 +138,9 @@ struct PageCursor {
 };
 
 // ------------------------------------------------------------------------------- roles
-// TMA: the k_pe part of Q_r once per work item, then the item's pages.
+// TMA: the k_pe part of Q_r once per work item, then the item's pages. A block-table
+// entry outside the cache is flagged and replaced by page 0 (the request's result is then
+// undefined, but nothing is read out of bounds).
 __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensorMap* tm_kc,
                          const CUtensorMap* tm_kpe, const CUtensorMap* tm_qpe, int worker,
                          int rank) {
@@ -149,7 +156,10 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
     ++q_iter;
     for (int pg = item.page_begin; pg < item.page_end; ++pg) {
       int page = p.block_table[(long long)b * p.max_pages + pg];
-      if (page < 0 || page >= p.num_pages) page = 0;      // masked by the softmax side
+      if (page < 0 || page >= p.num_pages) {
+        if (rank == 0) flag_status(p.status, MLA_ERR_DEVICE_GUARD);
+        page = 0;
+      }
       if (!wait_bar(sh, sh.bar(B_EMPTY0 + stage), (wrap & 1) ^ 1, p.status)) return;
       const uint32_t full = sh.bar(B_FULL0 + stage);
       ptx::mbar_arrive_expect_tx(full, kStageBytes);
@@ -216,17 +226,18 @@ __device__ void pv_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem
     const WorkItem item = p.items[it];
     for (int pg = item.page_begin; pg < item.page_end; ++pg) {
       const bool first = (pg == item.page_begin);
-      if (!wait_bar(sh, sh.bar(B_PFULL), n & 1, p.status)) return;
+      if (!wait_bar(sh, sh.bar(B_PFULL0 + (n & 1)), (n >> 1) & 1, p.status)) return;
       if (first && !wait_bar(sh, sh.bar(B_OFREE), (item_idx & 1) ^ 1, p.status)) return;
       ptx::tc_fence_after();
       const uint32_t sb = sh.stage(stage);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const uint64_t bd = ptx::smem_desc(sb + 2048 * k, kKTileC, 1024, ptx::kSwizzle128);
-        ptx::mma_bf16_ts(tmem + kColO, tmem + kColC + 8 * k, bd, kIdescPV, (!first || k) ? 1u : 0u);
+        ptx::mma_bf16_ts(tmem + kColO, tmem + kColP + 32 * (n & 1) + 8 * k, bd, kIdescPV,
+                         (!first || k) ? 1u : 0u);
       }
       ptx::mma_commit(sh.bar(B_EMPTY0 + stage));
-      ptx::mma_commit(sh.bar(B_PVDONE));
+      ptx::mma_commit(sh.bar(B_PVDONE0 + (n & 1)));
       ++n;
       if (++stage == kNS) stage = 0;
     }
@@ -301,16 +312,21 @@ __device__ void send_warps(const Shared& sh, const DecodeParams& p, uint32_t tme
       ptx::bulk_wait_read_le1();
     }
     if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+    // columns past the last token (rows that may hold anything) go out as 0, and finite
+    // values beyond the fp16 range saturate instead of becoming infinite
+    const int ntok = min(kP, cur.item.kv - cur.pg * kP);
+    if (ntok < kP) {
+#pragma unroll
+      for (int i = 0; i < 64; ++i)
+        if (i >= ntok) r[i] = 0u;
+    }
     uint8_t* srow = sh.base + kOffStg + j * kXBytes + row * 128;
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       uint32_t w[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const __half2 h2 = __floats2half2_rn(__uint_as_float(r[8 * c + 2 * k]),
-                                             __uint_as_float(r[8 * c + 2 * k + 1]));
-        w[k] = *reinterpret_cast<const uint32_t*>(&h2);
-      }
+      for (int k = 0; k < 4; ++k)
+        w[k] = ptx::f2h2_satfinite(__uint_as_float(r[8 * c + 2 * k]), __uint_as_float(r[8 * c + 2 * k + 1]));
       *reinterpret_cast<uint4*>(srow + ((c ^ sw) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
     }
     ptx::fence_proxy_async_smem();
@@ -330,109 +346,59 @@ __device__ void send_warps(const Shared& sh, const DecodeParams& p, uint32_t tme
   }
 }
 
-// Combine warps: own fp16 partial (staging n & 1) + the peer's (receive buffer n & 1) ->
-// combined scores in TMEM, once P of page n-1 (same columns) has been consumed.
-__device__ void combine_warps(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker,
-                              int rank, int warp, int lane) {
+// Softmax warps: the pair's fp16 partial scores -> combined scores -> online softmax -> P
+// into TMEM buffer n & 1; the item's output at its last page.
+__device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker,
+                                 int rank, int warp, int lane) {
   const int quarter = warp & 3;
   const int row = 32 * quarter + lane;
+  const int tid = 32 * (warp - 6) + lane;                // 0..127 over the softmax warps
   const uint32_t t_row = tmem + ((uint32_t)(32 * quarter) << 16);
-  const uint32_t peer = (uint32_t)(rank ^ 1);
-  const uint32_t peer_xempty0 = ptx::map_to_rank(sh.bar(B_XEMPTY0), peer);
+  const uint32_t peer_xempty0 = ptx::map_to_rank(sh.bar(B_XEMPTY0), (uint32_t)(rank ^ 1));
   const int sw = row & 7;
-  const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
-  uint32_t total = 0;
-  for (int it = it0; it < it1; ++it) total += p.items[it].page_end - p.items[it].page_begin;
-  for (uint32_t n = 0; n < total; ++n) {
+  PageCursor cur;
+  cur.init(p, p.worker_off[worker], p.worker_off[worker + 1]);
+  uint32_t n = 0;
+  float m_used = -INFINITY, l = 0.f;
+  while (cur.valid()) {
+    const WorkItem& item = cur.item;
+    const int pg = cur.pg;
+    if (cur.first()) {
+      m_used = -INFINITY;
+      l = 0.f;
+    }
+    const int ntok = min(kP, item.kv - pg * kP);
+
+    // page n's fp16 partials: the peer's (receive buffer n & 1) and our own (staging n & 1)
     const uint32_t j = n & 1;
     if (!wait_bar(sh, sh.bar(B_XFULL0 + j), (n >> 1) & 1, p.status, true)) return;
     if (warp == 6 && lane == 0) ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL0 + j), kXBytes);
     if (!wait_bar(sh, sh.bar(B_STGREADY0 + j), (n >> 1) & 1, p.status)) return;
-    const uint8_t* xrow = sh.base + kOffX + j * kXBytes + row * 128;
-    const uint8_t* srow = sh.base + kOffStg + j * kXBytes + row * 128;
-    uint32_t cs[64];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 a = *reinterpret_cast<const uint4*>(xrow + ((c ^ sw) * 16));
-      const uint4 b = *reinterpret_cast<const uint4*>(srow + ((c ^ sw) * 16));
-      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 fa = __half22float2(*reinterpret_cast<const __half2*>(&av[k]));
-        const float2 fb = __half22float2(*reinterpret_cast<const __half2*>(&bv[k]));
-        cs[8 * c + 2 * k] = __float_as_uint(fa.x + fb.x);
-        cs[8 * c + 2 * k + 1] = __float_as_uint(fa.y + fb.y);
-      }
-    }
+    uint32_t xa[32], xb[32];                              // packed fp16 pairs, columns 2i, 2i+1
     {
+      const uint8_t* xrow = sh.base + kOffX + j * kXBytes + row * 128;
+      const uint8_t* srow = sh.base + kOffStg + j * kXBytes + row * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 a = *reinterpret_cast<const uint4*>(xrow + ((c ^ sw) * 16));
+        const uint4 b = *reinterpret_cast<const uint4*>(srow + ((c ^ sw) * 16));
+        xa[4 * c] = a.x; xa[4 * c + 1] = a.y; xa[4 * c + 2] = a.z; xa[4 * c + 3] = a.w;
+        xb[4 * c] = b.x; xb[4 * c + 1] = b.y; xb[4 * c + 2] = b.z; xb[4 * c + 3] = b.w;
+      }
       // every lane's buffer reads have returned before the buffers are released
       uint32_t dep = 0;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) dep ^= cs[8 * c];
+      for (int i = 0; i < 32; i += 4) dep ^= xa[i] ^ xb[i];
       const uint32_t all = __ballot_sync(0xffffffffu, dep != 0x7fc00001u);
       if (lane == 0) {
         ptx::mbar_arrive_remote_relaxed(peer_xempty0 + 8 * j, all);
         ptx::mbar_arrive(sh.bar(B_STGFREE0 + j));
       }
     }
-    // the combined-score buffer still holds P of page n-1 until its P.C product is done
-    if (n > 0 && !wait_bar(sh, sh.bar(B_PVDONE), (n - 1) & 1, p.status)) return;
-    ptx::tc_fence_after();
-    ptx::tmem_st32(t_row + kColC, *reinterpret_cast<uint32_t(*)[32]>(cs));
-    ptx::tmem_st32(t_row + kColC + 32, *reinterpret_cast<uint32_t(*)[32]>(cs + 32));
-    ptx::tmem_wait_st();
-    ptx::tc_fence_before();
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(sh.bar(B_CFULL));
-  }
-}
-
-// Softmax warps: combined scores -> online softmax -> P over the same TMEM columns; the
-// item's output at its last page.
-__device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker,
-                                 int rank, int warp, int lane) {
-  const int quarter = warp & 3;
-  const int row = 32 * quarter + lane;
-  const int tid = 32 * (warp - 10) + lane;               // 0..127 over the softmax warps
-  const uint32_t t_row = tmem + ((uint32_t)(32 * quarter) << 16);
-  PageCursor cur, ahead;
-  cur.init(p, p.worker_off[worker], p.worker_off[worker + 1]);
-  if (!cur.valid()) return;
-  ahead = cur;
-  ahead.next();
-  // block-table entry and key count of a page, loaded one page before they are used
-  auto load_meta = [&](const PageCursor& c, int* page, int* kv) {
-    const int gg = c.item.group;
-    *page = p.block_table[(long long)(gg / p.q_len) * p.max_pages + c.pg];
-    *kv = p.group_kv[gg];
-  };
-  int page_cur = 0, kv_cur = 0, page_nxt = 0, kv_nxt = 0;
-  load_meta(cur, &page_cur, &kv_cur);
-  uint32_t n = 0;
-  float m_used = -INFINITY, l = 0.f;
-  while (cur.valid()) {
-    const WorkItem item = cur.item;
-    const int pg = cur.pg;
-    const int g = item.group;
-    if (cur.first()) {
-      m_used = -INFINITY;
-      l = 0.f;
-    }
-    if (ahead.valid()) load_meta(ahead, &page_nxt, &kv_nxt);
-    const bool valid = page_cur >= 0 && page_cur < p.num_pages;
-    if (!valid && row == 0 && rank == 0) flag_status(p.status, MLA_ERR_DEVICE_GUARD);
-    const int ntok = valid ? min(kP, kv_cur - pg * kP) : 0;
-
-    if (!wait_bar(sh, sh.bar(B_CFULL), n & 1, p.status)) return;
-    ptx::tc_fence_after();
-    uint32_t sr[64];
-    ptx::tmem_ld32(t_row + kColC, *reinterpret_cast<uint32_t(*)[32]>(sr));
-    ptx::tmem_ld32(t_row + kColC + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
-    ptx::tmem_wait_ld();
-    float* s = reinterpret_cast<float*>(sr);
-    // Rows past the last token (or a whole skipped page) may hold anything, NaN included,
-    // and 0 * NaN would poison O: zero them in the staged c_kv tiles before the P . C
-    // product reads them (the score MMA that read them is done).
+    // Columns past the last token: both partials arrive as 0; make the peer's -inf so the
+    // column gets P = 0. Their c_kv rows may hold anything, NaN included, and 0 * NaN would
+    // poison O: zero them in the staged tiles before the P . C product reads them (the
+    // score MMA that read them is done).
     bool zeroed = false;
     if (ntok < kP) {
       uint8_t* stg = sh.base + kOffStage + (int)(n % kNS) * kStageBytes;
@@ -444,14 +410,32 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
             make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int i = 0; i < 64; ++i)
-        if (i >= ntok) s[i] = -INFINITY;
+      for (int i = 0; i < 32; ++i) {
+        if (2 * i >= ntok) xa[i] = 0xFC00FC00u;
+        else if (2 * i + 1 >= ntok) xa[i] = (xa[i] & 0xFFFFu) | 0xFC000000u;
+      }
       zeroed = true;
     }
-    float mx = s[0];
+    // running maximum on the packed fp16 sums (a reference point only: P may exceed 1 by the
+    // fp16 rounding of the sum, far inside the 2^8 rescale margin)
+    float mx;
+    {
+      __half2 t[16];
 #pragma unroll
-    for (int i = 1; i < 64; ++i) mx = fmaxf(mx, s[i]);
-    mx *= p.scale_log2;
+      for (int i = 0; i < 16; ++i) {
+        const __half2 s0 = __hadd2(*reinterpret_cast<const __half2*>(&xa[2 * i]),
+                                   *reinterpret_cast<const __half2*>(&xb[2 * i]));
+        const __half2 s1 = __hadd2(*reinterpret_cast<const __half2*>(&xa[2 * i + 1]),
+                                   *reinterpret_cast<const __half2*>(&xb[2 * i + 1]));
+        t[i] = __hmax2(s0, s1);
+      }
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) t[i] = __hmax2(t[i], t[i + w]);
+      const float2 f = __half22float2(t[0]);
+      mx = fmaxf(f.x, f.y);
+    }
     bool rescale = false;
     float alpha = 1.f;
     if (mx > -INFINITY) {
@@ -470,19 +454,24 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
       for (int i = 0; i < 32; ++i) packed[i] = 0u;
     } else {
       const float neg_m = -m_used;
-      float psum = 0.f;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float p0 = ptx::ex2(fmaf(s[2 * i], p.scale_log2, neg_m));
-        const float p1 = ptx::ex2(fmaf(s[2 * i + 1], p.scale_log2, neg_m));
-        psum += p0 + p1;
+        const float p0 = ptx::ex2(ptx::add_f16lo_f32(xa[i], ptx::add_f16lo_f32(xb[i], neg_m)));
+        const float p1 = ptx::ex2(ptx::add_f16hi_f32(xa[i], ptx::add_f16hi_f32(xb[i], neg_m)));
+        ps[i & 3] += p0 + p1;
         const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
         packed[i] = *reinterpret_cast<const uint32_t*>(&h2);
       }
-      l += psum;
+      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
     }
-    // O is stable here: the previous P . C product finished before these scores were
-    // written, and this page's product waits for P below
+    // P buffer n & 1 was last read by the product of page n-2; a rescale of O needs the
+    // product of page n-1 done too
+    if (n >= 2 && !wait_bar(sh, sh.bar(B_PVDONE0 + j), ((n >> 1) & 1) ^ 1, p.status)) return;
+    if (rescale && n >= 1 &&
+        !wait_bar(sh, sh.bar(B_PVDONE0 + ((n - 1) & 1)), ((n - 1) >> 1) & 1, p.status))
+      return;
+    ptx::tc_fence_after();
     if (rescale) {
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
@@ -494,17 +483,17 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
         ptx::tmem_st32(t_row + kColO + 32 * c, v);
       }
     }
-    ptx::tmem_st32(t_row + kColC, packed);
+    ptx::tmem_st32(t_row + kColP + 32 * j, packed);
     ptx::tmem_wait_st();
     if (zeroed) ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(sh.bar(B_PFULL));
+    if (lane == 0) ptx::mbar_arrive(sh.bar(B_PFULL0 + j));
 
     // after the item's last page: normalise O_r and write it (output or split partial)
     if (cur.last()) {
-      const int it = cur.it;
-      if (!wait_bar(sh, sh.bar(B_PVDONE), n & 1, p.status)) return;
+      const int it = cur.it, g = item.group;
+      if (!wait_bar(sh, sh.bar(B_PVDONE0 + j), (n >> 1) & 1, p.status)) return;
       ptx::tc_fence_after();
       const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
       const float lse_v = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
@@ -513,8 +502,8 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
         uint32_t v[32];
         ptx::tmem_ld32(t_row + kColO + 32 * c, v);
         ptx::tmem_wait_ld();
-        const int col = 256 * rank + 32 * c;
         if (item.single) {
+          const int col = 256 * rank + 32 * c;
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out_latent) +
                                                 ((long long)g * kH + row) * kDC + col);
 #pragma unroll
@@ -529,11 +518,13 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
             dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(p.part_o + ((long long)it * kH + row) * kDC + col);
+          // quad-planar partial: quad q of head row at part_o[it][q][row][0:4]
+          const int q0 = 64 * rank + 8 * c;
+          float4* dst = reinterpret_cast<float4*>(p.part_o) + ((long long)it * (kDC / 4) + q0) * kH + row;
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            dst[q] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
-                                 __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+            dst[(long long)q * kH] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
+                                                 __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
         }
       }
       ptx::tc_fence_before();
@@ -546,9 +537,6 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
     }
     ++n;
     cur.next();
-    if (ahead.valid()) ahead.next();
-    page_cur = page_nxt;
-    kv_cur = kv_nxt;
   }
 }
 
@@ -578,9 +566,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::mbar_init(sh.bar(B_QPEEMPTY), 1);
     ptx::mbar_init(sh.bar(B_SFULL), 1);
     ptx::mbar_init(sh.bar(B_SFREE), 4);
-    ptx::mbar_init(sh.bar(B_CFULL), 4);
-    ptx::mbar_init(sh.bar(B_PFULL), 4);
-    ptx::mbar_init(sh.bar(B_PVDONE), 1);
+    ptx::mbar_init(sh.bar(B_PFULL0), 4);
+    ptx::mbar_init(sh.bar(B_PFULL1), 4);
+    ptx::mbar_init(sh.bar(B_PVDONE0), 1);
+    ptx::mbar_init(sh.bar(B_PVDONE1), 1);
     ptx::mbar_init(sh.bar(B_XFULL0), 1);
     ptx::mbar_init(sh.bar(B_XFULL1), 1);
     ptx::mbar_init(sh.bar(B_XEMPTY0), 4);
@@ -617,8 +606,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp <= 5) {
     send_warps(sh, p, tmem, worker, rank, warp, lane);
   } else if (warp <= 9) {
-    combine_warps(sh, p, tmem, worker, rank, warp, lane);
-  } else if (warp <= 13) {
     softmax_epilogue(sh, p, tmem, worker, rank, warp, lane);
   } else {
     if (lane == 0) pv_issuer(sh, p, tmem, worker);
@@ -626,7 +613,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   // teardown: every role gets here, normally or after a bounded wait gave up
   // both MMA issuers commit: every issued MMA must have finished before TMEM is released
-  if ((warp == 1 || warp == 14) && lane == 0) ptx::mma_commit(sh.bar(B_TEARDOWN));
+  if ((warp == 1 || warp == 10) && lane == 0) ptx::mma_commit(sh.bar(B_TEARDOWN));
   if (warp >= 2 && warp <= 5 && lane == 0) ptx::bulk_wait_read_all();
   __syncthreads();
   if (warp == 1) {

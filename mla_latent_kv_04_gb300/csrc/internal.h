@@ -16,6 +16,7 @@ struct WorkItem {
   int page_begin;   // group-relative page index
   int page_end;
   int single;       // 1: the item covers the whole group -> write the final output
+  int kv;           // keys the group attends to (its last page holds kv - 64 * (pages - 1))
 };
 
 // Byte offsets of every region of the decode workspace (all 256-byte aligned).
@@ -62,10 +63,13 @@ struct DecodeParams {
   const int* group_first;
   const int* group_last;
   const int* group_kv;
-  float* part_o;
-  float* part_lse;
+  float* part_o;              // split partials; layout set by part_planar
+  float* part_lse;            // [items][H]
   int32_t* status;
   int workers;
+  // 0: part_o is [items][H][d_c]; 1: [items][d_c / 4][H][4] (four latent dims of every head
+  // contiguous, so a warp of consecutive heads writes one 512-byte run)
+  int part_planar;
 };
 
 // Counts kernels launched through the library (read by mla_kernel_launches).
@@ -105,9 +109,11 @@ cudaError_t launch_absorb(mla_dtype act, const void* W_UK, const void* W_UV, con
 // Tensor-core GEMMs (bf16 in, fp32 accumulate), gemm_tc.cu.
 cudaError_t launch_output_proj_tc(const void* o_lat, const void* W_comb, int rows, int K, int N,
                                   void* out, float* acc, int32_t* status, cudaStream_t s);
+// q_scale multiplies the query before its bf16 rounding (1, or the softmax scale times
+// log2(e) for the tensor-core attention, which then works in log2 units).
 cudaError_t launch_query_absorb_tc(const void* q_nope, const void* W_UK_abs, int groups, int H,
-                                   int d_n, int d_c, int D, void* q_lat, int32_t* status,
-                                   cudaStream_t s);
+                                   int d_n, int d_c, int D, float q_scale, void* q_lat,
+                                   int32_t* status, cudaStream_t s);
 cudaError_t launch_append_proj_tc(const void* h, const void* W, int T, int d, int Dc, float* acc,
                                   int32_t* status, cudaStream_t s);
 cudaError_t launch_append_finish(mla_dtype cache, const float* acc, int T, const int32_t* req_ids,
@@ -116,8 +122,8 @@ cudaError_t launch_append_finish(mla_dtype cache, const float* acc, int T, const
                                  int d_r, const RopeTable& rt, float cache_scale, int32_t* status,
                                  cudaStream_t s);
 cudaError_t launch_q_rope(mla_dtype act, const void* q_pe, const int32_t* seq_lens, int batch,
-                          int q_len, int H, int d_c, int d_r, const RopeTable& rt, void* q_lat,
-                          cudaStream_t s);
+                          int q_len, int H, int d_c, int d_r, const RopeTable& rt, float q_scale,
+                          void* q_lat, cudaStream_t s);
 
 // out = o_lat . W_comb; `acc` is an fp32 [rows][N] accumulator in the caller's workspace.
 cudaError_t launch_output_proj_simt_ws(mla_dtype act, const void* o_lat, const void* W_comb,

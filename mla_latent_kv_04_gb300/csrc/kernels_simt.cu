@@ -221,7 +221,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) q_rope_kernel(const T* __restrict__ q_pe,
                                                      const int32_t* seq_lens, int batch, int q_len,
                                                      int H, int d_c, int d_r, RopeTable rt,
-                                                     T* __restrict__ q_lat) {
+                                                     float qs, T* __restrict__ q_lat) {
   __shared__ float cs[kMaxRopePairs], sn[kMaxRopePairs];
   const int g = blockIdx.x;
   const int h0 = blockIdx.y * 16, h1 = min(H, h0 + 16);
@@ -243,8 +243,8 @@ __global__ void __launch_bounds__(256) q_rope_kernel(const T* __restrict__ q_pe,
     const float x1 = to_f32(q_pe[gh * d_r + 2 * k + 1]);
     float y0 = 0.f, y1 = 0.f;
     if (pos >= 0) {
-      y0 = x0 * cs[k] - x1 * sn[k];
-      y1 = x0 * sn[k] + x1 * cs[k];
+      y0 = (x0 * cs[k] - x1 * sn[k]) * qs;
+      y1 = (x0 * sn[k] + x1 * cs[k]) * qs;
     }
     q_lat[gh * D + d_c + 2 * k] = from_f32<T>(y0);
     q_lat[gh * D + d_c + 2 * k + 1] = from_f32<T>(y1);
@@ -360,6 +360,7 @@ __global__ void __launch_bounds__(256) plan_kernel(PlanParams p) {
       it.page_begin = pb;
       it.page_end = pe;
       it.single = (pb == 0 && pe == e - a);
+      it.kv = p.group_kv[g];
       p.items[idx] = it;
       if (pb == 0) p.group_first[g] = idx;
       if (pe == e - a) p.group_last[g] = idx;
@@ -563,6 +564,56 @@ __global__ void __launch_bounds__(256) combine_kernel(DecodeParams p, int groups
   if (lane == 0) p.lse[gh] = L;
 }
 
+// The same merge over quad-planar partials ([item][d_c / 4][H][4]): block (group, 16-dim
+// slice), one thread per head; each split's slice is four coalesced 16-byte loads per
+// thread and the merged slice one 32-byte store.
+__global__ void __launch_bounds__(128) combine_planar_kernel(DecodeParams p) {
+  const int g = blockIdx.x, q0 = 4 * blockIdx.y, h = threadIdx.x;
+  const int first = p.group_first[g], last = p.group_last[g];
+  const int n = (first >= 0 && last >= first) ? last - first + 1 : 0;
+  if (n == 1 || h >= p.H) return;              // single items are written by the attention kernel
+  const long long gh = (long long)g * p.H + h;
+  uint4* out = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out_latent) + gh * p.d_c + 4 * q0);
+  float m = -INFINITY;
+  for (int s = 0; s < n; ++s) m = fmaxf(m, p.part_lse[(long long)(first + s) * p.H + h]);
+  if (n == 0 || m == -INFINITY) {
+    out[0] = make_uint4(0u, 0u, 0u, 0u);
+    out[1] = make_uint4(0u, 0u, 0u, 0u);
+    if (blockIdx.y == 0) p.lse[gh] = -INFINITY;
+    return;
+  }
+  float sum = 0.f;
+  for (int s = 0; s < n; ++s) sum += expf(p.part_lse[(long long)(first + s) * p.H + h] - m);
+  const float L = m + logf(sum);
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  const long long qstride = p.H, sstride = (long long)(p.d_c / 4) * p.H;
+  const float4* base = reinterpret_cast<const float4*>(p.part_o) + (long long)first * sstride + (long long)q0 * qstride + h;
+  for (int s = 0; s < n; ++s) {
+    const float w = expf(p.part_lse[(long long)(first + s) * p.H + h] - L);
+    float4 v[4];
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) v[qq] = base[s * sstride + qq * qstride];
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+      acc[4 * qq] = fmaf(w, v[qq].x, acc[4 * qq]);
+      acc[4 * qq + 1] = fmaf(w, v[qq].y, acc[4 * qq + 1]);
+      acc[4 * qq + 2] = fmaf(w, v[qq].z, acc[4 * qq + 2]);
+      acc[4 * qq + 3] = fmaf(w, v[qq].w, acc[4 * qq + 3]);
+    }
+  }
+  uint32_t pk[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    pk[i] = *reinterpret_cast<const uint32_t*>(&b2);
+  }
+  out[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  out[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  if (blockIdx.y == 0) p.lse[gh] = L;
+}
+
 template <typename T>
 __global__ void f32_to_act_kernel(const float* __restrict__ src, T* __restrict__ dst, long long n) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
@@ -597,24 +648,24 @@ static cudaError_t query_prologue_t(const void* q_nope, const void* q_pe, const 
   if (e != cudaSuccess) return e;
   if (groups > 0) {
     q_rope_kernel<T><<<dim3(groups, (H + 15) / 16), 256, 0, s>>>(reinterpret_cast<const T*>(q_pe), seq_lens, batch, q_len,
-                                           H, d_c, d_r, rt, reinterpret_cast<T*>(q_lat));
+                                           H, d_c, d_r, rt, 1.f, reinterpret_cast<T*>(q_lat));
     note_launch();
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_q_rope(mla_dtype act, const void* q_pe, const int32_t* seq_lens, int batch,
-                          int q_len, int H, int d_c, int d_r, const RopeTable& rt, void* q_lat,
-                          cudaStream_t s) {
+                          int q_len, int H, int d_c, int d_r, const RopeTable& rt, float q_scale,
+                          void* q_lat, cudaStream_t s) {
   const int groups = batch * q_len;
   if (groups <= 0) return cudaSuccess;
   const dim3 blocks(groups, (H + 15) / 16);
   if (act == MLA_F32)
     q_rope_kernel<float><<<blocks, 256, 0, s>>>(reinterpret_cast<const float*>(q_pe), seq_lens, batch,
-                                               q_len, H, d_c, d_r, rt, reinterpret_cast<float*>(q_lat));
+                                               q_len, H, d_c, d_r, rt, q_scale, reinterpret_cast<float*>(q_lat));
   else
     q_rope_kernel<bf16><<<blocks, 256, 0, s>>>(reinterpret_cast<const bf16*>(q_pe), seq_lens, batch,
-                                              q_len, H, d_c, d_r, rt, reinterpret_cast<bf16*>(q_lat));
+                                              q_len, H, d_c, d_r, rt, q_scale, reinterpret_cast<bf16*>(q_lat));
   note_launch();
   return cudaGetLastError();
 }
@@ -664,6 +715,12 @@ cudaError_t launch_decode_simt(mla_dtype act, mla_dtype cache, const DecodeParam
 
 cudaError_t launch_combine(mla_dtype act, const DecodeParams& p, int groups, cudaStream_t s) {
   if (groups <= 0) return cudaSuccess;
+  if (p.part_planar) {
+    if (act != MLA_BF16 || p.H > 128 || p.d_c % 16) return cudaErrorNotSupported;
+    combine_planar_kernel<<<dim3(groups, p.d_c / 16), 128, 0, s>>>(p);
+    note_launch();
+    return cudaGetLastError();
+  }
   const int blocks = (int)(((long long)groups * p.H + 7) / 8);
   if (act == MLA_F32) combine_kernel<float><<<blocks, 256, 0, s>>>(p, groups);
   else combine_kernel<bf16><<<blocks, 256, 0, s>>>(p, groups);

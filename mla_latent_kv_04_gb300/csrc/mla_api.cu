@@ -312,11 +312,13 @@ mla_status mla_decode_ex(const mla_config* cfg, const void* q_nope, const void* 
   if (e != cudaSuccess) return cuda_fail(e, "mla_decode (plan)");
 
   if (cfg->act_dtype == MLA_BF16) {
+    // the tensor-core attention takes its query pre-multiplied by softmax_scale * log2(e)
+    const float q_scale = tc ? softmax_scale_of(cfg) * kLog2e : 1.f;
     e = launch_query_absorb_tc(q_nope, W_UK_abs, batch * q_len, cfg->num_heads, cfg->d_nope,
-                               cfg->d_latent, D, ws + w.q_lat, pp.status, s);
+                               cfg->d_latent, D, q_scale, ws + w.q_lat, pp.status, s);
     if (e == cudaSuccess)
       e = launch_q_rope(cfg->act_dtype, q_pe, seq_lens, batch, q_len, cfg->num_heads,
-                        cfg->d_latent, cfg->d_rope, rt, ws + w.q_lat, s);
+                        cfg->d_latent, cfg->d_rope, rt, q_scale, ws + w.q_lat, s);
   } else {
     e = launch_query_prologue(cfg->act_dtype, q_nope, q_pe, W_UK_abs, seq_lens, batch, q_len,
                               cfg->num_heads, cfg->d_nope, cfg->d_latent, cfg->d_rope, rt,
@@ -338,7 +340,7 @@ mla_status mla_decode_ex(const mla_config* cfg, const void* q_nope, const void* 
   dp.D = D;
   dp.P = cfg->page_size;
   const float cs = cfg->cache_dtype == MLA_FP8_E4M3 ? cfg->cache_scale : 1.f;
-  dp.scale_log2 = softmax_scale_of(cfg) * cs * kLog2e;
+  dp.scale_log2 = tc ? cs : softmax_scale_of(cfg) * cs * kLog2e;   // tc: query pre-scaled
   dp.out_scale = cs;
   dp.out_latent = out_latent;
   dp.lse = lse;
@@ -351,6 +353,7 @@ mla_status mla_decode_ex(const mla_config* cfg, const void* q_nope, const void* 
   dp.part_lse = (float*)(ws + w.part_lse);
   dp.status = pp.status;
   dp.workers = w.workers;
+  dp.part_planar = tc ? 1 : 0;
   if (opts && opts->attn_events[0]) {
     e = cudaEventRecord((cudaEvent_t)opts->attn_events[0], s);
     if (e != cudaSuccess) return cuda_fail(e, "mla_decode (timing event)");

@@ -213,12 +213,25 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                ::"r"(bar) : "memory");
 }
 
+// Arrive (once) on the mbarrier at the same shared-memory offset in every CTA of the cluster
+// named by cta_mask, when every previously issued tcgen05 op of this thread is done.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+      ::"r"(bar), "h"(cta_mask) : "memory");
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, dense.
 //   bits [4,6) D format (1 = f32); [7,10) A format (1 = bf16); [10,13) B format (1 = bf16);
 //   bit 15 A major (0 = K-major, 1 = MN-major); bit 16 B major; [17,23) N >> 3; [24,29) M >> 4.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Same with fp16 A and B (format code 0 in both fields), both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor (sm_100 form):
@@ -244,6 +257,35 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Two floats -> packed fp16 (lo in the low half), round to nearest, finite values beyond the
+// fp16 range saturate to +-65504 instead of becoming infinite.
+__device__ __forceinline__ uint32_t f2h2_satfinite(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+// f32(low / high fp16 half of x) + c in one rounding (sm_100 mixed-precision add).
+__device__ __forceinline__ float add_f16lo_f32(uint32_t x, float c) {
+  float d;
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, lo, %2;\n\t}"
+      : "=f"(d) : "r"(x), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float add_f16hi_f32(uint32_t x, float c) {
+  float d;
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.f16 %0, hi, %2;\n\t}"
+      : "=f"(d) : "r"(x), "f"(c));
+  return d;
+}
+
+// max of three floats in one instruction (sm_100 three-input max.f32)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
   return y;
 }
 
