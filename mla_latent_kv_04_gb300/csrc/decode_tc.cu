@@ -30,11 +30,14 @@
 // The send warps run ahead of the softmax warps, so the cluster transfer, the score MMAs
 // and the softmax of consecutive pages overlap.
 // Roles: warp 0 issues TMA; warp 1 issues the score MMAs and owns the TMEM allocation;
-// warps 2-5 send partial scores and load Q_r into TMEM at each work item's start; warps
-// 6-9 combine the partials, run the softmax and write the outputs; warp 10 issues the P.C
-// MMAs. A thread of warps 2-9 owns one head row = one TMEM lane.
+// warps 2-5 send partial scores and load Q_r into TMEM at each work item's start (a thread
+// owns one head row = one TMEM lane); warps 6-13 combine the partials, run the softmax and
+// write the outputs, two threads per head row: warps 6-9 columns 0-31 and warps 10-13
+// columns 32-63 of each page (and the matching halves of O), sharing the row maximum
+// through shared memory with a 64-thread named barrier per lane quarter; warp 14 issues the
+// P.C MMAs.
 // TMEM: O_r 256 columns, raw S 64, P 2 x 32, Q_r latent part 128.
-// Split partials are written [item][d_c / 4][128 heads][4] fp32, so the 32 threads of a
+// Split partials are written bf16 [item][d_c / 8][128 heads][8], so the 32 threads of a
 // warp (32 consecutive heads) store one contiguous 512-byte run per instruction.
 // Every mbarrier wait is bounded (2 s): on timeout the kernel records MLA_ERR_TIMEOUT,
 // every role leaves its loop, TMEM is freed and the pair meets at a final cluster
@@ -51,6 +54,7 @@ namespace tc {
 
 constexpr int kH = 128, kDC = 512, kDR = 64, kD = 576, kP = 64;
 constexpr int kNS = 4;                                   // cache-page pipeline stages
+constexpr int kL2Ahead = 4;                              // L2 prefetch distance, in pages
 constexpr int kKTileC = 64 * 64 * 2;                     // one 64-dim SW128 chunk of a page
 constexpr int kKTilePE = 64 * 32 * 2;                    // the 32-dim SW64 k_pe half
 constexpr int kStageBytes = 4 * kKTileC + kKTilePE;      // 36864
@@ -60,14 +64,18 @@ constexpr int kOffStage = 0;
 constexpr int kOffX = kOffStage + kNS * kStageBytes;     // two receive buffers
 constexpr int kOffStg = kOffX + 2 * kXBytes;             // two staging buffers (own partial)
 constexpr int kOffQPe = kOffStg + 2 * kXBytes;
-constexpr int kOffBar = kOffQPe + kQPeBytes;
-constexpr int kSmemBytes = kOffBar + 320 + 1024;         // + slack to align the base to 1 KB
+constexpr int kOffRed = kOffQPe + kQPeBytes;             // row max [2 pages][2 halves][128 rows] fp32
+constexpr int kOffLsum = kOffRed + 2 * 2 * 128 * 4;      // row sum [2 halves][128 rows] fp32
+constexpr int kOffBar = kOffLsum + 2 * 128 * 4;
+constexpr int kBarArea = 512;                            // mbarriers, then the abort flag and TMEM slot
+constexpr int kSmemBytes = kOffBar + kBarArea + 1024;    // + slack to align the base to 1 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;                            // O_r: 256 fp32 columns
 constexpr uint32_t kColS = 256;                          // raw partial S: 64 fp32 columns
 constexpr uint32_t kColP = 320;                          // P: two buffers of 64 bf16 = 32
 constexpr uint32_t kColQ = 384;                          // Q_r latent part: 256 bf16 = 128
-constexpr int kThreads = 352;                            // 11 warps
+constexpr int kThreads = 480;                            // 15 warps
+constexpr int kSoftmaxWarps = 8;                         // two per head row (column halves)
 constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, 256, false, true);
 constexpr uint64_t kTimeoutNs = 2000000000ull;
@@ -76,9 +84,12 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 enum {
   B_FULL0 = 0, B_EMPTY0 = kNS, B_QFULL = 2 * kNS, B_QPEFULL, B_QPEEMPTY, B_SFULL, B_SFREE,
   B_PFULL0, B_PFULL1, B_PVDONE0, B_PVDONE1, B_XFULL0, B_XFULL1, B_XEMPTY0, B_XEMPTY1, B_OFREE, B_TEARDOWN,
-  B_STGREADY0, B_STGREADY1, B_STGFREE0, B_STGFREE1, B_COUNT
+  B_STGREADY0, B_STGREADY1, B_STGFREE0, B_STGFREE1,
+  B_RED0,                    // [quarter][page parity]: both halves' row maxima written (2 warps)
+  B_LRED0 = B_RED0 + 8,      // [quarter]: both halves' row sums written (2 warps)
+  B_COUNT = B_LRED0 + 4
 };
-static_assert(B_COUNT * 8 <= 240, "barrier area");
+static_assert(B_COUNT * 8 <= kBarArea - 16, "barrier area");
 
 struct Shared {
   uint8_t* base;       // 1 KB aligned
@@ -94,8 +105,10 @@ struct Shared {
 
 __device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_t parity,
                                          int32_t* status, bool cluster_scope = false) {
+  // each probe sleeps up to 20 us unless the phase completes first
   auto probe = [&]() {
-    return cluster_scope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+    return cluster_scope ? ptx::mbar_try_wait_cluster_sleep(bar, parity, 20000u)
+                         : ptx::mbar_try_wait_sleep(bar, parity, 20000u);
   };
   if (probe()) return true;
   const uint64_t t0 = ptx::globaltimer();
@@ -140,11 +153,24 @@ struct PageCursor {
 // ------------------------------------------------------------------------------- roles
 // TMA: the k_pe part of Q_r once per work item, then the item's pages. A block-table
 // entry outside the cache is flagged and replaced by page 0 (the request's result is then
-// undefined, but nothing is read out of bounds).
+// undefined, but nothing is read out of bounds). Rank 0 also asks L2 for the whole page
+// (both CTAs' halves, 72 KB contiguous) kL2Ahead pages before its TMA load, so that the
+// load, issued when a stage frees up, reads L2 rather than HBM.
 __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensorMap* tm_kc,
                          const CUtensorMap* tm_kpe, const CUtensorMap* tm_qpe, int worker,
                          int rank) {
   const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
+  const uint8_t* cache = reinterpret_cast<const uint8_t*>(p.cache);
+  PageCursor ahead;
+  ahead.init(p, it0, it1);
+  auto prefetch_next = [&]() {
+    if (rank != 0 || !ahead.valid()) return;
+    const int page = p.block_table[(long long)(ahead.item.group / p.q_len) * p.max_pages + ahead.pg];
+    if (page >= 0 && page < p.num_pages)
+      ptx::bulk_prefetch_l2(cache + (long long)page * (kP * kD * 2), kP * kD * 2);
+    ahead.next();
+  };
+  for (int i = 0; i < kL2Ahead; ++i) ahead.next();      // pages 0..kL2Ahead-1 load directly
   int stage = 0;
   uint32_t wrap = 0, q_iter = 0;
   for (int it = it0; it < it1; ++it) {
@@ -152,8 +178,14 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
     const int g = item.group, b = g / p.q_len;
     if (!wait_bar(sh, sh.bar(B_QPEEMPTY), (q_iter & 1) ^ 1, p.status)) return;
     ptx::mbar_arrive_expect_tx(sh.bar(B_QPEFULL), kQPeBytes);
-    ptx::tma_load_2d(sh.qpe(), tm_qpe, kDC + 32 * rank, g * kH, sh.bar(B_QPEFULL));
+    ptx::tma_load_3d(sh.qpe(), tm_qpe, 32 * rank, 0, g, sh.bar(B_QPEFULL));
     ++q_iter;
+    // the next item's latent query half (read by the send warps at its first page) into L2
+    if (it + 1 < it1) {
+      const int gn = p.items[it + 1].group;
+      ptx::bulk_prefetch_l2(reinterpret_cast<const bf16*>(p.q_lat) + (long long)gn * kH * kD + 32 * rank * kH * 8,
+                            32 * kH * 8 * 2);
+    }
     for (int pg = item.page_begin; pg < item.page_end; ++pg) {
       int page = p.block_table[(long long)b * p.max_pages + pg];
       if (page < 0 || page >= p.num_pages) {
@@ -167,6 +199,7 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
       for (int c = 0; c < 4; ++c)
         ptx::tma_load_2d(sh.stage(stage) + c * kKTileC, tm_kc, 256 * rank + 64 * c, page * kP, full);
       ptx::tma_load_2d(sh.stage(stage) + 4 * kKTileC, tm_kpe, kDC + 32 * rank, page * kP, full);
+      prefetch_next();
       if (++stage == kNS) {
         stage = 0;
         ++wrap;
@@ -245,18 +278,20 @@ __device__ void pv_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem
   }
 }
 
-// Q_r latent part of one head row (group g) into TMEM: 256 bf16, two per column.
+// Q_r latent part of one head row (group g) into TMEM: 256 bf16, two per column. The query
+// is planar ([d_c / 8][128 heads][8] per group), so each 16-byte load of a warp (32
+// consecutive head rows) reads one contiguous 512-byte run.
 __device__ __forceinline__ void store_q(const DecodeParams& p, uint32_t t_row, int g, int row,
                                         int rank) {
   const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(p.q_lat) +
-                                                    ((long long)g * kH + row) * kD) + 32 * rank;
+                                                    (long long)g * kH * kD) + (32 * rank) * kH + row;
   uint4 a[8], b[8];
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) a[i] = src[16 * half + i];
+    for (int i = 0; i < 8; ++i) a[i] = src[(16 * half + i) * kH];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) b[i] = src[16 * half + 8 + i];
+    for (int i = 0; i < 8; ++i) b[i] = src[(16 * half + 8 + i) * kH];
     uint32_t v[32];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -347,15 +382,20 @@ __device__ void send_warps(const Shared& sh, const DecodeParams& p, uint32_t tme
 }
 
 // Softmax warps: the pair's fp16 partial scores -> combined scores -> online softmax -> P
-// into TMEM buffer n & 1; the item's output at its last page.
+// into TMEM buffer n & 1; the item's output at its last page. Thread (row, half) handles
+// columns [32 half, 32 half + 32) of each page and O columns [128 half, 128 half + 128).
 __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker,
                                  int rank, int warp, int lane) {
   const int quarter = warp & 3;
+  const int half = (warp - 6) >> 2;
   const int row = 32 * quarter + lane;
-  const int tid = 32 * (warp - 6) + lane;                // 0..127 over the softmax warps
+  const int tid = 32 * (warp - 6) + lane;                // 0..255 over the softmax warps
   const uint32_t t_row = tmem + ((uint32_t)(32 * quarter) << 16);
   const uint32_t peer_xempty0 = ptx::map_to_rank(sh.bar(B_XEMPTY0), (uint32_t)(rank ^ 1));
   const int sw = row & 7;
+  float* red = reinterpret_cast<float*>(sh.base + kOffRed);    // [page parity][half][row]
+  float* lsum = reinterpret_cast<float*>(sh.base + kOffLsum);  // [half][row]
+  uint32_t n_items = 0;
   PageCursor cur;
   cur.init(p, p.worker_off[worker], p.worker_off[worker + 1]);
   uint32_t n = 0;
@@ -369,26 +409,28 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
     }
     const int ntok = min(kP, item.kv - pg * kP);
 
-    // page n's fp16 partials: the peer's (receive buffer n & 1) and our own (staging n & 1)
+    // page n's fp16 partials for our 32 columns: the peer's (receive buffer n & 1) and our
+    // own (staging n & 1)
     const uint32_t j = n & 1;
     if (!wait_bar(sh, sh.bar(B_XFULL0 + j), (n >> 1) & 1, p.status, true)) return;
     if (warp == 6 && lane == 0) ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL0 + j), kXBytes);
     if (!wait_bar(sh, sh.bar(B_STGREADY0 + j), (n >> 1) & 1, p.status)) return;
-    uint32_t xa[32], xb[32];                              // packed fp16 pairs, columns 2i, 2i+1
+    uint32_t xa[16], xb[16];                              // packed fp16 pairs, columns 32 half + 2i, +1
     {
       const uint8_t* xrow = sh.base + kOffX + j * kXBytes + row * 128;
       const uint8_t* srow = sh.base + kOffStg + j * kXBytes + row * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint4 a = *reinterpret_cast<const uint4*>(xrow + ((c ^ sw) * 16));
-        const uint4 b = *reinterpret_cast<const uint4*>(srow + ((c ^ sw) * 16));
+      for (int c = 0; c < 4; ++c) {
+        const int cc = 4 * half + c;
+        const uint4 a = *reinterpret_cast<const uint4*>(xrow + ((cc ^ sw) * 16));
+        const uint4 b = *reinterpret_cast<const uint4*>(srow + ((cc ^ sw) * 16));
         xa[4 * c] = a.x; xa[4 * c + 1] = a.y; xa[4 * c + 2] = a.z; xa[4 * c + 3] = a.w;
         xb[4 * c] = b.x; xb[4 * c + 1] = b.y; xb[4 * c + 2] = b.z; xb[4 * c + 3] = b.w;
       }
       // every lane's buffer reads have returned before the buffers are released
       uint32_t dep = 0;
 #pragma unroll
-      for (int i = 0; i < 32; i += 4) dep ^= xa[i] ^ xb[i];
+      for (int i = 0; i < 16; i += 4) dep ^= xa[i] ^ xb[i];
       const uint32_t all = __ballot_sync(0xffffffffu, dep != 0x7fc00001u);
       if (lane == 0) {
         ptx::mbar_arrive_remote_relaxed(peer_xempty0 + 8 * j, all);
@@ -404,25 +446,27 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
       uint8_t* stg = sh.base + kOffStage + (int)(n % kNS) * kStageBytes;
       const int nrows = kP - ntok;
       const int per_tile = nrows * 8;
-      for (int i = tid; i < 4 * per_tile; i += 128) {
+      for (int i = tid; i < 4 * per_tile; i += 32 * kSoftmaxWarps) {
         const int tile = i / per_tile, rem = i % per_tile;
         *reinterpret_cast<uint4*>(stg + tile * kKTileC + (ntok + rem / 8) * 128 + (rem % 8) * 16) =
             make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        if (2 * i >= ntok) xa[i] = 0xFC00FC00u;
-        else if (2 * i + 1 >= ntok) xa[i] = (xa[i] & 0xFFFFu) | 0xFC000000u;
+      for (int i = 0; i < 16; ++i) {
+        const int col = 32 * half + 2 * i;
+        if (col >= ntok) xa[i] = 0xFC00FC00u;
+        else if (col + 1 >= ntok) xa[i] = (xa[i] & 0xFFFFu) | 0xFC000000u;
       }
       zeroed = true;
     }
-    // running maximum on the packed fp16 sums (a reference point only: P may exceed 1 by the
-    // fp16 rounding of the sum, far inside the 2^8 rescale margin)
+    // row maximum (a reference point only: P may exceed 1 by the fp16 rounding of the sum,
+    // far inside the 2^8 rescale margin): our 32 columns on packed fp16 sums, then the other
+    // half's through shared memory
     float mx;
     {
-      __half2 t[16];
+      __half2 t[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < 8; ++i) {
         const __half2 s0 = __hadd2(*reinterpret_cast<const __half2*>(&xa[2 * i]),
                                    *reinterpret_cast<const __half2*>(&xb[2 * i]));
         const __half2 s1 = __hadd2(*reinterpret_cast<const __half2*>(&xa[2 * i + 1]),
@@ -430,11 +474,17 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
         t[i] = __hmax2(s0, s1);
       }
 #pragma unroll
-      for (int w = 8; w >= 1; w >>= 1)
+      for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
         for (int i = 0; i < w; ++i) t[i] = __hmax2(t[i], t[i + w]);
       const float2 f = __half22float2(t[0]);
-      mx = fmaxf(f.x, f.y);
+      const float mine = fmaxf(f.x, f.y);
+      volatile float* slot = red + (j * 2) * 128;
+      slot[half * 128 + row] = mine;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(sh.bar(B_RED0 + 2 * quarter + j));
+      if (!wait_bar(sh, sh.bar(B_RED0 + 2 * quarter + j), (n >> 1) & 1, p.status)) return;
+      mx = fmaxf(mine, slot[(half ^ 1) * 128 + row]);
     }
     bool rescale = false;
     float alpha = 1.f;
@@ -448,19 +498,27 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
         rescale = true;
       }
     }
-    uint32_t packed[32];
+    uint32_t packed[16];
     if (m_used == -INFINITY) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) packed[i] = 0u;
+      for (int i = 0; i < 16; ++i) packed[i] = 0u;
     } else {
       const float neg_m = -m_used;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      float e[32];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float p0 = ptx::ex2(ptx::add_f16lo_f32(xa[i], ptx::add_f16lo_f32(xb[i], neg_m)));
-        const float p1 = ptx::ex2(ptx::add_f16hi_f32(xa[i], ptx::add_f16hi_f32(xb[i], neg_m)));
-        ps[i & 3] += p0 + p1;
-        const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+      for (int i = 0; i < 16; ++i) {
+        e[2 * i] = ptx::add_f16lo_f32(xa[i], ptx::add_f16lo_f32(xb[i], neg_m));
+        e[2 * i + 1] = ptx::add_f16hi_f32(xa[i], ptx::add_f16hi_f32(xb[i], neg_m));
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) e[i] = ptx::ex2(e[i]);
+      float ps[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ps[i] = (e[8 * i] + e[8 * i + 1]) + (e[8 * i + 2] + e[8 * i + 3]) +
+                                      ((e[8 * i + 4] + e[8 * i + 5]) + (e[8 * i + 6] + e[8 * i + 7]));
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const __nv_bfloat162 h2 = __floats2bfloat162_rn(e[2 * i], e[2 * i + 1]);
         packed[i] = *reinterpret_cast<const uint32_t*>(&h2);
       }
       l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
@@ -474,16 +532,17 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
     ptx::tc_fence_after();
     if (rescale) {
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
-        ptx::tmem_ld32(t_row + kColO + 32 * c, v);
+        const uint32_t col = kColO + 128 * half + 32 * c;
+        ptx::tmem_ld32(t_row + col, v);
         ptx::tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-        ptx::tmem_st32(t_row + kColO + 32 * c, v);
+        ptx::tmem_st32(t_row + col, v);
       }
     }
-    ptx::tmem_st32(t_row + kColP + 32 * j, packed);
+    ptx::tmem_st16(t_row + kColP + 32 * j + 16 * half, packed);
     ptx::tmem_wait_st();
     if (zeroed) ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
@@ -493,17 +552,25 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
     // after the item's last page: normalise O_r and write it (output or split partial)
     if (cur.last()) {
       const int it = cur.it, g = item.group;
+      // the row sum over both halves
+      volatile float* lslot = lsum;
+      lslot[half * 128 + row] = l;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(sh.bar(B_LRED0 + quarter));
+      if (!wait_bar(sh, sh.bar(B_LRED0 + quarter), n_items & 1, p.status)) return;
+      ++n_items;
+      const float l_row = l + lslot[(half ^ 1) * 128 + row];
       if (!wait_bar(sh, sh.bar(B_PVDONE0 + j), (n >> 1) & 1, p.status)) return;
       ptx::tc_fence_after();
-      const float inv = (l > 0.f) ? p.out_scale / l : 0.f;
-      const float lse_v = (l > 0.f) ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      const float inv = (l_row > 0.f) ? p.out_scale / l_row : 0.f;
+      const float lse_v = (l_row > 0.f) ? (m_used + log2f(l_row)) * kLn2 : -INFINITY;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
-        ptx::tmem_ld32(t_row + kColO + 32 * c, v);
+        ptx::tmem_ld32(t_row + kColO + 128 * half + 32 * c, v);
         ptx::tmem_wait_ld();
         if (item.single) {
-          const int col = 256 * rank + 32 * c;
+          const int col = 256 * rank + 128 * half + 32 * c;
           uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out_latent) +
                                                 ((long long)g * kH + row) * kDC + col);
 #pragma unroll
@@ -518,19 +585,26 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
             dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
           }
         } else {
-          // quad-planar partial: quad q of head row at part_o[it][q][row][0:4]
-          const int q0 = 64 * rank + 8 * c;
-          float4* dst = reinterpret_cast<float4*>(p.part_o) + ((long long)it * (kDC / 4) + q0) * kH + row;
+          // octet-planar bf16 partial: dims 8o..8o+7 of head row at part_o[it][o][row][0:8]
+          const int o0 = 32 * rank + 16 * half + 4 * c;
+          uint4* dst = reinterpret_cast<uint4*>(p.part_o) + ((long long)it * (kDC / 8) + o0) * kH + row;
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            dst[(long long)q * kH] = make_float4(__uint_as_float(v[4 * q]) * inv, __uint_as_float(v[4 * q + 1]) * inv,
-                                                 __uint_as_float(v[4 * q + 2]) * inv, __uint_as_float(v[4 * q + 3]) * inv);
+          for (int q = 0; q < 4; ++q) {
+            uint32_t w[4];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[8 * q + 2 * jj]) * inv,
+                                                              __uint_as_float(v[8 * q + 2 * jj + 1]) * inv);
+              w[jj] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            dst[(long long)q * kH] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
         }
       }
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(sh.bar(B_OFREE));
-      if (rank == 0) {
+      if (rank == 0 && half == 0) {
         if (item.single) p.lse[(long long)g * kH + row] = lse_v;
         else p.part_lse[(long long)it * kH + row] = lse_v;
       }
@@ -550,8 +624,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t aligned = (raw + 1023u) & ~1023u;
   sh.base = smem_raw + (aligned - raw);
   sh.base_u32 = aligned;
-  sh.abort = reinterpret_cast<volatile int*>(sh.base + kOffBar + 256);
-  sh.tmem_slot = reinterpret_cast<uint32_t*>(sh.base + kOffBar + 264);
+  sh.abort = reinterpret_cast<volatile int*>(sh.base + kOffBar + kBarArea - 16);
+  sh.tmem_slot = reinterpret_cast<uint32_t*>(sh.base + kOffBar + kBarArea - 8);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (int)ptx::cluster_ctarank();
   const int worker = blockIdx.x >> 1;
@@ -566,20 +640,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::mbar_init(sh.bar(B_QPEEMPTY), 1);
     ptx::mbar_init(sh.bar(B_SFULL), 1);
     ptx::mbar_init(sh.bar(B_SFREE), 4);
-    ptx::mbar_init(sh.bar(B_PFULL0), 4);
-    ptx::mbar_init(sh.bar(B_PFULL1), 4);
+    ptx::mbar_init(sh.bar(B_PFULL0), kSoftmaxWarps);
+    ptx::mbar_init(sh.bar(B_PFULL1), kSoftmaxWarps);
     ptx::mbar_init(sh.bar(B_PVDONE0), 1);
     ptx::mbar_init(sh.bar(B_PVDONE1), 1);
     ptx::mbar_init(sh.bar(B_XFULL0), 1);
     ptx::mbar_init(sh.bar(B_XFULL1), 1);
-    ptx::mbar_init(sh.bar(B_XEMPTY0), 4);
-    ptx::mbar_init(sh.bar(B_XEMPTY1), 4);
-    ptx::mbar_init(sh.bar(B_OFREE), 4);
+    ptx::mbar_init(sh.bar(B_XEMPTY0), kSoftmaxWarps);
+    ptx::mbar_init(sh.bar(B_XEMPTY1), kSoftmaxWarps);
+    ptx::mbar_init(sh.bar(B_OFREE), kSoftmaxWarps);
     ptx::mbar_init(sh.bar(B_TEARDOWN), 2);
     ptx::mbar_init(sh.bar(B_STGREADY0), 4);
     ptx::mbar_init(sh.bar(B_STGREADY1), 4);
-    ptx::mbar_init(sh.bar(B_STGFREE0), 4);
-    ptx::mbar_init(sh.bar(B_STGFREE1), 4);
+    ptx::mbar_init(sh.bar(B_STGFREE0), kSoftmaxWarps);
+    ptx::mbar_init(sh.bar(B_STGFREE1), kSoftmaxWarps);
+    for (int i = 0; i < 12; ++i) ptx::mbar_init(sh.bar(B_RED0 + i), 2);
     *sh.abort = 0;
     ptx::fence_mbar_init();
     // first phase of each receive buffer (the peer's partials of pages 0 and 1)
@@ -605,7 +680,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) qk_issuer(sh, p, tmem, worker);
   } else if (warp <= 5) {
     send_warps(sh, p, tmem, worker, rank, warp, lane);
-  } else if (warp <= 9) {
+  } else if (warp <= 13) {
     softmax_epilogue(sh, p, tmem, worker, rank, warp, lane);
   } else {
     if (lane == 0) pv_issuer(sh, p, tmem, worker);
@@ -613,7 +688,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   // teardown: every role gets here, normally or after a bounded wait gave up
   // both MMA issuers commit: every issued MMA must have finished before TMEM is released
-  if ((warp == 1 || warp == 10) && lane == 0) ptx::mma_commit(sh.bar(B_TEARDOWN));
+  if ((warp == 1 || warp == 14) && lane == 0) ptx::mma_commit(sh.bar(B_TEARDOWN));
   if (warp >= 2 && warp <= 5 && lane == 0) ptx::bulk_wait_read_all();
   __syncthreads();
   if (warp == 1) {
@@ -665,6 +740,21 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_cols
   return r == CUDA_SUCCESS;
 }
 
+// 3-D map over the rotated query parts of the planar query ([groups][128][64] bf16 at
+// element offset 512 * 128 of each 128 x 576 group block); box = 32 columns x 128 heads.
+bool make_qpe_map(CUtensorMap* m, const void* q_lat, uint64_t groups) {
+  auto enc = encoder();
+  if (!enc) return false;
+  const void* base = reinterpret_cast<const bf16*>(q_lat) + (long long)kDC * kH;
+  cuuint64_t dims[3] = {(cuuint64_t)kDR, (cuuint64_t)kH, (cuuint64_t)groups};
+  cuuint64_t strides[2] = {(cuuint64_t)kDR * 2, (cuuint64_t)kH * kD * 2};
+  cuuint32_t box[3] = {32, (cuuint32_t)kH, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace tc
 
 bool tc_decode_supported(const mla_config* c) {
@@ -705,10 +795,10 @@ cudaError_t launch_decode_tc(mla_dtype cache, const DecodeParams& p, cudaStream_
   if (cache != MLA_BF16) return cudaErrorNotSupported;
   CUtensorMap kc, kpe, qpe;
   const uint64_t cache_rows = (uint64_t)p.num_pages * tc::kP;
-  const uint64_t q_rows = (uint64_t)p.batch * p.q_len * tc::kH;
+  const uint64_t groups = (uint64_t)p.batch * p.q_len;
   if (!tc::make_map(&kc, p.cache, cache_rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !tc::make_map(&kpe, p.cache, cache_rows, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !tc::make_map(&qpe, p.q_lat, q_rows, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+      !tc::make_qpe_map(&qpe, p.q_lat, groups))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(tc::decode_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);

@@ -172,12 +172,15 @@ struct EpiAtomic {            // acc[n][m] += v  (split-K partial sums, fp32 wor
     atomicAdd(acc + (long long)n * ld + m, v);
   }
 };
-struct EpiQLat {              // q_lat[n][z][m] = bf16(qs * v)  (n = group, z = head, m = latent dim)
+struct EpiQLat {              // bf16(qs * v) at (group n, head z, latent dim m), row-major or planar
   bf16* q;
   int H, D;
   float qs;
+  int planar;
   __device__ __forceinline__ void operator()(int z, int m, int n, float v) const {
-    q[((long long)n * H + z) * D + m] = __float2bfloat16_rn(qs * v);
+    const long long i = planar ? (long long)n * H * D + ((long long)(m >> 3) * H + z) * 8 + (m & 7)
+                               : ((long long)n * H + z) * D + m;
+    q[i] = __float2bfloat16_rn(qs * v);
   }
 };
 
@@ -311,7 +314,7 @@ cudaError_t launch_output_proj_tc(const void* o_lat, const void* W_comb, int row
 
 // q_lat[g][h][0:d_c] = q_nope[g][h][:] . W_UK_abs[h]  (per head, bf16 out).
 cudaError_t launch_query_absorb_tc(const void* q_nope, const void* W_UK_abs, int groups, int H,
-                                   int d_n, int d_c, int D, float q_scale, void* q_lat,
+                                   int d_n, int d_c, int D, float q_scale, int planar, void* q_lat,
                                    int32_t* status, cudaStream_t s) {
   using namespace gemm;
   CUtensorMap A, Bm[4];
@@ -330,7 +333,7 @@ cudaError_t launch_query_absorb_tc(const void* q_nope, const void* W_UK_abs, int
   gp.m_tiles = (d_c + kBM - 1) / kBM;
   gp.status = status;
   return dispatch(A, Bm[0], Bm[1], Bm[2], Bm[3], gp,
-                  EpiQLat{reinterpret_cast<bf16*>(q_lat), H, D, q_scale}, false, s);
+                  EpiQLat{reinterpret_cast<bf16*>(q_lat), H, D, q_scale, planar}, false, s);
 }
 
 // acc[T][Dc] += h[T][d] . W[d][Dc]  (split-K partial sums into a zeroed fp32 buffer).

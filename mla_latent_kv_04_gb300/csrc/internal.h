@@ -67,8 +67,8 @@ struct DecodeParams {
   float* part_lse;            // [items][H]
   int32_t* status;
   int workers;
-  // 0: part_o is [items][H][d_c]; 1: [items][d_c / 4][H][4] (four latent dims of every head
-  // contiguous, so a warp of consecutive heads writes one 512-byte run)
+  // 0: part_o is fp32 [items][H][d_c]; 1: bf16 [items][d_c / 8][H][8] (eight latent dims of
+  // every head contiguous, so a warp of consecutive heads writes one 512-byte run)
   int part_planar;
 };
 
@@ -111,8 +111,13 @@ cudaError_t launch_output_proj_tc(const void* o_lat, const void* W_comb, int row
                                   void* out, float* acc, int32_t* status, cudaStream_t s);
 // q_scale multiplies the query before its bf16 rounding (1, or the softmax scale times
 // log2(e) for the tensor-core attention, which then works in log2 units).
+// Query layouts in the workspace, per group of H heads (H * D elements each):
+//   row-major (planar = 0): [H][D], the latent part then the rotated k_pe part of each head;
+//   planar (planar = 1, tensor-core attention): the latent part as [d_c / 8][H][8] (eight
+//   dims of every head contiguous, so that a warp of consecutive heads reads 512 contiguous
+//   bytes), then the rotated part as [H][d_r].
 cudaError_t launch_query_absorb_tc(const void* q_nope, const void* W_UK_abs, int groups, int H,
-                                   int d_n, int d_c, int D, float q_scale, void* q_lat,
+                                   int d_n, int d_c, int D, float q_scale, int planar, void* q_lat,
                                    int32_t* status, cudaStream_t s);
 cudaError_t launch_append_proj_tc(const void* h, const void* W, int T, int d, int Dc, float* acc,
                                   int32_t* status, cudaStream_t s);
@@ -123,7 +128,7 @@ cudaError_t launch_append_finish(mla_dtype cache, const float* acc, int T, const
                                  cudaStream_t s);
 cudaError_t launch_q_rope(mla_dtype act, const void* q_pe, const int32_t* seq_lens, int batch,
                           int q_len, int H, int d_c, int d_r, const RopeTable& rt, float q_scale,
-                          void* q_lat, cudaStream_t s);
+                          int planar, void* q_lat, cudaStream_t s);
 
 // out = o_lat . W_comb; `acc` is an fp32 [rows][N] accumulator in the caller's workspace.
 cudaError_t launch_output_proj_simt_ws(mla_dtype act, const void* o_lat, const void* W_comb,

@@ -221,7 +221,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) q_rope_kernel(const T* __restrict__ q_pe,
                                                      const int32_t* seq_lens, int batch, int q_len,
                                                      int H, int d_c, int d_r, RopeTable rt,
-                                                     float qs, T* __restrict__ q_lat) {
+                                                     float qs, int planar, T* __restrict__ q_lat) {
   __shared__ float cs[kMaxRopePairs], sn[kMaxRopePairs];
   const int g = blockIdx.x;
   const int h0 = blockIdx.y * 16, h1 = min(H, h0 + 16);
@@ -246,8 +246,10 @@ __global__ void __launch_bounds__(256) q_rope_kernel(const T* __restrict__ q_pe,
       y0 = (x0 * cs[k] - x1 * sn[k]) * qs;
       y1 = (x0 * sn[k] + x1 * cs[k]) * qs;
     }
-    q_lat[gh * D + d_c + 2 * k] = from_f32<T>(y0);
-    q_lat[gh * D + d_c + 2 * k + 1] = from_f32<T>(y1);
+    const long long o = planar ? (long long)g * H * D + (long long)d_c * H + (long long)h * d_r + 2 * k
+                               : gh * D + d_c + 2 * k;
+    q_lat[o] = from_f32<T>(y0);
+    q_lat[o + 1] = from_f32<T>(y1);
   }
 }
 
@@ -564,16 +566,16 @@ __global__ void __launch_bounds__(256) combine_kernel(DecodeParams p, int groups
   if (lane == 0) p.lse[gh] = L;
 }
 
-// The same merge over quad-planar partials ([item][d_c / 4][H][4]): block (group, 16-dim
-// slice), one thread per head; each split's slice is four coalesced 16-byte loads per
+// The same merge over octet-planar bf16 partials ([item][d_c / 8][H][8]): block (group,
+// 16-dim slice), one thread per head; each split's slice is two coalesced 16-byte loads per
 // thread and the merged slice one 32-byte store.
 __global__ void __launch_bounds__(128) combine_planar_kernel(DecodeParams p) {
-  const int g = blockIdx.x, q0 = 4 * blockIdx.y, h = threadIdx.x;
+  const int g = blockIdx.x, o0 = 2 * blockIdx.y, h = threadIdx.x;
   const int first = p.group_first[g], last = p.group_last[g];
   const int n = (first >= 0 && last >= first) ? last - first + 1 : 0;
   if (n == 1 || h >= p.H) return;              // single items are written by the attention kernel
   const long long gh = (long long)g * p.H + h;
-  uint4* out = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out_latent) + gh * p.d_c + 4 * q0);
+  uint4* out = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out_latent) + gh * p.d_c + 8 * o0);
   float m = -INFINITY;
   for (int s = 0; s < n; ++s) m = fmaxf(m, p.part_lse[(long long)(first + s) * p.H + h]);
   if (n == 0 || m == -INFINITY) {
@@ -588,19 +590,17 @@ __global__ void __launch_bounds__(128) combine_planar_kernel(DecodeParams p) {
   float acc[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-  const long long qstride = p.H, sstride = (long long)(p.d_c / 4) * p.H;
-  const float4* base = reinterpret_cast<const float4*>(p.part_o) + (long long)first * sstride + (long long)q0 * qstride + h;
+  const long long ostride = p.H, sstride = (long long)(p.d_c / 8) * p.H;
+  const uint4* base = reinterpret_cast<const uint4*>(p.part_o) + (long long)first * sstride + (long long)o0 * ostride + h;
   for (int s = 0; s < n; ++s) {
     const float w = expf(p.part_lse[(long long)(first + s) * p.H + h] - L);
-    float4 v[4];
+    const uint4 v0 = base[s * sstride], v1 = base[s * sstride + ostride];
+    const uint32_t u[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-    for (int qq = 0; qq < 4; ++qq) v[qq] = base[s * sstride + qq * qstride];
-#pragma unroll
-    for (int qq = 0; qq < 4; ++qq) {
-      acc[4 * qq] = fmaf(w, v[qq].x, acc[4 * qq]);
-      acc[4 * qq + 1] = fmaf(w, v[qq].y, acc[4 * qq + 1]);
-      acc[4 * qq + 2] = fmaf(w, v[qq].z, acc[4 * qq + 2]);
-      acc[4 * qq + 3] = fmaf(w, v[qq].w, acc[4 * qq + 3]);
+    for (int i = 0; i < 8; ++i) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u[i]));
+      acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
+      acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
     }
   }
   uint32_t pk[8];
@@ -648,7 +648,7 @@ static cudaError_t query_prologue_t(const void* q_nope, const void* q_pe, const 
   if (e != cudaSuccess) return e;
   if (groups > 0) {
     q_rope_kernel<T><<<dim3(groups, (H + 15) / 16), 256, 0, s>>>(reinterpret_cast<const T*>(q_pe), seq_lens, batch, q_len,
-                                           H, d_c, d_r, rt, 1.f, reinterpret_cast<T*>(q_lat));
+                                           H, d_c, d_r, rt, 1.f, 0, reinterpret_cast<T*>(q_lat));
     note_launch();
   }
   return cudaGetLastError();
@@ -656,16 +656,16 @@ static cudaError_t query_prologue_t(const void* q_nope, const void* q_pe, const 
 
 cudaError_t launch_q_rope(mla_dtype act, const void* q_pe, const int32_t* seq_lens, int batch,
                           int q_len, int H, int d_c, int d_r, const RopeTable& rt, float q_scale,
-                          void* q_lat, cudaStream_t s) {
+                          int planar, void* q_lat, cudaStream_t s) {
   const int groups = batch * q_len;
   if (groups <= 0) return cudaSuccess;
   const dim3 blocks(groups, (H + 15) / 16);
   if (act == MLA_F32)
     q_rope_kernel<float><<<blocks, 256, 0, s>>>(reinterpret_cast<const float*>(q_pe), seq_lens, batch,
-                                               q_len, H, d_c, d_r, rt, q_scale, reinterpret_cast<float*>(q_lat));
+                                               q_len, H, d_c, d_r, rt, q_scale, planar, reinterpret_cast<float*>(q_lat));
   else
     q_rope_kernel<bf16><<<blocks, 256, 0, s>>>(reinterpret_cast<const bf16*>(q_pe), seq_lens, batch,
-                                              q_len, H, d_c, d_r, rt, q_scale, reinterpret_cast<bf16*>(q_lat));
+                                              q_len, H, d_c, d_r, rt, q_scale, planar, reinterpret_cast<bf16*>(q_lat));
   note_launch();
   return cudaGetLastError();
 }

@@ -314,11 +314,13 @@ mla_status mla_decode_ex(const mla_config* cfg, const void* q_nope, const void* 
   if (cfg->act_dtype == MLA_BF16) {
     // the tensor-core attention takes its query pre-multiplied by softmax_scale * log2(e)
     const float q_scale = tc ? softmax_scale_of(cfg) * kLog2e : 1.f;
+    // ... and in the planar layout (see internal.h)
+    const int planar = tc ? 1 : 0;
     e = launch_query_absorb_tc(q_nope, W_UK_abs, batch * q_len, cfg->num_heads, cfg->d_nope,
-                               cfg->d_latent, D, q_scale, ws + w.q_lat, pp.status, s);
+                               cfg->d_latent, D, q_scale, planar, ws + w.q_lat, pp.status, s);
     if (e == cudaSuccess)
       e = launch_q_rope(cfg->act_dtype, q_pe, seq_lens, batch, q_len, cfg->num_heads,
-                        cfg->d_latent, cfg->d_rope, rt, q_scale, ws + w.q_lat, s);
+                        cfg->d_latent, cfg->d_rope, rt, q_scale, planar, ws + w.q_lat, s);
   } else {
     e = launch_query_prologue(cfg->act_dtype, q_nope, q_pe, W_UK_abs, seq_lens, batch, q_len,
                               cfg->num_heads, cfg->d_nope, cfg->d_latent, cfg->d_rope, rt,
