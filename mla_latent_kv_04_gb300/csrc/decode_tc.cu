@@ -280,29 +280,31 @@ __device__ void pv_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem
 
 // Q_r latent part of one head row (group g) into TMEM: 256 bf16, two per column. The query
 // is planar ([d_c / 8][128 heads][8] per group), so each 16-byte load of a warp (32
-// consecutive head rows) reads one contiguous 512-byte run.
+// consecutive head rows) reads one contiguous 512-byte run. Four batches of 64 dims, the
+// loads of batch k + 1 issued before batch k is stored.
 __device__ __forceinline__ void store_q(const DecodeParams& p, uint32_t t_row, int g, int row,
                                         int rank) {
   const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const bf16*>(p.q_lat) +
                                                     (long long)g * kH * kD) + (32 * rank) * kH + row;
-  uint4 a[8], b[8];
+  uint4 cur[8], nxt[8];
 #pragma unroll
-  for (int half = 0; half < 2; ++half) {
+  for (int i = 0; i < 8; ++i) cur[i] = src[i * kH];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) a[i] = src[(16 * half + i) * kH];
+  for (int k = 0; k < 4; ++k) {
+    if (k < 3) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) b[i] = src[(16 * half + 8 + i) * kH];
+      for (int i = 0; i < 8; ++i) nxt[i] = src[(8 * (k + 1) + i) * kH];
+    }
     uint32_t v[32];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      v[4 * i] = a[i].x; v[4 * i + 1] = a[i].y; v[4 * i + 2] = a[i].z; v[4 * i + 3] = a[i].w;
+      v[4 * i] = cur[i].x; v[4 * i + 1] = cur[i].y; v[4 * i + 2] = cur[i].z; v[4 * i + 3] = cur[i].w;
     }
-    ptx::tmem_st32(t_row + kColQ + 64 * half, v);
+    ptx::tmem_st32(t_row + kColQ + 32 * k, v);
+    if (k < 3) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      v[4 * i] = b[i].x; v[4 * i + 1] = b[i].y; v[4 * i + 2] = b[i].z; v[4 * i + 3] = b[i].w;
+      for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
     }
-    ptx::tmem_st32(t_row + kColQ + 64 * half + 32, v);
   }
   ptx::tmem_wait_st();
 }
@@ -673,6 +675,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   ptx::cluster_sync();
   const uint32_t tmem = *sh.tmem_slot;
+  // launched with programmatic serialization: the set-up above overlapped the prologue
+  // kernels; the work list and the query are theirs, so wait for them here
+  ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
 
   if (warp == 0) {
     if (lane == 0) producer(sh, p, &tm_kc, &tm_kpe, &tm_qpe, worker, rank);
@@ -803,9 +809,19 @@ cudaError_t launch_decode_tc(mla_dtype cache, const DecodeParams& p, cudaStream_
   cudaError_t e = cudaFuncSetAttribute(tc::decode_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
   if (e != cudaSuccess) return e;
-  tc::decode_tc_kernel<<<2 * p.workers, tc::kThreads, tc::kSmemBytes, s>>>(kc, kpe, qpe, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * p.workers, 1, 1);
+  cfg.blockDim = dim3(tc::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = tc::kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, tc::decode_tc_kernel, kc, kpe, qpe, p);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace mla

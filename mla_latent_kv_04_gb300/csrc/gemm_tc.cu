@@ -28,6 +28,7 @@ struct Params {
   int batch;             // z dimension (heads for the query absorption)
   int m_tiles, n_tiles, k_blocks, k_splits;
   int32_t* status;
+  int reset_status;      // 1: block 0 clears *status first (the first kernel of a decode call)
 };
 
 template <int BN, int NS>
@@ -74,6 +75,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto empty = [&](int s) { return base + C::kBarOff + 8 * (C::kStages + s); };
   const uint32_t done = base + C::kBarOff + 8 * (2 * C::kStages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (gp.reset_status && blockIdx.x == 0 && threadIdx.x == 0) {
+    atomicExch(gp.status, 0);
+    __threadfence();
+  }
+  // a kernel launched after this one with programmatic serialization may start now (it
+  // waits for this grid's completion before it reads what this grid writes)
+  ptx::griddep_launch_dependents();
 
   int unit = blockIdx.x;
   const int ks = unit % gp.k_splits;  unit /= gp.k_splits;
@@ -332,6 +340,7 @@ cudaError_t launch_query_absorb_tc(const void* q_nope, const void* W_UK_abs, int
   gp.batch = H;
   gp.m_tiles = (d_c + kBM - 1) / kBM;
   gp.status = status;
+  gp.reset_status = 1;
   return dispatch(A, Bm[0], Bm[1], Bm[2], Bm[3], gp,
                   EpiQLat{reinterpret_cast<bf16*>(q_lat), H, D, q_scale, planar}, false, s);
 }

@@ -126,6 +126,12 @@ cudaError_t launch_append_finish(mla_dtype cache, const float* acc, int T, const
                                  int max_pages, void* cache_ptr, int num_pages, int P, int d_c,
                                  int d_r, const RopeTable& rt, float cache_scale, int32_t* status,
                                  cudaStream_t s);
+// Planner (block 0) and q_pe rotation (the other blocks) in one bf16 launch, issued with
+// programmatic serialization right after the query absorption GEMM so that it overlaps it;
+// the kernel completes only after the GEMM has.
+cudaError_t launch_prep(const PlanParams& pp, const void* q_pe, const int32_t* seq_lens, int q_len,
+                        int H, int d_c, int d_r, const RopeTable& rt, float q_scale, int planar,
+                        void* q_lat, cudaStream_t s);
 cudaError_t launch_q_rope(mla_dtype act, const void* q_pe, const int32_t* seq_lens, int batch,
                           int q_len, int H, int d_c, int d_r, const RopeTable& rt, float q_scale,
                           int planar, void* q_lat, cudaStream_t s);

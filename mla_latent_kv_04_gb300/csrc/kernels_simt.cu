@@ -10,6 +10,7 @@
 #include <stdio.h>
 
 #include "internal.h"
+#include "sm100_ptx.cuh"
 
 namespace mla {
 
@@ -218,13 +219,11 @@ __global__ void transpose_heads_kernel(const T* __restrict__ W_UK, T* __restrict
 // One block per (group, 16 heads): the d_r/2 rotation angles of the group's position are
 // computed once into shared memory, then applied to those heads' q_pe.
 template <typename T>
-__global__ void __launch_bounds__(256) q_rope_kernel(const T* __restrict__ q_pe,
-                                                     const int32_t* seq_lens, int batch, int q_len,
-                                                     int H, int d_c, int d_r, RopeTable rt,
-                                                     float qs, int planar, T* __restrict__ q_lat) {
+__device__ __forceinline__ void rope_body(const T* __restrict__ q_pe, const int32_t* seq_lens,
+                                          int q_len, int H, int d_c, int d_r, const RopeTable& rt,
+                                          float qs, int planar, T* __restrict__ q_lat, int g, int hy) {
   __shared__ float cs[kMaxRopePairs], sn[kMaxRopePairs];
-  const int g = blockIdx.x;
-  const int h0 = blockIdx.y * 16, h1 = min(H, h0 + 16);
+  const int h0 = hy * 16, h1 = min(H, h0 + 16);
   const int b = g / q_len, t = g % q_len;
   const int pos = seq_lens[b] - q_len + t;
   const int pairs = d_r / 2;
@@ -251,6 +250,14 @@ __global__ void __launch_bounds__(256) q_rope_kernel(const T* __restrict__ q_pe,
     q_lat[o] = from_f32<T>(y0);
     q_lat[o + 1] = from_f32<T>(y1);
   }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) q_rope_kernel(const T* __restrict__ q_pe,
+                                                     const int32_t* seq_lens, int batch, int q_len,
+                                                     int H, int d_c, int d_r, RopeTable rt,
+                                                     float qs, int planar, T* __restrict__ q_lat) {
+  rope_body<T>(q_pe, seq_lens, q_len, H, d_c, d_r, rt, qs, planar, q_lat, blockIdx.x, blockIdx.y);
 }
 
 // ======================================================================== split planner
@@ -303,15 +310,14 @@ __device__ __forceinline__ int group_of(const int* cu, int n, long long x) {
 // worker w processes its range as one work item per group it touches. An item that
 // covers a whole group writes the final output, the others write partials merged by
 // the combine kernel.
-__global__ void __launch_bounds__(256) plan_kernel(PlanParams p) {
-  extern __shared__ int sm[];
+__device__ void plan_body(const PlanParams& p, int* sm, bool reset_status) {
   const int groups = p.batch * p.q_len;
   int* cu = sm;                             // [groups + 1]
   int* wc = sm + groups + 1;                // [workers + 1]
   int* warp_tot = wc + p.workers + 1;       // [32]
   const int tid = threadIdx.x, nt = blockDim.x;
   // each decode call reports its own status: clear the word before anything can flag it
-  if (tid == 0) *p.status = 0;
+  if (reset_status && tid == 0) *p.status = 0;
   __syncthreads();
   for (int g = tid; g < groups; g += nt) {
     const int b = g / p.q_len, t = g % p.q_len;
@@ -369,6 +375,31 @@ __global__ void __launch_bounds__(256) plan_kernel(PlanParams p) {
       ++idx;
     }
   }
+}
+
+__global__ void __launch_bounds__(256) plan_kernel(PlanParams p) {
+  extern __shared__ int sm[];
+  plan_body(p, sm, true);
+}
+
+// The bf16 decode prologue's small jobs in one launch, issued right after the query
+// absorption GEMM with programmatic serialization so that they run alongside it: block 0
+// plans the split work, blocks 1.. rotate q_pe (group (b - 1) / hblocks, 16 heads each).
+// The kernel ends by waiting for the GEMM, so its completion implies the whole prologue's.
+template <typename T>
+__global__ void __launch_bounds__(256) prep_kernel(PlanParams pp, const T* __restrict__ q_pe,
+                                                   const int32_t* seq_lens, int q_len, int H, int d_c,
+                                                   int d_r, RopeTable rt, float qs, int planar,
+                                                   T* __restrict__ q_lat, int hblocks) {
+  extern __shared__ int sm[];
+  ptx::griddep_launch_dependents();
+  if (blockIdx.x == 0) {
+    plan_body(pp, sm, false);
+  } else {
+    const int b = blockIdx.x - 1;
+    rope_body<T>(q_pe, seq_lens, q_len, H, d_c, d_r, rt, qs, planar, q_lat, b / hblocks, b % hblocks);
+  }
+  ptx::griddep_wait();
 }
 
 // ======================================================================== SIMT decode
@@ -570,6 +601,7 @@ __global__ void __launch_bounds__(256) combine_kernel(DecodeParams p, int groups
 // 16-dim slice), one thread per head; each split's slice is two coalesced 16-byte loads per
 // thread and the merged slice one 32-byte store.
 __global__ void __launch_bounds__(128) combine_planar_kernel(DecodeParams p) {
+  ptx::griddep_wait();                         // the attention kernel's partials
   const int g = blockIdx.x, o0 = 2 * blockIdx.y, h = threadIdx.x;
   const int first = p.group_first[g], last = p.group_last[g];
   const int n = (first >= 0 && last >= first) ? last - first + 1 : 0;
@@ -654,6 +686,34 @@ static cudaError_t query_prologue_t(const void* q_nope, const void* q_pe, const 
   return cudaGetLastError();
 }
 
+cudaError_t launch_prep(const PlanParams& pp, const void* q_pe, const int32_t* seq_lens, int q_len,
+                        int H, int d_c, int d_r, const RopeTable& rt, float q_scale, int planar,
+                        void* q_lat, cudaStream_t s) {
+  const int groups = pp.batch * q_len;
+  const int hblocks = (H + 15) / 16;
+  const size_t smem = (size_t)(groups + 1 + pp.workers + 1 + 32) * sizeof(int);
+  auto kern = prep_kernel<bf16>;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1 + groups * hblocks, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, pp, reinterpret_cast<const bf16*>(q_pe), seq_lens, q_len,
+                                     H, d_c, d_r, rt, q_scale, planar, reinterpret_cast<bf16*>(q_lat),
+                                     hblocks);
+  note_launch();
+  return e;
+}
+
 cudaError_t launch_q_rope(mla_dtype act, const void* q_pe, const int32_t* seq_lens, int batch,
                           int q_len, int H, int d_c, int d_r, const RopeTable& rt, float q_scale,
                           int planar, void* q_lat, cudaStream_t s) {
@@ -717,9 +777,18 @@ cudaError_t launch_combine(mla_dtype act, const DecodeParams& p, int groups, cud
   if (groups <= 0) return cudaSuccess;
   if (p.part_planar) {
     if (act != MLA_BF16 || p.H > 128 || p.d_c % 16) return cudaErrorNotSupported;
-    combine_planar_kernel<<<dim3(groups, p.d_c / 16), 128, 0, s>>>(p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(groups, p.d_c / 16, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, combine_planar_kernel, p);
     note_launch();
-    return cudaGetLastError();
+    return e;
   }
   const int blocks = (int)(((long long)groups * p.H + 7) / 8);
   if (act == MLA_F32) combine_kernel<float><<<blocks, 256, 0, s>>>(p, groups);

@@ -308,20 +308,21 @@ mla_status mla_decode_ex(const mla_config* cfg, const void* q_nope, const void* 
   pp.group_last = (int*)(ws + w.group_last);
   pp.group_kv = (int*)(ws + w.group_kv);
   pp.status = (int32_t*)(ws + w.status);
-  cudaError_t e = launch_plan(pp, s);
-  if (e != cudaSuccess) return cuda_fail(e, "mla_decode (plan)");
-
+  cudaError_t e = cudaSuccess;
   if (cfg->act_dtype == MLA_BF16) {
     // the tensor-core attention takes its query pre-multiplied by softmax_scale * log2(e)
     const float q_scale = tc ? softmax_scale_of(cfg) * kLog2e : 1.f;
     // ... and in the planar layout (see internal.h)
     const int planar = tc ? 1 : 0;
+    // query absorption (clears the status word), then planner + rotation alongside it
     e = launch_query_absorb_tc(q_nope, W_UK_abs, batch * q_len, cfg->num_heads, cfg->d_nope,
                                cfg->d_latent, D, q_scale, planar, ws + w.q_lat, pp.status, s);
     if (e == cudaSuccess)
-      e = launch_q_rope(cfg->act_dtype, q_pe, seq_lens, batch, q_len, cfg->num_heads,
-                        cfg->d_latent, cfg->d_rope, rt, q_scale, planar, ws + w.q_lat, s);
+      e = launch_prep(pp, q_pe, seq_lens, q_len, cfg->num_heads, cfg->d_latent, cfg->d_rope, rt,
+                      q_scale, planar, ws + w.q_lat, s);
   } else {
+    e = launch_plan(pp, s);
+    if (e != cudaSuccess) return cuda_fail(e, "mla_decode (plan)");
     e = launch_query_prologue(cfg->act_dtype, q_nope, q_pe, W_UK_abs, seq_lens, batch, q_len,
                               cfg->num_heads, cfg->d_nope, cfg->d_latent, cfg->d_rope, rt,
                               ws + w.q_lat, s);

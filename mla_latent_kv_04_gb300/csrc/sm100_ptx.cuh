@@ -309,6 +309,16 @@ __device__ __forceinline__ float add_f16hi_f32(uint32_t x, float c) {
   return d;
 }
 
+// Programmatic dependent launch: let the next kernel in the stream (launched with the
+// programmatic-serialization attribute) start its blocks now; and wait until the kernels
+// this one depends on have completed with their memory visible (no-ops without PDL).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // max of three floats in one instruction (sm_100 three-input max.f32)
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float y;
