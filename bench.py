@@ -243,6 +243,30 @@ def kernel_work(wl):
     }
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture
+# of the kernel (summaries under profiles/), valid only while the kernel's source file is
+# the one captured: each entry carries that file's sha256 and reads as null otherwise.
+NCU_TRAFFIC = {
+    "attn": {"bytes": 158363392 + 5099520, "source": "mla_latent_kv_04_gb300/csrc/decode_tc.cu",
+             "sha256": "75b20b826aab5b17adeb7ed5cbb519fa1c7c0d534184bf4dde1d578b1892f32d"},
+    "oproj": {"bytes": 675981568 + 3065088, "source": "mla_latent_kv_04_gb300/csrc/gemm_tc.cu",
+              "sha256": "b35005581ba73274e15ab989962568de4b5ee21bb093813295b4a1f71e858694"},
+}
+
+
+def ncu_traffic(part):
+    import hashlib
+    e = NCU_TRAFFIC.get(part)
+    if not e:
+        return None
+    try:
+        with open(os.path.join(ROOT, e["source"]), "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    return e["bytes"] if digest == e["sha256"] else None
+
+
 def roofline_entry(work, ms, peaks, tensor_peak):
     sec = ms * 1e-3
     gbs = work["bytes"] / sec / 1e9
@@ -462,7 +486,7 @@ def main():
              "append": "mla_append_cache"}
     roof = dict(rl[dom])
     roof["kernel"] = names[dom]
-    roof["traffic"] = None
+    roof["traffic"] = ncu_traffic(dom)
     roof["peak_source"] = peaks["source"] + (" (sustained bf16)" if roof["bound"] == "tensor" else "")
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -475,7 +499,8 @@ def main():
                    "l2": "inputs larger than L2: the step streams the 151 MB cache and the "
                          "671 MB folded W_comb"},
         "roofline": roof,
-        "decode_roofline": dict(rl["attn"], kernel="mla_decode attention kernel"),
+        "decode_roofline": dict(rl["attn"], kernel="mla_decode attention kernel",
+                                traffic=ncu_traffic("attn")),
         "parts_ms": {k: round(v, 4) for k, v in parts.items()},
         "parts_roofline": rl,
         "clocks": clk,
