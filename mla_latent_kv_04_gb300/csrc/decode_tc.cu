@@ -54,6 +54,7 @@ namespace tc {
 
 constexpr int kH = 128, kDC = 512, kDR = 64, kD = 576, kP = 64;
 constexpr int kNS = 4;                                   // cache-page pipeline stages
+constexpr int kXB = 2;                                   // score-exchange buffers (page n uses n % kXB)
 constexpr int kL2Ahead = 4;                              // L2 prefetch distance, in pages
 constexpr int kKTileC = 64 * 64 * 2;                     // one 64-dim SW128 chunk of a page
 constexpr int kKTilePE = 64 * 32 * 2;                    // the 32-dim SW64 k_pe half
@@ -61,14 +62,15 @@ constexpr int kStageBytes = 4 * kKTileC + kKTilePE;      // 36864
 constexpr int kXBytes = 128 * 64 * 2;                    // one fp16 partial-score buffer
 constexpr int kQPeBytes = 128 * 32 * 2;                  // Q_r k_pe part, SW64 [128][32]
 constexpr int kOffStage = 0;
-constexpr int kOffX = kOffStage + kNS * kStageBytes;     // two receive buffers
-constexpr int kOffStg = kOffX + 2 * kXBytes;             // two staging buffers (own partial)
-constexpr int kOffQPe = kOffStg + 2 * kXBytes;
+constexpr int kOffX = kOffStage + kNS * kStageBytes;     // receive buffers (the peer's partial)
+constexpr int kOffStg = kOffX + kXB * kXBytes;           // staging buffers (own partial)
+constexpr int kOffQPe = kOffStg + kXB * kXBytes;
 constexpr int kOffRed = kOffQPe + kQPeBytes;             // row max [2 pages][2 halves][128 rows] fp32
 constexpr int kOffLsum = kOffRed + 2 * 2 * 128 * 4;      // row sum [2 halves][128 rows] fp32
 constexpr int kOffBar = kOffLsum + 2 * 128 * 4;
 constexpr int kBarArea = 512;                            // mbarriers, then the abort flag and TMEM slot
 constexpr int kSmemBytes = kOffBar + kBarArea + 1024;    // + slack to align the base to 1 KB
+static_assert(kSmemBytes <= 232448, "dynamic shared memory per CTA");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;                            // O_r: 256 fp32 columns
 constexpr uint32_t kColS = 256;                          // raw partial S: 64 fp32 columns
@@ -340,13 +342,14 @@ __device__ void send_warps(const Shared& sh, const DecodeParams& p, uint32_t tme
     ptx::tmem_wait_ld();
     ptx::tc_fence_before();
     __syncwarp();
-    const uint32_t j = n & 1;
+    const uint32_t j = n % kXB, xpar = (n / kXB) & 1;
     int ok = 1;
     if (lane == 0) {
       ptx::mbar_arrive(sh.bar(B_SFREE));
-      // staging buffer j: the combine warps have read page n-2 and its copy has read it too
-      ok = wait_bar(sh, sh.bar(B_STGFREE0 + j), ((n >> 1) & 1) ^ 1, p.status) ? 1 : 0;
-      ptx::bulk_wait_read_le1();
+      // staging buffer j: our softmax has read page n - kXB from it and that page's copy
+      // has read it too
+      ok = wait_bar(sh, sh.bar(B_STGFREE0 + j), xpar ^ 1, p.status) ? 1 : 0;
+      if (kXB == 1) ptx::bulk_wait_read_all(); else ptx::bulk_wait_read_le1();
     }
     if (!__shfl_sync(0xffffffffu, ok, 0)) return;
     // columns past the last token (rows that may hold anything) go out as 0, and finite
@@ -370,7 +373,7 @@ __device__ void send_warps(const Shared& sh, const DecodeParams& p, uint32_t tme
     __syncwarp();
     if (lane == 0) {
       ptx::mbar_arrive(sh.bar(B_STGREADY0 + j));
-      ok = wait_bar(sh, sh.bar(B_XEMPTY0 + j), ((n >> 1) & 1) ^ 1, p.status, true) ? 1 : 0;
+      ok = wait_bar(sh, sh.bar(B_XEMPTY0 + j), xpar ^ 1, p.status, true) ? 1 : 0;
       if (ok) {
         ptx::bulk_s2s(peer_x_warp + j * kXBytes, sh.stg(j) + quarter * 4096, 4096,
                       peer_xfull0 + 8 * j);
@@ -411,16 +414,17 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
     }
     const int ntok = min(kP, item.kv - pg * kP);
 
-    // page n's fp16 partials for our 32 columns: the peer's (receive buffer n & 1) and our
-    // own (staging n & 1)
+    // page n's fp16 partials for our 32 columns: the peer's (receive buffer n % kXB) and
+    // our own (staging n % kXB); P goes to TMEM buffer n & 1
+    const uint32_t xj = n % kXB, xpar = (n / kXB) & 1;
     const uint32_t j = n & 1;
-    if (!wait_bar(sh, sh.bar(B_XFULL0 + j), (n >> 1) & 1, p.status, true)) return;
-    if (warp == 6 && lane == 0) ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL0 + j), kXBytes);
-    if (!wait_bar(sh, sh.bar(B_STGREADY0 + j), (n >> 1) & 1, p.status)) return;
+    if (!wait_bar(sh, sh.bar(B_XFULL0 + xj), xpar, p.status, true)) return;
+    if (warp == 6 && lane == 0) ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL0 + xj), kXBytes);
+    if (!wait_bar(sh, sh.bar(B_STGREADY0 + xj), xpar, p.status)) return;
     uint32_t xa[16], xb[16];                              // packed fp16 pairs, columns 32 half + 2i, +1
     {
-      const uint8_t* xrow = sh.base + kOffX + j * kXBytes + row * 128;
-      const uint8_t* srow = sh.base + kOffStg + j * kXBytes + row * 128;
+      const uint8_t* xrow = sh.base + kOffX + xj * kXBytes + row * 128;
+      const uint8_t* srow = sh.base + kOffStg + xj * kXBytes + row * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int cc = 4 * half + c;
@@ -435,8 +439,8 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
       for (int i = 0; i < 16; i += 4) dep ^= xa[i] ^ xb[i];
       const uint32_t all = __ballot_sync(0xffffffffu, dep != 0x7fc00001u);
       if (lane == 0) {
-        ptx::mbar_arrive_remote_relaxed(peer_xempty0 + 8 * j, all);
-        ptx::mbar_arrive(sh.bar(B_STGFREE0 + j));
+        ptx::mbar_arrive_remote_relaxed(peer_xempty0 + 8 * xj, all);
+        ptx::mbar_arrive(sh.bar(B_STGFREE0 + xj));
       }
     }
     // Columns past the last token: both partials arrive as 0; make the peer's -inf so the
@@ -659,9 +663,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 12; ++i) ptx::mbar_init(sh.bar(B_RED0 + i), 2);
     *sh.abort = 0;
     ptx::fence_mbar_init();
-    // first phase of each receive buffer (the peer's partials of pages 0 and 1)
-    ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL0), kXBytes);
-    ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL1), kXBytes);
+    // first phase of each receive buffer (the peer's partials of pages 0 .. kXB - 1)
+    for (int x = 0; x < kXB; ++x) ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL0 + x), kXBytes);
     ptx::prefetch_tensormap(&tm_kc);
     ptx::prefetch_tensormap(&tm_kpe);
     ptx::prefetch_tensormap(&tm_qpe);

@@ -310,10 +310,26 @@ __device__ __forceinline__ int group_of(const int* cu, int n, long long x) {
 // worker w processes its range as one work item per group it touches. An item that
 // covers a whole group writes the final output, the others write partials merged by
 // the combine kernel.
+// Work items cost more than their pages: each has a query load into tensor memory and an
+// epilogue, about kItemCost pages' worth on the tensor-core path.
+constexpr int kItemCost = 3;
+
+// Page position of virtual position x: groups occupy [vcu[g], vcu[g + 1]) in the virtual
+// sequence, kItemCost start-up units then their pages; a position inside the start-up
+// units snaps to the group's first page.
+__device__ __forceinline__ long long page_of_virtual(const int* cu, const int* vcu, int n, long long x) {
+  if (x >= vcu[n]) return cu[n];
+  const int g = group_of(vcu, n, x);
+  long long o = x - vcu[g] - (cu[g + 1] > cu[g] ? kItemCost : 0);
+  if (o < 0) o = 0;
+  return cu[g] + o;
+}
+
 __device__ void plan_body(const PlanParams& p, int* sm, bool reset_status) {
   const int groups = p.batch * p.q_len;
-  int* cu = sm;                             // [groups + 1]
-  int* wc = sm + groups + 1;                // [workers + 1]
+  int* cu = sm;                             // [groups + 1] page prefix sums
+  int* vcu = cu + groups + 1;               // [groups + 1] virtual prefix sums (pages + item cost)
+  int* wc = vcu + groups + 1;               // [workers + 1]
   int* warp_tot = wc + p.workers + 1;       // [32]
   const int tid = threadIdx.x, nt = blockDim.x;
   // each decode call reports its own status: clear the word before anything can flag it
@@ -333,17 +349,29 @@ __device__ void plan_body(const PlanParams& p, int* sm, bool reset_status) {
     p.group_kv[g] = kv;
     p.group_first[g] = -1;
     p.group_last[g] = -2;
-    cu[g + 1] = (kv + p.page_size - 1) / p.page_size;
+    const int pages = (kv + p.page_size - 1) / p.page_size;
+    cu[g + 1] = pages;
+    vcu[g + 1] = pages > 0 ? pages + kItemCost : 0;
   }
   if (tid == 0) {
     cu[0] = 0;
+    vcu[0] = 0;
     wc[0] = 0;
   }
   __syncthreads();
   block_inclusive_scan(cu + 1, groups, warp_tot);
-  const long long T = cu[groups];
+  __syncthreads();
+  block_inclusive_scan(vcu + 1, groups, warp_tot);
+  const long long V = vcu[groups];
+  // worker w covers the pages of virtual range [V w / W, V (w + 1) / W): equal shares of
+  // pages plus item start-up cost
+  auto range = [&](int w, long long* lo, long long* hi) {
+    *lo = page_of_virtual(cu, vcu, groups, V * w / p.workers);
+    *hi = page_of_virtual(cu, vcu, groups, V * (w + 1) / p.workers);
+  };
   for (int w = tid; w < p.workers; w += nt) {
-    const long long lo = T * w / p.workers, hi = T * (w + 1) / p.workers;
+    long long lo, hi;
+    range(w, &lo, &hi);
     int cnt = 0;
     if (hi > lo) {
       const int g0 = group_of(cu, groups, lo), g1 = group_of(cu, groups, hi - 1);
@@ -355,7 +383,8 @@ __device__ void plan_body(const PlanParams& p, int* sm, bool reset_status) {
   block_inclusive_scan(wc + 1, p.workers, warp_tot);
   for (int w = tid; w <= p.workers; w += nt) p.worker_off[w] = wc[w];
   for (int w = tid; w < p.workers; w += nt) {
-    const long long lo = T * w / p.workers, hi = T * (w + 1) / p.workers;
+    long long lo, hi;
+    range(w, &lo, &hi);
     if (hi <= lo) continue;
     int idx = wc[w];
     const int g0 = group_of(cu, groups, lo), g1 = group_of(cu, groups, hi - 1);
@@ -655,7 +684,7 @@ __global__ void f32_to_act_kernel(const float* __restrict__ src, T* __restrict__
 
 // ======================================================================== launchers
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
-  const size_t smem = (size_t)(p.batch * p.q_len + 1 + p.workers + 1 + 32) * sizeof(int);
+  const size_t smem = (size_t)(2 * (p.batch * p.q_len + 1) + p.workers + 1 + 32) * sizeof(int);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
@@ -691,7 +720,7 @@ cudaError_t launch_prep(const PlanParams& pp, const void* q_pe, const int32_t* s
                         void* q_lat, cudaStream_t s) {
   const int groups = pp.batch * q_len;
   const int hblocks = (H + 15) / 16;
-  const size_t smem = (size_t)(groups + 1 + pp.workers + 1 + 32) * sizeof(int);
+  const size_t smem = (size_t)(2 * (groups + 1) + pp.workers + 1 + 32) * sizeof(int);
   auto kern = prep_kernel<bf16>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
