@@ -637,25 +637,50 @@ __global__ void __launch_bounds__(128) combine_planar_kernel(DecodeParams p) {
   if (n == 1 || h >= p.H) return;              // single items are written by the attention kernel
   const long long gh = (long long)g * p.H + h;
   uint4* out = reinterpret_cast<uint4*>(reinterpret_cast<bf16*>(p.out_latent) + gh * p.d_c + 8 * o0);
-  float m = -INFINITY;
-  for (int s = 0; s < n; ++s) m = fmaxf(m, p.part_lse[(long long)(first + s) * p.H + h]);
-  if (n == 0 || m == -INFINITY) {
+  if (n == 0) {
     out[0] = make_uint4(0u, 0u, 0u, 0u);
     out[1] = make_uint4(0u, 0u, 0u, 0u);
     if (blockIdx.y == 0) p.lse[gh] = -INFINITY;
     return;
   }
-  float sum = 0.f;
-  for (int s = 0; s < n; ++s) sum += expf(p.part_lse[(long long)(first + s) * p.H + h] - m);
-  const float L = m + logf(sum);
+  const long long ostride = p.H, sstride = (long long)(p.d_c / 8) * p.H;
+  const uint4* base = reinterpret_cast<const uint4*>(p.part_o) + (long long)first * sstride + (long long)o0 * ostride + h;
+  const float* lse_p = p.part_lse + (long long)first * p.H + h;
+  // up to kW splits with every load issued before any is used; further splits streamed
+  constexpr int kW = 8;
+  float ls[kW];
+  uint4 va[kW], vb[kW];
+#pragma unroll
+  for (int s = 0; s < kW; ++s) {
+    if (s < n) {
+      ls[s] = lse_p[(long long)s * p.H];
+      va[s] = base[s * sstride];
+      vb[s] = base[s * sstride + ostride];
+    }
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int s = 0; s < kW; ++s)
+    if (s < n) m = fmaxf(m, ls[s]);
+  for (int s = kW; s < n; ++s) m = fmaxf(m, lse_p[(long long)s * p.H]);
+  if (m == -INFINITY) {
+    out[0] = make_uint4(0u, 0u, 0u, 0u);
+    out[1] = make_uint4(0u, 0u, 0u, 0u);
+    if (blockIdx.y == 0) p.lse[gh] = -INFINITY;
+    return;
+  }
+  float wts[kW], sum = 0.f;
+#pragma unroll
+  for (int s = 0; s < kW; ++s) {
+    wts[s] = (s < n) ? expf(ls[s] - m) : 0.f;
+    sum += wts[s];
+  }
+  for (int s = kW; s < n; ++s) sum += expf(lse_p[(long long)s * p.H] - m);
+  const float inv = 1.f / sum;
   float acc[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-  const long long ostride = p.H, sstride = (long long)(p.d_c / 8) * p.H;
-  const uint4* base = reinterpret_cast<const uint4*>(p.part_o) + (long long)first * sstride + (long long)o0 * ostride + h;
-  for (int s = 0; s < n; ++s) {
-    const float w = expf(p.part_lse[(long long)(first + s) * p.H + h] - L);
-    const uint4 v0 = base[s * sstride], v1 = base[s * sstride + ostride];
+  auto accumulate = [&](float w, const uint4& v0, const uint4& v1) {
     const uint32_t u[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -663,7 +688,12 @@ __global__ void __launch_bounds__(128) combine_planar_kernel(DecodeParams p) {
       acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
       acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
     }
-  }
+  };
+#pragma unroll
+  for (int s = 0; s < kW; ++s)
+    if (s < n) accumulate(wts[s] * inv, va[s], vb[s]);
+  for (int s = kW; s < n; ++s)
+    accumulate(expf(lse_p[(long long)s * p.H] - m) * inv, base[s * sstride], base[s * sstride + ostride]);
   uint32_t pk[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -672,7 +702,7 @@ __global__ void __launch_bounds__(128) combine_planar_kernel(DecodeParams p) {
   }
   out[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
   out[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-  if (blockIdx.y == 0) p.lse[gh] = L;
+  if (blockIdx.y == 0) p.lse[gh] = m + logf(sum);
 }
 
 template <typename T>
