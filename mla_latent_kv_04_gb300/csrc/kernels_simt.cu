@@ -296,45 +296,42 @@ __device__ void block_inclusive_scan(int* a, int n, int* warp_tot) {
   __syncthreads();
 }
 
-// Largest g in [0, n) with cu[g] <= x (cu non-decreasing, cu[0] = 0 <= x < cu[n]).
-__device__ __forceinline__ int group_of(const int* cu, int n, long long x) {
+// The flattened sequence of all groups' key pages is cut into `workers` ranges of equal
+// cost, where a work item costs its pages plus kItemCost start-up units (its query load
+// into tensor memory and its epilogue, about that many pages' worth on the tensor-core
+// path); worker w processes its range as one work item per group it touches. An item that
+// covers a whole group writes the final output, the others write partials merged by the
+// combine kernel.
+//
+// Every step is data-parallel with O(1) work per thread (the plan runs on the decode's
+// critical path, where serial per-thread chains cost microseconds): per group the
+// prefix sums of pages, cost and non-empty groups; each group places the cost cuts that
+// fall inside it; each worker reads its item count from the non-empty prefix.
+constexpr int kItemCost = 3;
+
+// Largest g in [0, n) with a[g] <= x (a non-decreasing, a[0] = 0 <= x < a[n]).
+__device__ __forceinline__ int last_at_most(const int* a, int n, long long x) {
   int lo = 0, hi = n - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (cu[mid] <= x) lo = mid; else hi = mid - 1;
+    if (a[mid] <= x) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
 
-// The flattened sequence of all groups' key pages is cut into `workers` equal ranges;
-// worker w processes its range as one work item per group it touches. An item that
-// covers a whole group writes the final output, the others write partials merged by
-// the combine kernel.
-// Work items cost more than their pages: each has a query load into tensor memory and an
-// epilogue, about kItemCost pages' worth on the tensor-core path.
-constexpr int kItemCost = 3;
-
-// Page position of virtual position x: groups occupy [vcu[g], vcu[g + 1]) in the virtual
-// sequence, kItemCost start-up units then their pages; a position inside the start-up
-// units snaps to the group's first page.
-__device__ __forceinline__ long long page_of_virtual(const int* cu, const int* vcu, int n, long long x) {
-  if (x >= vcu[n]) return cu[n];
-  const int g = group_of(vcu, n, x);
-  long long o = x - vcu[g] - (cu[g + 1] > cu[g] ? kItemCost : 0);
-  if (o < 0) o = 0;
-  return cu[g] + o;
-}
-
 __device__ void plan_body(const PlanParams& p, int* sm, bool reset_status) {
-  const int groups = p.batch * p.q_len;
-  int* cu = sm;                             // [groups + 1] page prefix sums
-  int* vcu = cu + groups + 1;               // [groups + 1] virtual prefix sums (pages + item cost)
-  int* wc = vcu + groups + 1;               // [workers + 1]
-  int* warp_tot = wc + p.workers + 1;       // [32]
+  const int groups = p.batch * p.q_len, W = p.workers;
+  int* cu = sm;                             // [groups + 1] page prefix
+  int* vcu = cu + groups + 1;               // [groups + 1] cost prefix
+  int* nz = vcu + groups + 1;               // [groups + 1] non-empty group prefix
+  int* cutp = nz + groups + 1;              // [W + 1] page position of cut k
+  int* cutg = cutp + W + 1;                 // [W + 1] group holding cut k
+  int* wc = cutg + W + 1;                   // [W + 1] item prefix
+  int* warp_tot = wc + W + 1;               // [32]
+  int* kvs = warp_tot + 32;                 // [groups] keys per group
   const int tid = threadIdx.x, nt = blockDim.x;
   // each decode call reports its own status: clear the word before anything can flag it
   if (reset_status && tid == 0) *p.status = 0;
-  __syncthreads();
   for (int g = tid; g < groups; g += nt) {
     const int b = g / p.q_len, t = g % p.q_len;
     const int S = p.seq_lens[b];
@@ -347,61 +344,69 @@ __device__ void plan_body(const PlanParams& p, int* sm, bool reset_status) {
       }
     }
     p.group_kv[g] = kv;
+    kvs[g] = kv;
     p.group_first[g] = -1;
     p.group_last[g] = -2;
     const int pages = (kv + p.page_size - 1) / p.page_size;
     cu[g + 1] = pages;
     vcu[g + 1] = pages > 0 ? pages + kItemCost : 0;
+    nz[g + 1] = pages > 0 ? 1 : 0;
   }
   if (tid == 0) {
     cu[0] = 0;
     vcu[0] = 0;
+    nz[0] = 0;
     wc[0] = 0;
   }
   __syncthreads();
   block_inclusive_scan(cu + 1, groups, warp_tot);
-  __syncthreads();
   block_inclusive_scan(vcu + 1, groups, warp_tot);
+  block_inclusive_scan(nz + 1, groups, warp_tot);
+  // cut k sits at cost floor(V k / W), inside the (non-empty) group g with
+  // vcu[g] <= cut < vcu[g + 1]; a cut inside a group's start-up units falls on its first page
   const long long V = vcu[groups];
-  // worker w covers the pages of virtual range [V w / W, V (w + 1) / W): equal shares of
-  // pages plus item start-up cost
-  auto range = [&](int w, long long* lo, long long* hi) {
-    *lo = page_of_virtual(cu, vcu, groups, V * w / p.workers);
-    *hi = page_of_virtual(cu, vcu, groups, V * (w + 1) / p.workers);
-  };
-  for (int w = tid; w < p.workers; w += nt) {
-    long long lo, hi;
-    range(w, &lo, &hi);
-    int cnt = 0;
-    if (hi > lo) {
-      const int g0 = group_of(cu, groups, lo), g1 = group_of(cu, groups, hi - 1);
-      for (int g = g0; g <= g1; ++g) cnt += (cu[g + 1] > cu[g]);
+  for (int k = tid; k <= W; k += nt) {
+    if (k == W || V == 0) {
+      cutp[k] = k == W ? cu[groups] : 0;
+      cutg[k] = groups;
+      continue;
     }
-    wc[w + 1] = cnt;
+    const long long c = V * k / W;
+    const int g = last_at_most(vcu, groups, c);
+    const long long o = c - vcu[g] - kItemCost;
+    cutp[k] = cu[g] + (int)(o < 0 ? 0 : o);
+    cutg[k] = g;
   }
   __syncthreads();
-  block_inclusive_scan(wc + 1, p.workers, warp_tot);
-  for (int w = tid; w <= p.workers; w += nt) p.worker_off[w] = wc[w];
-  for (int w = tid; w < p.workers; w += nt) {
-    long long lo, hi;
-    range(w, &lo, &hi);
+  // worker w: pages [cutp[w], cutp[w + 1]), one item per non-empty group from cutg[w] to the
+  // group of its last page
+  auto last_group_end = [&](int w) {       // one past the group of page cutp[w + 1] - 1
+    const int g1 = cutg[w + 1];
+    return (g1 < groups && cutp[w + 1] > cu[g1]) ? g1 + 1 : g1;
+  };
+  for (int w = tid; w < W; w += nt)
+    wc[w + 1] = cutp[w + 1] > cutp[w] ? nz[last_group_end(w)] - nz[cutg[w]] : 0;
+  __syncthreads();
+  block_inclusive_scan(wc + 1, W, warp_tot);
+  for (int w = tid; w <= W; w += nt) p.worker_off[w] = wc[w];
+  for (int w = tid; w < W; w += nt) {
+    const int lo = cutp[w], hi = cutp[w + 1];
     if (hi <= lo) continue;
-    int idx = wc[w];
-    const int g0 = group_of(cu, groups, lo), g1 = group_of(cu, groups, hi - 1);
-    for (int g = g0; g <= g1; ++g) {
+    const int g0 = cutg[w], g1 = last_group_end(w);
+    for (int g = g0; g < g1; ++g) {
       const int a = cu[g], e = cu[g + 1];
       if (e == a) continue;
-      const int pb = (int)(max(lo, (long long)a) - a), pe = (int)(min(hi, (long long)e) - a);
+      const int idx = wc[w] + nz[g] - nz[g0];
+      const int pb = max(lo, a) - a, pe = min(hi, e) - a;
       WorkItem it;
       it.group = g;
       it.page_begin = pb;
       it.page_end = pe;
       it.single = (pb == 0 && pe == e - a);
-      it.kv = p.group_kv[g];
+      it.kv = kvs[g];
       p.items[idx] = it;
       if (pb == 0) p.group_first[g] = idx;
       if (pe == e - a) p.group_last[g] = idx;
-      ++idx;
     }
   }
 }
@@ -714,7 +719,7 @@ __global__ void f32_to_act_kernel(const float* __restrict__ src, T* __restrict__
 
 // ======================================================================== launchers
 cudaError_t launch_plan(const PlanParams& p, cudaStream_t s) {
-  const size_t smem = (size_t)(2 * (p.batch * p.q_len + 1) + p.workers + 1 + 32) * sizeof(int);
+  const size_t smem = (size_t)(4 * (p.batch * p.q_len + 1) + 3 * (p.workers + 1) + 32) * sizeof(int);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
@@ -750,7 +755,7 @@ cudaError_t launch_prep(const PlanParams& pp, const void* q_pe, const int32_t* s
                         void* q_lat, cudaStream_t s) {
   const int groups = pp.batch * q_len;
   const int hblocks = (H + 15) / 16;
-  const size_t smem = (size_t)(2 * (groups + 1) + pp.workers + 1 + 32) * sizeof(int);
+  const size_t smem = (size_t)(4 * (groups + 1) + 3 * (pp.workers + 1) + 32) * sizeof(int);
   auto kern = prep_kernel<bf16>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
