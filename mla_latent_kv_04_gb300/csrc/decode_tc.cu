@@ -55,7 +55,8 @@ namespace tc {
 constexpr int kH = 128, kDC = 512, kDR = 64, kD = 576, kP = 64;
 constexpr int kNS = 4;                                   // cache-page pipeline stages
 constexpr int kXB = 2;                                   // score-exchange buffers (page n uses n % kXB)
-constexpr int kL2Ahead = 4;                              // L2 prefetch distance, in pages
+constexpr int kL2Ahead = 1;                              // L2 prefetch distance, in pages
+constexpr int kQAhead = 4;                               // next item's query into L2, pages before the end
 constexpr int kKTileC = 64 * 64 * 2;                     // one 64-dim SW128 chunk of a page
 constexpr int kKTilePE = 64 * 32 * 2;                    // the 32-dim SW64 k_pe half
 constexpr int kStageBytes = 4 * kKTileC + kKTilePE;      // 36864
@@ -107,10 +108,10 @@ struct Shared {
 
 __device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_t parity,
                                          int32_t* status, bool cluster_scope = false) {
-  // each probe sleeps up to 20 us unless the phase completes first
+  // polled without a suspend hint: waking a suspended warp costs more than the issue
+  // slots the polling takes from the other warps
   auto probe = [&]() {
-    return cluster_scope ? ptx::mbar_try_wait_cluster_sleep(bar, parity, 20000u)
-                         : ptx::mbar_try_wait_sleep(bar, parity, 20000u);
+    return cluster_scope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
   };
   if (probe()) return true;
   const uint64_t t0 = ptx::globaltimer();
@@ -182,13 +183,16 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
     ptx::mbar_arrive_expect_tx(sh.bar(B_QPEFULL), kQPeBytes);
     ptx::tma_load_3d(sh.qpe(), tm_qpe, 32 * rank, 0, g, sh.bar(B_QPEFULL));
     ++q_iter;
-    // the next item's latent query half (read by the send warps at its first page) into L2
-    if (it + 1 < it1) {
-      const int gn = p.items[it + 1].group;
-      ptx::bulk_prefetch_l2(reinterpret_cast<const bf16*>(p.q_lat) + (long long)gn * kH * kD + 32 * rank * kH * 8,
-                            32 * kH * 8 * 2);
-    }
+    // the next item's latent query half (read by the send warps at its first page) and its
+    // rotated part into L2, kQAhead pages before this item ends (earlier, it would be
+    // evicted by the cache stream before use)
+    const int q_at = max(item.page_begin, item.page_end - kQAhead);
     for (int pg = item.page_begin; pg < item.page_end; ++pg) {
+      if (pg == q_at && it + 1 < it1) {
+        const bf16* qn = reinterpret_cast<const bf16*>(p.q_lat) + (long long)p.items[it + 1].group * kH * kD;
+        ptx::bulk_prefetch_l2(qn + 32 * rank * kH * 8, 32 * kH * 8 * 2);
+        ptx::bulk_prefetch_l2(qn + kDC * kH, kH * kDR * 2);
+      }
       int page = p.block_table[(long long)b * p.max_pages + pg];
       if (page < 0 || page >= p.num_pages) {
         if (rank == 0) flag_status(p.status, MLA_ERR_DEVICE_GUARD);
