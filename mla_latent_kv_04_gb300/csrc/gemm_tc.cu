@@ -14,6 +14,7 @@
 #include <cudaTypedefs.h>
 
 #include "internal.h"
+#include "prologue.cuh"
 #include "sm100_ptx.cuh"
 
 namespace mla {
@@ -29,6 +30,12 @@ struct Params {
   int m_tiles, n_tiles, k_blocks, k_splits;
   int32_t* status;
   int reset_status;      // 1: block 0 clears *status first (the first kernel of a decode call)
+  int pdl;               // 1: launched with programmatic serialization after the kernel it
+                         // overlaps; the grid waits for that kernel at its end
+  int plan_block;        // 1: one extra block runs the decode's split planner
+  PlanParams plan;
+  int rope_blocks;       // extra blocks that rotate q_pe (after the planner block)
+  RopeJob rope;
 };
 
 template <int BN, int NS>
@@ -75,15 +82,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto empty = [&](int s) { return base + C::kBarOff + 8 * (C::kStages + s); };
   const uint32_t done = base + C::kBarOff + 8 * (2 * C::kStages);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (gp.reset_status && blockIdx.x == 0 && threadIdx.x == 0) {
-    atomicExch(gp.status, 0);
-    __threadfence();
-  }
   // a kernel launched after this one with programmatic serialization may start now (it
   // waits for this grid's completion before it reads what this grid writes)
   ptx::griddep_launch_dependents();
+  // the decode prologue's small jobs in extra blocks: the planner (which clears the status
+  // word first) as block 0, so that it starts first, and the q_pe rotation after the GEMM's
+  // blocks, so that it does not displace them
+  const int side_blocks = gp.plan_block;
+  const int main_end = (int)gridDim.x - gp.rope_blocks;
+  if ((int)blockIdx.x < side_blocks || (int)blockIdx.x >= main_end) {
+    if ((int)blockIdx.x < side_blocks) {
+      plan_body(gp.plan, reinterpret_cast<int*>(basep), true);
+    } else {
+      const int r = (int)blockIdx.x - main_end;
+      const RopeJob& q = gp.rope;
+      if (q.d_r % 16 == 0)
+        rope_body_bf16x8(q.q_pe, q.seq_lens, q.q_len, q.H, q.d_c, q.d_r, q.rt, q.qs, q.planar, q.q_lat,
+                         r / q.hblocks, r % q.hblocks, 32);
+      else
+        rope_body<bf16>(q.q_pe, q.seq_lens, q.q_len, q.H, q.d_c, q.d_r, q.rt, q.qs, q.planar, q.q_lat,
+                        r / q.hblocks, r % q.hblocks, 32);
+    }
+    ptx::griddep_wait();
+    return;
+  }
+  if (gp.reset_status && (int)blockIdx.x == side_blocks && threadIdx.x == 0) {
+    atomicExch(gp.status, 0);
+    __threadfence();
+  }
 
-  int unit = blockIdx.x;
+  int unit = (int)blockIdx.x - side_blocks;
   const int ks = unit % gp.k_splits;  unit /= gp.k_splits;
   const int nt = unit % gp.n_tiles;   unit /= gp.n_tiles;
   const int mt = unit % gp.m_tiles;   unit /= gp.m_tiles;
@@ -170,6 +198,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::kTmemCols);
   }
+  // under programmatic serialization: this grid completes only after the kernel before it,
+  // so a kernel that waits for this one sees that kernel's results too (no-op otherwise)
+  ptx::griddep_wait();
 }
 
 // ------------------------------------------------------------------------------ epilogues
@@ -242,9 +273,21 @@ static cudaError_t run(const CUtensorMap& A, const CUtensorMap& B, Params gp, co
   if (e != cudaSuccess) return e;
   const long long units = (long long)gp.batch * gp.m_tiles * gp.n_tiles * gp.k_splits;
   if (units <= 0) return cudaSuccess;
-  kern<<<(unsigned)units, kThreads, C::kSmem, s>>>(A, B, gp, epi);
+  cudaLaunchConfig_t cfg = {};
+  if (gp.plan_block && plan_smem_bytes(gp.plan.batch * gp.plan.q_len, gp.plan.workers) > (size_t)C::kBarOff)
+    return cudaErrorInvalidValue;
+  cfg.gridDim = dim3((unsigned)(units + gp.plan_block + gp.rope_blocks), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = gp.pdl ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, kern, A, B, gp, epi);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 // Chooses the N tile and the K split: enough CTAs to cover the SMs about once.
@@ -323,7 +366,8 @@ cudaError_t launch_output_proj_tc(const void* o_lat, const void* W_comb, int row
 // q_lat[g][h][0:d_c] = q_nope[g][h][:] . W_UK_abs[h]  (per head, bf16 out).
 cudaError_t launch_query_absorb_tc(const void* q_nope, const void* W_UK_abs, int groups, int H,
                                    int d_n, int d_c, int D, float q_scale, int planar, void* q_lat,
-                                   int32_t* status, cudaStream_t s) {
+                                   int32_t* status, const PlanParams* plan, const RopeJob* rope,
+                                   cudaStream_t s) {
   using namespace gemm;
   CUtensorMap A, Bm[4];
   // A = W_UK_abs[h] : dims {d_c (m), d_n (k), H (z)}
@@ -340,7 +384,14 @@ cudaError_t launch_query_absorb_tc(const void* q_nope, const void* W_UK_abs, int
   gp.batch = H;
   gp.m_tiles = (d_c + kBM - 1) / kBM;
   gp.status = status;
-  gp.reset_status = 1;
+  // with the planner as an extra block this is the decode's first kernel and the planner
+  // clears the status word; otherwise the prep kernel before it did
+  gp.reset_status = 0;
+  gp.pdl = plan ? 0 : 1;
+  gp.plan_block = plan ? 1 : 0;
+  if (plan) gp.plan = *plan;
+  gp.rope_blocks = rope ? rope->groups * rope->hblocks : 0;
+  if (rope) gp.rope = *rope;
   return dispatch(A, Bm[0], Bm[1], Bm[2], Bm[3], gp,
                   EpiQLat{reinterpret_cast<bf16*>(q_lat), H, D, q_scale, planar}, false, s);
 }

@@ -116,9 +116,14 @@ cudaError_t launch_output_proj_tc(const void* o_lat, const void* W_comb, int row
 //   planar (planar = 1, tensor-core attention): the latent part as [d_c / 8][H][8] (eight
 //   dims of every head contiguous, so that a warp of consecutive heads reads 512 contiguous
 //   bytes), then the rotated part as [H][d_r].
+// plan / rope: if non-null, extra blocks of the GEMM run the split planner (which clears the
+// status word) and the q_pe rotation, and the GEMM is the decode's first kernel; if null,
+// the GEMM follows the prep kernel (which did both) with programmatic serialization.
+struct RopeJob;
 cudaError_t launch_query_absorb_tc(const void* q_nope, const void* W_UK_abs, int groups, int H,
                                    int d_n, int d_c, int D, float q_scale, int planar, void* q_lat,
-                                   int32_t* status, cudaStream_t s);
+                                   int32_t* status, const PlanParams* plan, const RopeJob* rope,
+                                   cudaStream_t s);
 cudaError_t launch_append_proj_tc(const void* h, const void* W, int T, int d, int Dc, float* acc,
                                   int32_t* status, cudaStream_t s);
 cudaError_t launch_append_finish(mla_dtype cache, const float* acc, int T, const int32_t* req_ids,
@@ -126,9 +131,9 @@ cudaError_t launch_append_finish(mla_dtype cache, const float* acc, int T, const
                                  int max_pages, void* cache_ptr, int num_pages, int P, int d_c,
                                  int d_r, const RopeTable& rt, float cache_scale, int32_t* status,
                                  cudaStream_t s);
-// Planner (block 0) and q_pe rotation (the other blocks) in one bf16 launch, issued with
-// programmatic serialization right after the query absorption GEMM so that it overlaps it;
-// the kernel completes only after the GEMM has.
+// q_pe rotation in one bf16 launch, plus (if pp.workers > 0) the status reset and the
+// planner in block 0, then as the decode's first kernel; without the planner it follows the
+// query absorption GEMM (which planned) with programmatic serialization.
 cudaError_t launch_prep(const PlanParams& pp, const void* q_pe, const int32_t* seq_lens, int q_len,
                         int H, int d_c, int d_r, const RopeTable& rt, float q_scale, int planar,
                         void* q_lat, cudaStream_t s);

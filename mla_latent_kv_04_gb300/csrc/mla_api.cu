@@ -10,6 +10,7 @@
 
 #include "internal.h"
 #include "decode_tc.h"
+#include "prologue.cuh"
 
 using namespace mla;
 
@@ -314,12 +315,34 @@ mla_status mla_decode_ex(const mla_config* cfg, const void* q_nope, const void* 
     const float q_scale = tc ? softmax_scale_of(cfg) * kLog2e : 1.f;
     // ... and in the planar layout (see internal.h)
     const int planar = tc ? 1 : 0;
-    // query absorption (clears the status word), then planner + rotation alongside it
-    e = launch_query_absorb_tc(q_nope, W_UK_abs, batch * q_len, cfg->num_heads, cfg->d_nope,
-                               cfg->d_latent, D, q_scale, planar, ws + w.q_lat, pp.status, s);
-    if (e == cudaSuccess)
+    // one launch: the query absorption GEMM with the planner (which clears the status word)
+    // and the q_pe rotation as extra blocks. A plan too large for the GEMM block's shared
+    // memory runs in the prep kernel, which then goes first.
+    if (plan_smem_bytes(batch * q_len, w.workers) <= 32 * 1024) {
+      RopeJob rj;
+      rj.q_pe = reinterpret_cast<const bf16*>(q_pe);
+      rj.seq_lens = seq_lens;
+      rj.q_lat = reinterpret_cast<bf16*>(ws + w.q_lat);
+      rj.groups = batch * q_len;
+      rj.q_len = q_len;
+      rj.H = cfg->num_heads;
+      rj.d_c = cfg->d_latent;
+      rj.d_r = cfg->d_rope;
+      rj.planar = planar;
+      rj.hblocks = (cfg->num_heads + 31) / 32;
+      rj.qs = q_scale;
+      rj.rt = rt;
+      e = launch_query_absorb_tc(q_nope, W_UK_abs, batch * q_len, cfg->num_heads, cfg->d_nope,
+                                 cfg->d_latent, D, q_scale, planar, ws + w.q_lat, pp.status, &pp,
+                                 &rj, s);
+    } else {
       e = launch_prep(pp, q_pe, seq_lens, q_len, cfg->num_heads, cfg->d_latent, cfg->d_rope, rt,
                       q_scale, planar, ws + w.q_lat, s);
+      if (e == cudaSuccess)
+        e = launch_query_absorb_tc(q_nope, W_UK_abs, batch * q_len, cfg->num_heads, cfg->d_nope,
+                                   cfg->d_latent, D, q_scale, planar, ws + w.q_lat, pp.status,
+                                   nullptr, nullptr, s);
+    }
   } else {
     e = launch_plan(pp, s);
     if (e != cudaSuccess) return cuda_fail(e, "mla_decode (plan)");
