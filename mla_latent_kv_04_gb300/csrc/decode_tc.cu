@@ -472,7 +472,8 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
     // row maximum (a reference point only: P may exceed 1 by the fp16 rounding of the sum,
     // far inside the 2^8 rescale margin): our 32 columns on packed fp16 sums, then the other
     // half's through shared memory
-    float mx;
+    volatile float* slot = red + (j * 2) * 128;
+    float mine;
     {
       __half2 t[8];
 #pragma unroll
@@ -488,32 +489,16 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
 #pragma unroll
         for (int i = 0; i < w; ++i) t[i] = __hmax2(t[i], t[i + w]);
       const float2 f = __half22float2(t[0]);
-      const float mine = fmaxf(f.x, f.y);
-      volatile float* slot = red + (j * 2) * 128;
+      mine = fmaxf(f.x, f.y);
       slot[half * 128 + row] = mine;
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(sh.bar(B_RED0 + 2 * quarter + j));
-      if (!wait_bar(sh, sh.bar(B_RED0 + 2 * quarter + j), (n >> 1) & 1, p.status)) return;
-      mx = fmaxf(mine, slot[(half ^ 1) * 128 + row]);
     }
-    bool rescale = false;
-    float alpha = 1.f;
-    if (mx > -INFINITY) {
-      if (m_used == -INFINITY) {
-        m_used = mx;
-      } else if (mx > m_used + 8.f) {
-        alpha = ptx::ex2(m_used - mx);
-        m_used = mx;
-        l *= alpha;
-        rescale = true;
-      }
-    }
+    // P and its row sum against reference value m_ref
     uint32_t packed[16];
-    if (m_used == -INFINITY) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) packed[i] = 0u;
-    } else {
-      const float neg_m = -m_used;
+    float psum = 0.f;
+    auto exps = [&](float m_ref) {
+      const float neg_m = -m_ref;
       float e[32];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -531,16 +516,49 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
         const __nv_bfloat162 h2 = __floats2bfloat162_rn(e[2 * i], e[2 * i + 1]);
         packed[i] = *reinterpret_cast<const uint32_t*>(&h2);
       }
-      l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+      psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+    };
+    // Usually the running reference value stays (our half does not exceed it by more than
+    // 2^8, and the other half rarely does): form P from it while the other half's maximum is
+    // on its way, and recompute only if the full row maximum moves the reference (an item's
+    // first page, or a rescale).
+    const bool early = (m_used != -INFINITY) && !(mine > m_used + 8.f);
+    if (early) exps(m_used);
+    if (!wait_bar(sh, sh.bar(B_RED0 + 2 * quarter + j), (n >> 1) & 1, p.status)) return;
+    const float mx = fmaxf(mine, slot[(half ^ 1) * 128 + row]);
+    bool rescale = false;
+    float alpha = 1.f;
+    if (mx > -INFINITY) {
+      if (m_used == -INFINITY) {
+        m_used = mx;
+      } else if (mx > m_used + 8.f) {
+        alpha = ptx::ex2(m_used - mx);
+        m_used = mx;
+        l *= alpha;
+        rescale = true;
+      }
     }
+    if (!early || rescale) {
+      if (m_used == -INFINITY) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) packed[i] = 0u;
+        psum = 0.f;
+      } else {
+        exps(m_used);
+      }
+    }
+    l += psum;
     // P buffer n & 1 was last read by the product of page n-2; a rescale of O needs the
     // product of page n-1 done too
     if (n >= 2 && !wait_bar(sh, sh.bar(B_PVDONE0 + j), ((n >> 1) & 1) ^ 1, p.status)) return;
-    if (rescale && n >= 1 &&
+    // tcgen05 loads and stores are warp-collective: the warp rescales its 32 rows together
+    // when any of them needs it (alpha is 1 for the others)
+    const bool warp_rescale = __any_sync(0xffffffffu, rescale);
+    if (warp_rescale && n >= 1 &&
         !wait_bar(sh, sh.bar(B_PVDONE0 + ((n - 1) & 1)), ((n - 1) >> 1) & 1, p.status))
       return;
     ptx::tc_fence_after();
-    if (rescale) {
+    if (warp_rescale) {
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
