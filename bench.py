@@ -247,10 +247,10 @@ def kernel_work(wl):
 # of the kernel (summaries under profiles/), valid only while the kernel's source file is
 # the one captured: each entry carries that file's sha256 and reads as null otherwise.
 NCU_TRAFFIC = {
-    "attn": {"bytes": 158363392 + 5099520, "source": "mla_latent_kv_04_gb300/csrc/decode_tc.cu",
-             "sha256": "75b20b826aab5b17adeb7ed5cbb519fa1c7c0d534184bf4dde1d578b1892f32d"},
-    "oproj": {"bytes": 675981568 + 3065088, "source": "mla_latent_kv_04_gb300/csrc/gemm_tc.cu",
-              "sha256": "b35005581ba73274e15ab989962568de4b5ee21bb093813295b4a1f71e858694"},
+    "attn": {"bytes": 157550848 + 4771584, "source": "mla_latent_kv_04_gb300/csrc/decode_tc.cu",
+             "sha256": "e4afc260fe1acdcf4dcb6188e81592ea46c915bc00921c276f3f95819de28da0"},
+    "oproj": {"bytes": 676020736 + 3005952, "source": "mla_latent_kv_04_gb300/csrc/gemm_tc.cu",
+              "sha256": "8c77bc985fbcb9479e8f1b27644d50ca34a61061432579b8c00f4b7dfeb41b32"},
 }
 
 
