@@ -37,7 +37,7 @@ import numpy as np
 __all__ = [
     "softmax_scale", "rope", "project_latent", "decompress", "decode_decompressed",
     "absorb_weights", "absorbed_query", "decode_absorbed", "output_projection",
-    "mha_output", "e4m3_encode", "e4m3_decode", "cache_image", "cache_elems_per_token",
+    "lift_latent", "mha_output", "e4m3_encode", "e4m3_decode", "cache_image", "cache_elems_per_token",
     "cache_bytes", "combine_partials",
 ]
 
@@ -211,6 +211,18 @@ def output_projection(o_lat, W_comb):
     """Output_t = sum_i o_lat_i W_i^combined ([P1] §3-2, second equation).
     o_lat [rows][H*d_c] (head-major), W_comb [H*d_c][d_model]."""
     return np.asarray(o_lat, np.float64) @ np.asarray(W_comb, np.float64)
+
+
+def lift_latent(o_lat, W_UV, num_heads: int):
+    """u_i = o_lat_i W_i^UV, each head's latent output lifted to its value width ([P1] §3-2,
+    first equation: sum_j A_j (c_j W_i^UV) = (sum_j A_j c_j) W_i^UV).
+    o_lat [rows][H][d_c] (or [rows][H*d_c]), W_UV [d_c][H*d_v] (head i owns columns
+    i*d_v..) -> u [rows][H][d_v]."""
+    o = np.asarray(o_lat, np.float64)
+    o = o.reshape(o.shape[0], num_heads, -1)
+    W = np.asarray(W_UV, np.float64)
+    d_v = W.shape[1] // num_heads
+    return np.einsum("rhc,chv->rhv", o, W.reshape(W.shape[0], num_heads, d_v))
 
 
 def mha_output(u, W_O):

@@ -232,6 +232,37 @@ def test_folded_output_projection_is_lossless():
     assert np.max(np.abs(a - b)) <= 1e-12 * np.max(np.abs(a))
 
 
+def test_lift_latent_equals_decompressed_value_output():
+    # huny.dev §3-2, first equation: the decompressed route's value output u (values
+    # c_j W_i^UV averaged by the attention weights) is the latent output lifted by W_i^UV.
+    T = _tiny_case(seed=13, S=27, q=2)
+    r = oracle.decode_decompressed(T["c"], T["k_rot"], T["q_nope"], T["q_pe"], T["W_UK"],
+                                   T["W_UV"], T["scale"])
+    u = oracle.lift_latent(r["o_lat"], T["W_UV"], T["H"])
+    assert u.shape == r["u"].shape
+    assert np.max(np.abs(u - r["u"])) <= 1e-13 * max(1.0, np.max(np.abs(r["u"])))
+    # a head-block weight that is the identity on head 1 only copies that head's first dims
+    d_c, H = T["c"].shape[1], T["H"]
+    d_v = T["W_UV"].shape[1] // H
+    W = np.zeros((d_c, H * d_v))
+    W[:d_v, d_v:2 * d_v] = np.eye(d_v)
+    u1 = oracle.lift_latent(r["o_lat"], W, H)
+    assert np.array_equal(u1[:, 1], r["o_lat"][:, 1, :d_v])
+    assert not u1[:, 0].any() and not u1[:, 2:].any()
+
+
+def test_unfolded_output_path_equals_folded():
+    # huny.dev §3-2 second equation, both sides: sum_i (o_i W_i^UV) W_i^O == o . W_comb.
+    T = _tiny_case(seed=14, S=19, q=2)
+    rng = np.random.default_rng(14)
+    H, d_c = T["H"], T["c"].shape[1]
+    o = rng.standard_normal((3, H * d_c))
+    _, W_comb = oracle.absorb_weights(T["W_UK"], T["W_UV"], T["W_O"], H)
+    a = oracle.mha_output(oracle.lift_latent(o, T["W_UV"], H), T["W_O"])
+    b = oracle.output_projection(o, W_comb)
+    assert np.max(np.abs(a - b)) <= 1e-12 * np.max(np.abs(a))
+
+
 def test_seq_len_one_returns_the_only_latent():
     T = _tiny_case(seed=11, S=1)
     W_UK_abs, _ = oracle.absorb_weights(T["W_UK"], T["W_UV"], T["W_O"], T["H"])
