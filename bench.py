@@ -187,13 +187,16 @@ def setup(wl, dev):
     out = torch.empty(rows * d.d_model, dtype=act, device=dev)
     ws = torch.zeros(M.mla_decode_workspace_size(cfg, B, q), dtype=torch.uint8, device=dev)
     ws_o = torch.zeros(M.mla_output_proj_workspace_size(cfg, rows), dtype=torch.uint8, device=dev)
+    ws_u = torch.zeros(M.mla_output_proj_unfolded_workspace_size(cfg, rows), dtype=torch.uint8,
+                       device=dev)
     n_a = M.mla_append_cache_workspace_size(cfg, rows)
     ws_a = torch.zeros(n_a, dtype=torch.uint8, device=dev) if n_a else None
     torch.cuda.synchronize()
     return {"cfg": cfg, "dw": dw, "cache": cache, "bt_d": bt_d, "W_UK_abs": W_UK_abs,
             "W_comb": W_comb, "host": host, "dev_in": dev_in,
             "new_req": up(new_req, torch.int32), "new_pos": up(new_pos, torch.int32),
-            "out_lat": out_lat, "lse": lse, "out": out, "ws": ws, "ws_o": ws_o, "ws_a": ws_a,
+            "out_lat": out_lat, "lse": lse, "out": out, "ws": ws, "ws_o": ws_o, "ws_u": ws_u,
+            "ws_a": ws_a,
             "status": status}
 
 
@@ -240,6 +243,10 @@ def kernel_work(wl):
         "append": {"bytes": rows * d.d_model * ea + d.d_model * d.d_cache * ea
                    + rows * d.d_cache * W.elt_bytes(wl.cache),
                    "flops": 2.0 * rows * d.d_model * d.d_cache},
+        # the unfolded output path: W_UV and W_O instead of W_comb (not part of the step)
+        "oproj_unfolded": {"bytes": (d.d_latent * H * d.d_v + H * d.d_v * d.d_model) * ea
+                           + rows * K * ea + rows * d.d_model * ea,
+                           "flops": 2.0 * rows * (K * d.d_v + H * d.d_v * d.d_model)},
     }
 
 
@@ -445,6 +452,16 @@ def main():
     d1.record()
     torch.cuda.synchronize()
     decode_alone_ms = d0.elapsed_time(d1) / K
+    # the unfolded output path (u_i = o_i W_i^UV, then u W_O), alone, back to back; it is an
+    # alternative to the step's folded projection and not part of the step
+    u0, u1 = mk()
+    u0.record()
+    for i in range(K):
+        M.mla_output_proj_unfolded(st["cfg"], st["out_lat"], st["dw"]["W_UV"], st["dw"]["W_O"],
+                                   st["out"], st["ws_u"])
+    u1.record()
+    torch.cuda.synchronize()
+    oproj_unfolded_ms = u0.elapsed_time(u1) / K
     if world > 1:
         tt = torch.tensor([ms], dtype=torch.float64)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
@@ -519,6 +536,11 @@ def main():
                                 traffic=ncu_traffic("attn")),
         "parts_ms": {k: round(v, 4) for k, v in parts.items()},
         "decode_alone_ms": round(decode_alone_ms, 4),
+        "oproj_unfolded": dict(roofline_entry(work["oproj_unfolded"], oproj_unfolded_ms, peaks, tpk),
+                               ms=round(oproj_unfolded_ms, 4),
+                               note="alternative to the step's folded output projection: "
+                                    "u_i = o_i W_i^UV then u W_O (W_UV + W_O instead of W_comb); "
+                                    "not part of the step"),
         "parts_roofline": rl,
         "clocks": clk,
         "gpu_launches": int(launches),

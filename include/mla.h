@@ -196,6 +196,25 @@ mla_status mla_output_proj(const mla_config* cfg, const void* out_latent, const 
                            int rows, void* out, void* workspace, size_t workspace_bytes,
                            void* stream);
 
+/* Bytes of workspace mla_output_proj_unfolded needs for `rows` rows (may be 0). */
+mla_status mla_output_proj_unfolded_workspace_size(const mla_config* cfg, int rows,
+                                                   size_t* bytes);
+
+/* Output projection without the fold, the two sides of huny.dev §3-2 read before the
+ * absorption (its first equation, then the per-head output projection):
+ *   u[r][i] = out_latent[r][i] W_i^UV      (per head: d_c -> d_v, rounded to the act dtype)
+ *   out[r]  = sum_i u[r][i] W_i^O
+ *   out_latent [rows][H*d_c]; W_UV [d_c][H*d_v] and W_O [H*d_v][d] as given to
+ *   mla_absorb_weights (head i owns columns i*d_v.. of W_UV, rows i*d_v.. of W_O);
+ *   out [rows][d]  (act dtype), fp32 accumulation. It streams H*d_c*d_v + H*d_v*d weight
+ *   elements instead of W_comb's H*d_c*d (185 MB instead of 671 MB at DeepSeek-V2 shapes);
+ *   equal to mla_output_proj up to the rounding of u. workspace: 256-byte aligned device
+ *   buffer of mla_output_proj_unfolded_workspace_size bytes (an fp32 accumulator, a status
+ *   word and u). Errors as mla_output_proj. */
+mla_status mla_output_proj_unfolded(const mla_config* cfg, const void* out_latent, const void* W_UV,
+                                    const void* W_O, int rows, void* out, void* workspace,
+                                    size_t workspace_bytes, void* stream);
+
 /* Wait for `stream`, then read the device status word at `status_word` (a decode
  * workspace or an append dev_status) into *code (an mla_status value, MLA_OK if clean)
  * and reset it to 0. */

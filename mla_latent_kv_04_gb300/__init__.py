@@ -74,6 +74,8 @@ _SIGNATURES = {
     "mla_decode_noalloc": (_I, [_CFG, _P, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P, _P, _P]),
     "mla_output_proj_workspace_size": (_I, [_CFG, _I, ctypes.POINTER(_SZ)]),
     "mla_output_proj": (_I, [_CFG, _P, _P, _I, _P, _P, _SZ, _P]),
+    "mla_output_proj_unfolded_workspace_size": (_I, [_CFG, _I, ctypes.POINTER(_SZ)]),
+    "mla_output_proj_unfolded": (_I, [_CFG, _P, _P, _P, _I, _P, _P, _SZ, _P]),
     "mla_read_device_status": (_I, [_P, _P, ctypes.POINTER(_I)]),
     "mla_status_string": (ctypes.c_char_p, [_I]),
     "mla_last_error": (ctypes.c_char_p, []),
@@ -315,6 +317,27 @@ def mla_output_proj(cfg, out_latent, W_comb, out, workspace, stream=None):
         _ptr(W_comb, "W_comb", a, K * cfg.d_model), rows, _ptr(out, "out", a, rows * cfg.d_model),
         _ptr(workspace, "workspace", (_torch().uint8,)), workspace.numel(), _stream(stream)),
         "mla_output_proj")
+
+
+def mla_output_proj_unfolded_workspace_size(cfg, rows) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().mla_output_proj_unfolded_workspace_size(ctypes.byref(cfg), int(rows),
+                                                         ctypes.byref(n)),
+           "mla_output_proj_unfolded_workspace_size")
+    return int(n.value)
+
+
+def mla_output_proj_unfolded(cfg, out_latent, W_UV, W_O, out, workspace, stream=None):
+    a = (_act_dtype(cfg),)
+    K = cfg.num_heads * cfg.d_latent
+    HV = cfg.num_heads * cfg.d_v
+    rows = out_latent.numel() // K
+    _check(lib().mla_output_proj_unfolded(
+        ctypes.byref(cfg), _ptr(out_latent, "out_latent", a, rows * K),
+        _ptr(W_UV, "W_UV", a, cfg.d_latent * HV), _ptr(W_O, "W_O", a, HV * cfg.d_model), rows,
+        _ptr(out, "out", a, rows * cfg.d_model),
+        _ptr(workspace, "workspace", (_torch().uint8,)), workspace.numel(), _stream(stream)),
+        "mla_output_proj_unfolded")
 
 
 def mla_read_device_status(status_word, stream=None) -> int:

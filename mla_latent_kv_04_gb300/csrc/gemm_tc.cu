@@ -223,6 +223,15 @@ struct EpiQLat {              // bf16(qs * v) at (group n, head z, latent dim m)
   }
 };
 
+struct EpiU {                 // bf16 u[n][z * dv + m]: head z's latent output of row n, lifted
+  bf16* u;
+  long long ld;
+  int dv;
+  __device__ __forceinline__ void operator()(int z, int m, int n, float v) const {
+    u[(long long)n * ld + (long long)z * dv + m] = __float2bfloat16_rn(v);
+  }
+};
+
 // ------------------------------------------------------------------------------ host side
 static PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -361,6 +370,30 @@ cudaError_t launch_output_proj_tc(const void* o_lat, const void* W_comb, int row
       acc, reinterpret_cast<bf16*>(out), n);
   note_launch();
   return cudaGetLastError();
+}
+
+// u[r][h][0:d_v] = o_lat[r][h][:] . W_UV[:, h d_v : (h + 1) d_v]  (per head, bf16 out).
+cudaError_t launch_lift_tc(const void* o_lat, const void* W_UV, int rows, int H, int d_c, int d_v,
+                           void* u, int32_t* status, cudaStream_t s) {
+  using namespace gemm;
+  if (rows <= 0) return cudaSuccess;
+  CUtensorMap A, Bm[4];
+  // A = W_UV as head z's M x K: dims {d_v (m), d_c (k), H (z)}; a row of W_UV holds every head
+  if (!map3d(&A, W_UV, (uint64_t)d_v, (uint64_t)d_c, (uint64_t)H, (uint64_t)H * d_v * 2,
+             (uint64_t)d_v * 2, 64, 64) ||
+      // B = o_lat : dims {d_c (k), rows (n), H (z)}
+      !b_maps(Bm, o_lat, (uint64_t)d_c, (uint64_t)rows, (uint64_t)H, (uint64_t)H * d_c * 2,
+              (uint64_t)d_c * 2))
+    return cudaErrorInvalidValue;
+  Params gp{};
+  gp.M = d_v;
+  gp.N = rows;
+  gp.K = d_c;
+  gp.batch = H;
+  gp.m_tiles = (d_v + kBM - 1) / kBM;
+  gp.status = status;
+  return dispatch(A, Bm[0], Bm[1], Bm[2], Bm[3], gp,
+                  EpiU{reinterpret_cast<bf16*>(u), (long long)H * d_v, d_v}, false, s);
 }
 
 // q_lat[g][h][0:d_c] = q_nope[g][h][:] . W_UK_abs[h]  (per head, bf16 out).

@@ -141,6 +141,13 @@ cudaError_t launch_q_rope(mla_dtype act, const void* q_pe, const int32_t* seq_le
                           int q_len, int H, int d_c, int d_r, const RopeTable& rt, float q_scale,
                           int planar, void* q_lat, cudaStream_t s);
 
+// u[r][h][:] = o_lat[r][h][:] . W_i^UV (the latent output lifted to the value width):
+// tensor-core GEMM for bf16 (d_c and d_v multiples of 64), SIMT GEMM otherwise.
+cudaError_t launch_lift_tc(const void* o_lat, const void* W_UV, int rows, int H, int d_c, int d_v,
+                           void* u, int32_t* status, cudaStream_t s);
+cudaError_t launch_lift_simt(mla_dtype act, const void* o_lat, const void* W_UV, int rows, int H,
+                             int d_c, int d_v, void* u, cudaStream_t s);
+
 // out = o_lat . W_comb; `acc` is an fp32 [rows][N] accumulator in the caller's workspace.
 cudaError_t launch_output_proj_simt_ws(mla_dtype act, const void* o_lat, const void* W_comb,
                                        int rows, int K, int N, void* out, float* acc,

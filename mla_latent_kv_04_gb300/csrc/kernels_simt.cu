@@ -818,6 +818,23 @@ static cudaError_t output_proj_t(const void* o_lat, const void* W_comb, int rows
   return cudaGetLastError();
 }
 
+// u[r][h][0:d_v] = o_lat[r][h][:] . W_UV[:, h d_v : (h + 1) d_v], one batch entry per head.
+template <typename T>
+static cudaError_t lift_t(const void* o_lat, const void* W_UV, int rows, int H, int d_c, int d_v,
+                          void* u, cudaStream_t s) {
+  StoreEpi<T> epi{reinterpret_cast<T*>(u), (long long)H * d_v, (long long)d_v};
+  return simt_gemm(reinterpret_cast<const T*>(o_lat), (long long)H * d_c, (long long)d_c,
+                   reinterpret_cast<const T*>(W_UV), (long long)H * d_v, (long long)d_v, rows, d_v,
+                   d_c, H, 1, epi, s);
+}
+
+cudaError_t launch_lift_simt(mla_dtype act, const void* o_lat, const void* W_UV, int rows, int H,
+                             int d_c, int d_v, void* u, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  if (act == MLA_F32) return lift_t<float>(o_lat, W_UV, rows, H, d_c, d_v, u, s);
+  return lift_t<bf16>(o_lat, W_UV, rows, H, d_c, d_v, u, s);
+}
+
 cudaError_t launch_output_proj_simt_ws(mla_dtype act, const void* o_lat, const void* W_comb,
                                        int rows, int K, int N, void* out, float* acc,
                                        cudaStream_t s) {

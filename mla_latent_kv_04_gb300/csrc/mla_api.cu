@@ -440,6 +440,53 @@ mla_status mla_output_proj(const mla_config* cfg, const void* out_latent, const 
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_output_proj");
 }
 
+// workspace of the unfolded projection: fp32 accumulator, status word, lifted u
+static size_t unfolded_acc_bytes(const mla_config* c, int rows) {
+  return align256((size_t)rows * c->d_model * 4);
+}
+static size_t unfolded_u_bytes(const mla_config* c, int rows) {
+  return align256((size_t)rows * c->num_heads * c->d_v * act_size(c->act_dtype));
+}
+
+mla_status mla_output_proj_unfolded_workspace_size(const mla_config* cfg, int rows, size_t* bytes) {
+  mla_status st = check_config(cfg);
+  if (st != MLA_OK) return st;
+  if (rows < 0 || !bytes) return invalid("rows must be >= 0 and bytes non-NULL");
+  *bytes = unfolded_acc_bytes(cfg, rows) + 256 + unfolded_u_bytes(cfg, rows);
+  return MLA_OK;
+}
+
+mla_status mla_output_proj_unfolded(const mla_config* cfg, const void* out_latent, const void* W_UV,
+                                    const void* W_O, int rows, void* out, void* workspace,
+                                    size_t workspace_bytes, void* stream) {
+  mla_status st = check_config(cfg);
+  if (st != MLA_OK) return st;
+  if (rows < 0) return invalid("rows must be >= 0");
+  if (rows == 0) return MLA_OK;
+  if (!out_latent || !W_UV || !W_O || !out) return invalid("null pointer");
+  const size_t acc_bytes = unfolded_acc_bytes(cfg, rows);
+  if (!workspace || workspace_bytes < acc_bytes + 256 + unfolded_u_bytes(cfg, rows)) {
+    g_last_error = "workspace smaller than mla_output_proj_unfolded_workspace_size";
+    return MLA_ERR_WORKSPACE;
+  }
+  if (((uintptr_t)workspace & 255) != 0) return invalid("workspace must be 256-byte aligned");
+  cudaStream_t s = (cudaStream_t)stream;
+  float* acc = (float*)workspace;
+  int32_t* status = (int32_t*)((char*)workspace + acc_bytes);
+  void* u = (char*)workspace + acc_bytes + 256;
+  const int H = cfg->num_heads, d_c = cfg->d_latent, d_v = cfg->d_v, d = cfg->d_model;
+  cudaError_t e;
+  if (cfg->act_dtype == MLA_BF16 && d_c % 64 == 0 && d_v % 64 == 0) {
+    e = launch_lift_tc(out_latent, W_UV, rows, H, d_c, d_v, u, status, s);
+    if (e == cudaSuccess) e = launch_output_proj_tc(u, W_O, rows, H * d_v, d, out, acc, status, s);
+  } else {
+    e = launch_lift_simt(cfg->act_dtype, out_latent, W_UV, rows, H, d_c, d_v, u, s);
+    if (e == cudaSuccess)
+      e = launch_output_proj_simt_ws(cfg->act_dtype, u, W_O, rows, H * d_v, d, out, acc, s);
+  }
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_output_proj_unfolded");
+}
+
 mla_status mla_read_device_status(const void* status_word, void* stream, int* code) {
   if (!status_word || !code) return invalid("null pointer");
   cudaStream_t s = (cudaStream_t)stream;

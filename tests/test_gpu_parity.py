@@ -153,6 +153,33 @@ def test_output_projection_bf16():
     assert np.array_equal(got_a, ref_a)           # a pure relayout: exact
 
 
+@pytest.mark.parametrize("wl_name,rows", [("v2_b32_s4096", 3), ("v2_b32_s4096", 40),
+                                          ("tiny_f32", 5)])
+def test_output_projection_unfolded(wl_name, rows):
+    # huny.dev §3-2 read before the fold: u_i = o_i W_i^UV, out = sum_i u_i W_i^O; the bf16
+    # path runs the tensor-core GEMMs (u rounded to bf16), the fp32 path the SIMT ones
+    base = W.WORKLOADS[wl_name]
+    wl = W.scaled(base, (5, 9) if wl_name != "tiny_f32" else (7,), name=wl_name + "_unfold")
+    st = Hn.build_state(wl, DEV)
+    cfg = st["cfg"]
+    H, d_c, d = wl.dims.num_heads, wl.dims.d_latent, wl.dims.d_model
+    act = Hn.torch_act(wl)
+    rng = np.random.default_rng(6)
+    o_lat = (rng.standard_normal((rows, H * d_c)) * 0.1).astype(np.float32)
+    if wl.act != "f32":
+        o_lat = W.round_bf16(o_lat)
+    o_d = Hn.to_dev(o_lat, act, DEV)
+    out = torch.empty(rows * d, dtype=act, device=DEV)
+    ws = torch.zeros(M.mla_output_proj_unfolded_workspace_size(cfg, rows), dtype=torch.uint8,
+                     device=DEV)
+    M.mla_output_proj_unfolded(cfg, o_d, st["dw"]["W_UV"], st["dw"]["W_O"], out, ws)
+    torch.cuda.synchronize()
+    wts = st["weights"]
+    ref = oracle.mha_output(oracle.lift_latent(o_lat, wts["W_UV"], H), wts["W_O"])
+    got = out.float().cpu().numpy().astype(np.float64).reshape(rows, d)
+    _check(wl, got, ref, "unfolded output projection")
+
+
 # ----------------------------------------------------------------------------- placement
 
 @pytest.mark.parametrize("wl_name", ["tiny_f32", "v2_b32_s4096", "v2_fp8_b128_s8192"])
