@@ -408,6 +408,18 @@ def main():
     for _ in range(args.warmup):
         step(st, inp)
     torch.cuda.synchronize()
+    # The step as one CUDA graph: the library's calls captured once (their launches, memsets
+    # and programmatic launch dependencies), then replayed; this removes the host launch
+    # gaps between the step's kernels. The library counts launches when they are issued, so
+    # the kernels of one step are counted at capture.
+    graph = torch.cuda.CUDAGraph()
+    n_cap = M.mla_kernel_launches()
+    with torch.cuda.graph(graph):
+        step(st, inp)
+    launches_per_step = M.mla_kernel_launches() - n_cap
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
 
     # device-timed region: inputs resident in HBM
     K = args.steps
@@ -422,18 +434,25 @@ def main():
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    launches0 = M.mla_kernel_launches()
     barrier()
     torch.cuda.synchronize()
     t0.record()
     for i in range(K):
-        step(st, inp)
+        graph.replay()
     t1.record()
     torch.cuda.synchronize()
     barrier()
-    launches = M.mla_kernel_launches() - launches0
+    launches = launches_per_step * K
     clk = clocks.stop()
     ms = t0.elapsed_time(t1) / K
+    # the same steps issued call by call on the stream (no graph), for comparison
+    s0, s1 = mk()
+    s0.record()
+    for i in range(K):
+        step(st, inp)
+    s1.record()
+    torch.cuda.synchronize()
+    ms_stream = s0.elapsed_time(s1) / K
     # per-part breakdown in a second pass: the events recorded between the parts (and around
     # the attention kernel) sit between kernels chained by programmatic dependent launch and
     # cost overlap, so they stay out of the headline loop above
@@ -482,10 +501,14 @@ def main():
     lse_host = torch.empty(st["lse"].shape, dtype=torch.float32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
     d2h = out_host.numel() * out_host.element_size() + lse_host.numel() * 4
+    # the graph reads the step's inputs from these device buffers
+    graph_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_e2e):
+        step(st, dev2)
     for _ in range(max(1, args.warmup)):
         for k in dev2:
             dev2[k].copy_(pinned[k], non_blocking=True)
-        step(st, dev2)
+        graph_e2e.replay()
         out_host.copy_(st["out"], non_blocking=True)
         lse_host.copy_(st["lse"], non_blocking=True)
     torch.cuda.synchronize()
@@ -496,7 +519,7 @@ def main():
     for _ in range(K):
         for k in dev2:
             dev2[k].copy_(pinned[k], non_blocking=True)
-        step(st, dev2)
+        graph_e2e.replay()
         out_host.copy_(st["out"], non_blocking=True)
         lse_host.copy_(st["lse"], non_blocking=True)
     e1.record()
@@ -529,6 +552,9 @@ def main():
                    "seq_len": wl.seq_lens[0], "q_len": wl.q_len, "heads": wl.dims.num_heads,
                    "cache_dtype": wl.cache, "page_size": wl.dims.page_size,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "launch": "the step captured once as a CUDA graph and replayed (its kernels, "
+                             "memsets and programmatic launch dependencies); ms_per_step_stream "
+                             "is the same step issued call by call",
                    "l2": "inputs larger than L2: the step streams the 151 MB cache and the "
                          "671 MB folded W_comb"},
         "roofline": roof,
@@ -536,6 +562,7 @@ def main():
                                 traffic=ncu_traffic("attn")),
         "parts_ms": {k: round(v, 4) for k, v in parts.items()},
         "decode_alone_ms": round(decode_alone_ms, 4),
+        "ms_per_step_stream": round(ms_stream, 4),
         "oproj_unfolded": dict(roofline_entry(work["oproj_unfolded"], oproj_unfolded_ms, peaks, tpk),
                                ms=round(oproj_unfolded_ms, 4),
                                note="alternative to the step's folded output projection: "
