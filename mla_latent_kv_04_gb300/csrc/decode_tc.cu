@@ -77,7 +77,9 @@ constexpr uint32_t kColO = 0;                            // O_r: 256 fp32 column
 constexpr uint32_t kColS = 256;                          // raw partial S: 64 fp32 columns
 constexpr uint32_t kColP = 320;                          // P: two buffers of 64 bf16 = 32
 constexpr uint32_t kColQ = 384;                          // Q_r latent part: 256 bf16 = 128
-constexpr int kThreads = 480;                            // 15 warps
+constexpr int kThreads = 480;                            // 15 warps (bf16 cache)
+constexpr int kWarpConv0 = 15;                           // fp8 cache: 4 converter warps after them
+constexpr int kThreadsFp8 = kThreads + 4 * 32;
 constexpr int kSoftmaxWarps = 8;                         // two per head row (column halves)
 constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, 256, false, true);
@@ -90,7 +92,9 @@ enum {
   B_STGREADY0, B_STGREADY1, B_STGFREE0, B_STGFREE1,
   B_RED0,                    // [quarter][page parity]: both halves' row maxima written (2 warps)
   B_LRED0 = B_RED0 + 8,      // [quarter]: both halves' row sums written (2 warps)
-  B_COUNT = B_LRED0 + 4
+  B_CONV0 = B_LRED0 + 4,     // [stage] fp8 cache: the stage converted to bf16 (4 converter warps)
+  B_CVREAD = B_CONV0 + kNS,  // fp8 cache: every converter has read the page's e4m3 bytes (4 warps)
+  B_COUNT = B_CVREAD + 1
 };
 static_assert(B_COUNT * 8 <= kBarArea - 16, "barrier area");
 
@@ -159,9 +163,13 @@ struct PageCursor {
 // undefined, but nothing is read out of bounds). Rank 0 also asks L2 for the whole page
 // (both CTAs' halves, 72 KB contiguous) kL2Ahead pages before its TMA load, so that the
 // load, issued when a stage frees up, reads L2 rather than HBM.
+// An fp8 cache lands as e4m3 bytes (18 KB, unswizzled) in the back half of the stage, for
+// the converter warps to expand into the bf16 layout the MMAs read.
+template <bool kFp8>
 __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensorMap* tm_kc,
                          const CUtensorMap* tm_kpe, const CUtensorMap* tm_qpe, int worker,
                          int rank) {
+  constexpr int kElt = kFp8 ? 1 : 2;                     // cache bytes per element
   const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
   const uint8_t* cache = reinterpret_cast<const uint8_t*>(p.cache);
   PageCursor ahead;
@@ -170,7 +178,7 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
     if (rank != 0 || !ahead.valid()) return;
     const int page = p.block_table[(long long)(ahead.item.group / p.q_len) * p.max_pages + ahead.pg];
     if (page >= 0 && page < p.num_pages)
-      ptx::bulk_prefetch_l2(cache + (long long)page * (kP * kD * 2), kP * kD * 2);
+      ptx::bulk_prefetch_l2(cache + (long long)page * (kP * kD * kElt), kP * kD * kElt);
     ahead.next();
   };
   for (int i = 0; i < kL2Ahead; ++i) ahead.next();      // pages 0..kL2Ahead-1 load directly
@@ -200,11 +208,19 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
       }
       if (!wait_bar(sh, sh.bar(B_EMPTY0 + stage), (wrap & 1) ^ 1, p.status)) return;
       const uint32_t full = sh.bar(B_FULL0 + stage);
-      ptx::mbar_arrive_expect_tx(full, kStageBytes);
+      if constexpr (kFp8) {
+        const uint32_t land = sh.stage(stage) + kStageBytes / 2;
+        ptx::mbar_arrive_expect_tx(full, kStageBytes / 2);
+        ptx::tma_load_2d(land, tm_kc, 256 * rank, page * kP, full);
+        ptx::tma_load_2d(land + 8192, tm_kc, 256 * rank + 128, page * kP, full);
+        ptx::tma_load_2d(land + 16384, tm_kpe, kDC + 32 * rank, page * kP, full);
+      } else {
+        ptx::mbar_arrive_expect_tx(full, kStageBytes);
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        ptx::tma_load_2d(sh.stage(stage) + c * kKTileC, tm_kc, 256 * rank + 64 * c, page * kP, full);
-      ptx::tma_load_2d(sh.stage(stage) + 4 * kKTileC, tm_kpe, kDC + 32 * rank, page * kP, full);
+        for (int c = 0; c < 4; ++c)
+          ptx::tma_load_2d(sh.stage(stage) + c * kKTileC, tm_kc, 256 * rank + 64 * c, page * kP, full);
+        ptx::tma_load_2d(sh.stage(stage) + 4 * kKTileC, tm_kpe, kDC + 32 * rank, page * kP, full);
+      }
       prefetch_next();
       if (++stage == kNS) {
         stage = 0;
@@ -214,8 +230,9 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
   }
 }
 
-// Score MMAs: S = Q_r K_r^T for every page, as soon as the page has landed and the
-// exchange warps have read the previous raw scores.
+// Score MMAs: S = Q_r K_r^T for every page, as soon as the page has landed (with an fp8
+// cache: has been converted) and the exchange warps have read the previous raw scores.
+template <bool kFp8>
 __device__ void qk_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker) {
   const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
   int stage = 0;
@@ -227,7 +244,7 @@ __device__ void qk_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem
         if (!wait_bar(sh, sh.bar(B_QFULL), item_idx & 1, p.status)) return;
         if (!wait_bar(sh, sh.bar(B_QPEFULL), item_idx & 1, p.status)) return;
       }
-      if (!wait_bar(sh, sh.bar(B_FULL0 + stage), wrap & 1, p.status)) return;
+      if (!wait_bar(sh, sh.bar((kFp8 ? B_CONV0 : B_FULL0) + stage), wrap & 1, p.status)) return;
       if (!wait_bar(sh, sh.bar(B_SFREE), (n & 1) ^ 1, p.status)) return;
       ptx::tc_fence_after();
       const uint32_t st = sh.stage(stage);
@@ -642,7 +659,92 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
   }
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// Two e4m3 values (low byte first) -> two bf16 (low half first), exactly: e4m3 -> f16 is
+// exact in hardware, and every e4m3 value (at most 4 significant bits, exponents 2^-9 ..
+// 2^8) is exact in f32 and in bf16.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t v16) {
+  uint32_t h2, out;
+  asm("{\n\t.reg .b16 x;\n\tcvt.u16.u32 x, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, x;\n\t}" : "=r"(h2) : "r"(v16));
+  asm("{\n\t.reg .f16 lo, hi;\n\t.reg .f32 flo, fhi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+      "cvt.f32.f16 flo, lo;\n\tcvt.f32.f16 fhi, hi;\n\tcvt.rn.bf16x2.f32 %0, fhi, flo;\n\t}"
+      : "=r"(out) : "r"(h2));
+  return out;
+}
+
+// 16 e4m3 bytes -> 16 bf16 as two 16-byte vectors (elements in order).
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4& in, uint4& lo, uint4& hi) {
+  lo = make_uint4(e4m3x2_to_bf16x2(in.x & 0xFFFFu), e4m3x2_to_bf16x2(in.x >> 16),
+                  e4m3x2_to_bf16x2(in.y & 0xFFFFu), e4m3x2_to_bf16x2(in.y >> 16));
+  hi = make_uint4(e4m3x2_to_bf16x2(in.z & 0xFFFFu), e4m3x2_to_bf16x2(in.z >> 16),
+                  e4m3x2_to_bf16x2(in.w & 0xFFFFu), e4m3x2_to_bf16x2(in.w >> 16));
+}
+
+// Converter warps (fp8 cache): each page's e4m3 slice (two 128-dim boxes and the 32-dim
+// rope box, unswizzled, in the back half of the stage) -> the bf16 slice in the layout the
+// MMAs read (four 64-dim SW128 chunks and the SW64 rope tile, the whole stage). The stored
+// codes are converted exactly; the cache's scale is folded into the query and the output.
+// The bf16 writes overlap the e4m3 bytes, so every converter reads its share first and the
+// four warps meet at a barrier before any writes. Thread t reads eight 16-byte units of the
+// c boxes (a warp covers 4 rows x 128 bytes, conflict-free) and one of the rope box.
+__device__ void convert_warps(const Shared& sh, const DecodeParams& p, int worker, int warp, int lane) {
+  const int t = 32 * (warp - kWarpConv0) + lane;         // 0..127
+  PageCursor cur;
+  cur.init(p, p.worker_off[worker], p.worker_off[worker + 1]);
+  int stage = 0;
+  uint32_t wrap = 0, n = 0;
+  while (cur.valid()) {
+    if (!wait_bar(sh, sh.bar(B_FULL0 + stage), wrap & 1, p.status)) return;
+    uint8_t* st = sh.base + kOffStage + stage * kStageBytes;
+    const uint8_t* land = st + kStageBytes / 2;
+    uint4 in[9];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = t + 128 * k, j = i >> 9, r = (i >> 3) & 63, u = i & 7;
+      in[k] = *reinterpret_cast<const uint4*>(land + 8192 * j + 128 * r + 16 * u);
+    }
+    in[8] = *reinterpret_cast<const uint4*>(land + 16384 + 32 * (t >> 1) + 16 * (t & 1));
+    // every lane's reads have returned (their values are used) before the warp reports
+    uint32_t dep = 0;
+#pragma unroll
+    for (int k = 0; k < 9; ++k) dep ^= in[k].x;
+    const uint32_t all = __ballot_sync(0xffffffffu, dep != 0x7fc00001u);
+    if (lane == 0 && all != 0x12345678u) ptx::mbar_arrive(sh.bar(B_CVREAD));
+    if (!wait_bar(sh, sh.bar(B_CVREAD), n & 1, p.status)) return;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = t + 128 * k, j = i >> 9, r = (i >> 3) & 63, u = i & 7;
+      // dims 128 j + 16 u .. +15 = 64-dim chunk 2 j + u / 4, 16-byte units 2 (u % 4), +1
+      uint8_t* row = st + (2 * j + (u >> 2)) * kKTileC + 128 * r;
+      const int cb = 2 * (u & 3);
+      uint4 lo, hi;
+      e4m3x16_to_bf16(in[k], lo, hi);
+      *reinterpret_cast<uint4*>(row + ((cb ^ (r & 7)) * 16)) = lo;
+      *reinterpret_cast<uint4*>(row + (((cb + 1) ^ (r & 7)) * 16)) = hi;
+    }
+    {
+      // rope dims 16 u .. +15 of row r -> 16-byte units 2 u, +1 of the 64-byte SW64 row
+      // (64-byte swizzle: unit ^= (row >> 1) & 3)
+      const int r = t >> 1, cb = 2 * (t & 1);
+      uint8_t* row = st + 4 * kKTileC + 64 * r;
+      uint4 lo, hi;
+      e4m3x16_to_bf16(in[8], lo, hi);
+      *reinterpret_cast<uint4*>(row + ((cb ^ ((r >> 1) & 3)) * 16)) = lo;
+      *reinterpret_cast<uint4*>(row + (((cb + 1) ^ ((r >> 1) & 3)) * 16)) = hi;
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(sh.bar(B_CONV0 + stage));
+    ++n;
+    if (++stage == kNS) {
+      stage = 0;
+      ++wrap;
+    }
+    cur.next();
+  }
+}
+
+template <bool kFp8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
                      const __grid_constant__ CUtensorMap tm_kpe,
                      const __grid_constant__ CUtensorMap tm_qpe, const DecodeParams p) {
@@ -678,6 +780,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ptx::mbar_init(sh.bar(B_XEMPTY1), kSoftmaxWarps);
     ptx::mbar_init(sh.bar(B_OFREE), kSoftmaxWarps);
     ptx::mbar_init(sh.bar(B_TEARDOWN), 2);
+    if (kFp8) {
+      for (int s = 0; s < kNS; ++s) ptx::mbar_init(sh.bar(B_CONV0 + s), 4);
+      ptx::mbar_init(sh.bar(B_CVREAD), 4);
+    }
     ptx::mbar_init(sh.bar(B_STGREADY0), 4);
     ptx::mbar_init(sh.bar(B_STGREADY1), 4);
     ptx::mbar_init(sh.bar(B_STGFREE0), kSoftmaxWarps);
@@ -706,9 +812,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ptx::griddep_wait();
 
   if (warp == 0) {
-    if (lane == 0) producer(sh, p, &tm_kc, &tm_kpe, &tm_qpe, worker, rank);
+    if (lane == 0) producer<kFp8>(sh, p, &tm_kc, &tm_kpe, &tm_qpe, worker, rank);
   } else if (warp == 1) {
-    if (lane == 0) qk_issuer(sh, p, tmem, worker);
+    if (lane == 0) qk_issuer<kFp8>(sh, p, tmem, worker);
+  } else if (kFp8 && warp >= kWarpConv0) {
+    convert_warps(sh, p, worker, warp, lane);
   } else if (warp <= 5) {
     send_warps(sh, p, tmem, worker, rank, warp, lane);
   } else if (warp <= 13) {
@@ -771,6 +879,19 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_cols
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over an e4m3 cache viewed as bytes [rows][576], unswizzled; box = box_cols x box_rows.
+bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kD};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D map over the rotated query parts of the planar query ([groups][128][64] bf16 at
 // element offset 512 * 128 of each 128 x 576 group block); box = 32 columns x 128 heads.
 bool make_qpe_map(CUtensorMap* m, const void* q_lat, uint64_t groups) {
@@ -789,7 +910,8 @@ bool make_qpe_map(CUtensorMap* m, const void* q_lat, uint64_t groups) {
 }  // namespace tc
 
 bool tc_decode_supported(const mla_config* c) {
-  return c && c->act_dtype == MLA_BF16 && c->cache_dtype == MLA_BF16 && c->num_heads == tc::kH &&
+  return c && c->act_dtype == MLA_BF16 &&
+         (c->cache_dtype == MLA_BF16 || c->cache_dtype == MLA_FP8_E4M3) && c->num_heads == tc::kH &&
          c->d_latent == tc::kDC && c->d_rope == tc::kDR && c->page_size == tc::kP;
 }
 
@@ -800,7 +922,7 @@ int tc_decode_max_workers() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (cached[dev] == 0) {
-    if (cudaFuncSetAttribute(tc::decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tc::decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              tc::kSmemBytes) != cudaSuccess)
       return 0;
     cudaLaunchConfig_t cfg = {};
@@ -815,7 +937,7 @@ int tc_decode_max_workers() {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc::decode_tc_kernel, &cfg) != cudaSuccess || n <= 0)
+    if (cudaOccupancyMaxActiveClusters(&n, tc::decode_tc_kernel<false>, &cfg) != cudaSuccess || n <= 0)
       return 0;
     cached[dev] = n;
   }
@@ -823,20 +945,23 @@ int tc_decode_max_workers() {
 }
 
 cudaError_t launch_decode_tc(mla_dtype cache, const DecodeParams& p, cudaStream_t s) {
-  if (cache != MLA_BF16) return cudaErrorNotSupported;
+  if (cache != MLA_BF16 && cache != MLA_FP8_E4M3) return cudaErrorNotSupported;
+  const bool fp8 = (cache == MLA_FP8_E4M3);
   CUtensorMap kc, kpe, qpe;
   const uint64_t cache_rows = (uint64_t)p.num_pages * tc::kP;
   const uint64_t groups = (uint64_t)p.batch * p.q_len;
-  if (!tc::make_map(&kc, p.cache, cache_rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tc::make_map(&kpe, p.cache, cache_rows, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !tc::make_qpe_map(&qpe, p.q_lat, groups))
-    return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(tc::decode_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
+  const bool maps =
+      fp8 ? (tc::make_map_u8(&kc, p.cache, cache_rows, 128, 64) &&
+             tc::make_map_u8(&kpe, p.cache, cache_rows, 32, 64))
+          : (tc::make_map(&kc, p.cache, cache_rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+             tc::make_map(&kpe, p.cache, cache_rows, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B));
+  if (!maps || !tc::make_qpe_map(&qpe, p.q_lat, groups)) return cudaErrorInvalidValue;
+  auto kern = fp8 ? tc::decode_tc_kernel<true> : tc::decode_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * p.workers, 1, 1);
-  cfg.blockDim = dim3(tc::kThreads, 1, 1);
+  cfg.blockDim = dim3(fp8 ? tc::kThreadsFp8 : tc::kThreads, 1, 1);
   cfg.dynamicSmemBytes = tc::kSmemBytes;
   cfg.stream = s;
   cudaLaunchAttribute attr;
@@ -844,7 +969,7 @@ cudaError_t launch_decode_tc(mla_dtype cache, const DecodeParams& p, cudaStream_
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, tc::decode_tc_kernel, kc, kpe, qpe, p);
+  e = cudaLaunchKernelEx(&cfg, kern, kc, kpe, qpe, p);
   note_launch();
   return e;
 }

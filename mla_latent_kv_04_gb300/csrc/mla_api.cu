@@ -312,7 +312,9 @@ mla_status mla_decode_ex(const mla_config* cfg, const void* q_nope, const void* 
   cudaError_t e = cudaSuccess;
   if (cfg->act_dtype == MLA_BF16) {
     // the tensor-core attention takes its query pre-multiplied by softmax_scale * log2(e)
-    const float q_scale = tc ? softmax_scale_of(cfg) * kLog2e : 1.f;
+    // (and by an fp8 cache's scale: it multiplies the stored codes, converted exactly)
+    const float code_scale = cfg->cache_dtype == MLA_FP8_E4M3 ? cfg->cache_scale : 1.f;
+    const float q_scale = tc ? softmax_scale_of(cfg) * kLog2e * code_scale : 1.f;
     // ... and in the planar layout (see internal.h)
     const int planar = tc ? 1 : 0;
     // one launch: the query absorption GEMM with the planner (which clears the status word)

@@ -106,13 +106,15 @@ def test_split_count_invariance(kernel):
         assert d <= 1e-2 * np.max(np.abs(outs[0]["out_latent"])) + 1e-3
 
 
-@pytest.mark.parametrize("kernel", [M.KERNEL_SIMT], ids=_kernel_id)
+@pytest.mark.parametrize("kernel", KERNELS, ids=_kernel_id)
 def test_fp8_cache_small(kernel):
-    wl = W.scaled(W.WORKLOADS["v2_fp8_b128_s8192"], (5, 64, 300, 1), name="v2_fp8_small")
+    # partial pages, several pages, splits; e4m3 codes in the cache, one per-tensor scale
+    wl = W.scaled(W.WORKLOADS["v2_fp8_b128_s8192"], (5, 64, 300, 1, 1000), name="v2_fp8_small")
     st = Hn.build_state(wl, DEV)
-    r = Hn.run_decode(wl, st, DEV, kernel=kernel)
-    assert r["status"] == M.MLA_OK
-    _check_all_requests(wl, st, r)
+    for nw in (0, 3):
+        r = Hn.run_decode(wl, st, DEV, kernel=kernel, num_workers=nw)
+        assert r["status"] == M.MLA_OK
+        _check_all_requests(wl, st, r)
 
 
 def test_decompressed_oracle_agrees_on_gpu_inputs():
