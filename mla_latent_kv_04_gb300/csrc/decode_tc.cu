@@ -172,13 +172,16 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
   constexpr int kElt = kFp8 ? 1 : 2;                     // cache bytes per element
   const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
   const uint8_t* cache = reinterpret_cast<const uint8_t*>(p.cache);
+  // the cache is read once: its lines go first out of L2, so that what this decode reads
+  // again (queries, and the split partials the combine kernel merges) stays there
+  const uint64_t pol = ptx::l2_policy_evict_first();
   PageCursor ahead;
   ahead.init(p, it0, it1);
   auto prefetch_next = [&]() {
     if (rank != 0 || !ahead.valid()) return;
     const int page = p.block_table[(long long)(ahead.item.group / p.q_len) * p.max_pages + ahead.pg];
     if (page >= 0 && page < p.num_pages)
-      ptx::bulk_prefetch_l2(cache + (long long)page * (kP * kD * kElt), kP * kD * kElt);
+      ptx::bulk_prefetch_l2_hint(cache + (long long)page * (kP * kD * kElt), kP * kD * kElt, pol);
     ahead.next();
   };
   for (int i = 0; i < kL2Ahead; ++i) ahead.next();      // pages 0..kL2Ahead-1 load directly
@@ -211,15 +214,17 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
       if constexpr (kFp8) {
         const uint32_t land = sh.stage(stage) + kStageBytes / 2;
         ptx::mbar_arrive_expect_tx(full, kStageBytes / 2);
-        ptx::tma_load_2d(land, tm_kc, 256 * rank, page * kP, full);
-        ptx::tma_load_2d(land + 8192, tm_kc, 256 * rank + 128, page * kP, full);
-        ptx::tma_load_2d(land + 16384, tm_kpe, kDC + 32 * rank, page * kP, full);
+        ptx::tma_load_2d_hint(land, tm_kc, 256 * rank, page * kP, full, pol);
+        ptx::tma_load_2d_hint(land + 8192, tm_kc, 256 * rank + 128, page * kP, full, pol);
+        ptx::tma_load_2d_hint(land + 16384, tm_kpe, kDC + 32 * rank, page * kP, full, pol);
       } else {
         ptx::mbar_arrive_expect_tx(full, kStageBytes);
 #pragma unroll
         for (int c = 0; c < 4; ++c)
-          ptx::tma_load_2d(sh.stage(stage) + c * kKTileC, tm_kc, 256 * rank + 64 * c, page * kP, full);
-        ptx::tma_load_2d(sh.stage(stage) + 4 * kKTileC, tm_kpe, kDC + 32 * rank, page * kP, full);
+          ptx::tma_load_2d_hint(sh.stage(stage) + c * kKTileC, tm_kc, 256 * rank + 64 * c, page * kP,
+                                full, pol);
+        ptx::tma_load_2d_hint(sh.stage(stage) + 4 * kKTileC, tm_kpe, kDC + 32 * rank, page * kP, full,
+                              pol);
       }
       prefetch_next();
       if (++stage == kNS) {
