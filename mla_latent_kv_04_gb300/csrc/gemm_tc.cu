@@ -142,14 +142,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool ok = true;
 
   if (warp == 0 && lane == 0) {
+    // every A operand here is a weight read once per decode step: its lines go first out of L2
+    const uint64_t pol = ptx::l2_policy_evict_first();
     int stage = 0;
     uint32_t wrap = 0;
     for (int kb = kb0; kb < kb1; ++kb) {
       if (!wait_bar(empty(stage), (wrap & 1) ^ 1, abort, gp.status)) break;
       const uint32_t st = base + stage * C::kStageBytes;
       ptx::mbar_arrive_expect_tx(full(stage), C::kStageBytes);
-      ptx::tma_load_3d(st, &tmA, m0, kb * kBK, z, full(stage));
-      ptx::tma_load_3d(st + 8192, &tmA, m0 + 64, kb * kBK, z, full(stage));
+      ptx::tma_load_3d_hint(st, &tmA, m0, kb * kBK, z, full(stage), pol);
+      ptx::tma_load_3d_hint(st + 8192, &tmA, m0 + 64, kb * kBK, z, full(stage), pol);
       ptx::tma_load_3d(st + C::kABytes, &tmB, kb * kBK, n0, z, full(stage));
       if (++stage == C::kStages) { stage = 0; ++wrap; }
     }
