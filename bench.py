@@ -254,10 +254,10 @@ def kernel_work(wl):
 # of the kernel (summaries under profiles/), valid only while the kernel's source file is
 # the one captured: each entry carries that file's sha256 and reads as null otherwise.
 NCU_TRAFFIC = {
-    "attn": {"bytes": 157550848 + 4771584, "source": "mla_latent_kv_04_gb300/csrc/decode_tc.cu",
-             "sha256": "e4afc260fe1acdcf4dcb6188e81592ea46c915bc00921c276f3f95819de28da0"},
-    "oproj": {"bytes": 676020736 + 3005952, "source": "mla_latent_kv_04_gb300/csrc/gemm_tc.cu",
-              "sha256": "8c77bc985fbcb9479e8f1b27644d50ca34a61061432579b8c00f4b7dfeb41b32"},
+    "attn": {"bytes": 155789824 + 2767104, "source": "mla_latent_kv_04_gb300/csrc/decode_tc.cu",
+             "sha256": "74b359452a6386f8d9d758d5b5deca41f055b1bfbec54fad4d68c2abf039e66b"},
+    "oproj": {"bytes": 676007680 + 2829824, "source": "mla_latent_kv_04_gb300/csrc/gemm_tc.cu",
+              "sha256": "fcc76f4f5e020deb941e793c1e12aea0b2b609c7b9f0ca895c90148578e69783"},
 }
 
 
