@@ -140,6 +140,10 @@ __global__ void __launch_bounds__(128) append_latent_kernel(
   const long long slot = append_slot(req_ids, positions, block_table, batch, max_pages, num_pages,
                                      P, r, (threadIdx.x == 0) ? status : nullptr, &pos);
   if (slot < 0) return;
+  // launched with programmatic serialization after the projection that writes c_kv / k_pe
+  // (the finish of an append from h): its page slot is found while that GEMM ends (no-op
+  // otherwise)
+  ptx::griddep_wait();
   const int D = d_c + d_r;
   CT* dst = cache + slot * D;
   for (int e = threadIdx.x; e < D / 2; e += blockDim.x) {
@@ -730,17 +734,30 @@ cudaError_t launch_append_finish(mla_dtype cache, const float* acc, int T, const
                                  cudaStream_t s) {
   if (T <= 0) return cudaSuccess;
   const long long ld = d_c + d_r;
+  // programmatic serialization: the blocks start while the projection GEMM (which signals
+  // launch_dependents at its start) ends, and wait for it before reading `acc`
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(T, 1, 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
   if (cache == MLA_BF16)
-    append_latent_kernel<float, bf16><<<T, 128, 0, s>>>(acc, acc + d_c, ld, ld, req_ids, positions,
-                                                        block_table, batch, max_pages,
-                                                        reinterpret_cast<bf16*>(cache_ptr), num_pages,
-                                                        P, d_c, d_r, 1, rt, cache_scale, status);
+    e = cudaLaunchKernelEx(&cfg, append_latent_kernel<float, bf16>, (const float*)acc,
+                           (const float*)(acc + d_c), ld, ld, req_ids, positions, block_table, batch,
+                           max_pages, reinterpret_cast<bf16*>(cache_ptr), num_pages, P, d_c, d_r, 1, rt,
+                           cache_scale, status);
   else
-    append_latent_kernel<float, uint8_t><<<T, 128, 0, s>>>(
-        acc, acc + d_c, ld, ld, req_ids, positions, block_table, batch, max_pages,
-        reinterpret_cast<uint8_t*>(cache_ptr), num_pages, P, d_c, d_r, 1, rt, cache_scale, status);
+    e = cudaLaunchKernelEx(&cfg, append_latent_kernel<float, uint8_t>, (const float*)acc,
+                           (const float*)(acc + d_c), ld, ld, req_ids, positions, block_table, batch,
+                           max_pages, reinterpret_cast<uint8_t*>(cache_ptr), num_pages, P, d_c, d_r, 1,
+                           rt, cache_scale, status);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 template <typename AT, typename CT>
