@@ -32,6 +32,9 @@ struct Params {
   int reset_status;      // 1: block 0 clears *status first (the first kernel of a decode call)
   int pdl;               // 1: launched with programmatic serialization after the kernel it
                          // overlaps; the grid waits for that kernel at its end
+  int wait_first;        // 1: launched with programmatic serialization as the first kernel of a
+                         // call; every block waits for the kernel before it ahead of reading
+                         // any input (only the launch and set-up overlap that kernel)
   int plan_block;        // 1: one extra block runs the decode's split planner
   PlanParams plan;
   int rope_blocks;       // extra blocks that rotate q_pe (after the planner block)
@@ -91,6 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int side_blocks = gp.plan_block;
   const int main_end = (int)gridDim.x - gp.rope_blocks;
   if ((int)blockIdx.x < side_blocks || (int)blockIdx.x >= main_end) {
+    if (gp.wait_first) ptx::griddep_wait();
     if ((int)blockIdx.x < side_blocks) {
       plan_body(gp.plan, reinterpret_cast<int*>(basep), true);
     } else {
@@ -139,6 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (gp.wait_first) ptx::griddep_wait();   // the inputs (the token operand) are the previous kernels'
   bool ok = true;
 
   if (warp == 0 && lane == 0) {
@@ -338,6 +343,8 @@ static bool b_maps(CUtensorMap (&maps)[4], const void* ptr, uint64_t K, uint64_t
 }
 
 __global__ void finish_oproj_kernel(float* __restrict__ acc, bf16* __restrict__ out, long long n) {
+  // launched with programmatic serialization after the split-K GEMM that fills `acc`
+  ptx::griddep_wait();
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
     out[i] = __float2bfloat16_rn(acc[i]);
@@ -368,10 +375,20 @@ cudaError_t launch_output_proj_tc(const void* o_lat, const void* W_comb, int row
   e = dispatch(A, Bm[0], Bm[1], Bm[2], Bm[3], gp, EpiAtomic{acc, (long long)N}, true, s);
   if (e != cudaSuccess) return e;
   const long long n = (long long)rows * N;
-  finish_oproj_kernel<<<(int)((n + 255) / 256 < 2048 ? (n + 255) / 256 : 2048), 256, 0, s>>>(
-      acc, reinterpret_cast<bf16*>(out), n);
+  // programmatic serialization: the conversion's blocks start while the GEMM (which signals
+  // launch_dependents at its start) ends, and wait for it before reading `acc`
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((n + 255) / 256 < 2048 ? (n + 255) / 256 : 2048), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, finish_oproj_kernel, acc, reinterpret_cast<bf16*>(out), n);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 // u[r][h][0:d_v] = o_lat[r][h][:] . W_UV[:, h d_v : (h + 1) d_v]  (per head, bf16 out).
@@ -422,7 +439,10 @@ cudaError_t launch_query_absorb_tc(const void* q_nope, const void* W_UK_abs, int
   // with the planner as an extra block this is the decode's first kernel and the planner
   // clears the status word; otherwise the prep kernel before it did
   gp.reset_status = 0;
-  gp.pdl = plan ? 0 : 1;
+  // with the planner it is also launched with programmatic serialization, waiting for the
+  // kernel before it (whatever the caller ran) ahead of every read of an input
+  gp.pdl = 1;
+  gp.wait_first = plan ? 1 : 0;
   gp.plan_block = plan ? 1 : 0;
   if (plan) gp.plan = *plan;
   gp.rope_blocks = rope ? rope->groups * rope->hblocks : 0;

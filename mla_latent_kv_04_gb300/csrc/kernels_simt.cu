@@ -139,6 +139,8 @@ __global__ void __launch_bounds__(128) append_latent_kernel(
   int pos = 0;
   const long long slot = append_slot(req_ids, positions, block_table, batch, max_pages, num_pages,
                                      P, r, (threadIdx.x == 0) ? status : nullptr, &pos);
+  // a kernel launched after this one with programmatic serialization may start its set-up
+  ptx::griddep_launch_dependents();
   if (slot < 0) return;
   // launched with programmatic serialization after the projection that writes c_kv / k_pe
   // (the finish of an append from h): its page slot is found while that GEMM ends (no-op
