@@ -238,10 +238,26 @@ def kernel_work(wl):
     return {
         "attn": {"bytes": attn_bytes, "flops": attn_flops},
         "decode": {"bytes": sum(dec_b.values()), "flops": W.decode_flops(wl)},
-        "oproj": {"bytes": 676009728 + 2774528, "source": "mla_latent_kv_04_gb300/csrc/gemm_tc.cu",
+        "oproj": {"bytes": K * d.d_model * ea + rows * K * ea + rows * d.d_model * ea,
+                  "flops": 2.0 * rows * K * d.d_model},
+        "append": {"bytes": rows * d.d_model * ea + d.d_model * d.d_cache * ea
+                   + rows * d.d_cache * W.elt_bytes(wl.cache),
+                   "flops": 2.0 * rows * d.d_model * d.d_cache},
+        # the unfolded output path: W_UV and W_O instead of W_comb (not part of the step)
+        "oproj_unfolded": {"bytes": (d.d_latent * H * d.d_v + H * d.d_v * d.d_model) * ea
+                           + rows * K * ea + rows * d.d_model * ea,
+                           "flops": 2.0 * rows * (K * d.d_v + H * d.d_v * d.d_model)},
+    }
+
+
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture
+# of the kernel (summaries under profiles/), valid only while the kernel's source file is
+# the one captured: each entry carries that file's sha256 and reads as null otherwise.
+NCU_TRAFFIC = {
+    "attn": {"bytes": 155789824 + 2767104, "source": "mla_latent_kv_04_gb300/csrc/decode_tc.cu",
+             "sha256": "74b359452a6386f8d9d758d5b5deca41f055b1bfbec54fad4d68c2abf039e66b"},
+    "oproj": {"bytes": 676009728 + 2774528, "source": "mla_latent_kv_04_gb300/csrc/gemm_tc.cu",
               "sha256": "beea09b47825d73a81f70bf3be30b51c3aef29343d76b00171c9457511693a89"},
-    "oproj": {"bytes": 676007680 + 2829824, "source": "mla_latent_kv_04_gb300/csrc/gemm_tc.cu",
-              "sha256": "fcc76f4f5e020deb941e793c1e12aea0b2b609c7b9f0ca895c90148578e69783"},
 }
 
 
