@@ -73,10 +73,16 @@ def test_tiny_f32_ragged_multi_request():
 
 SMALL_Q1 = (1, 2, 63, 64, 65, 130, 700, 0)
 SMALL_Q2 = (2, 3, 64, 65, 129, 0, 517)
+# several causal query tokens per request (speculative decoding); q 64 is a chunk of a
+# chunked prefill. Lengths include steps whose every token is new (seq_len == q_len).
+SMALL_Q4 = (4, 5, 64, 67, 0, 300)
+SMALL_Q8 = (8, 71, 128, 513)
+CHUNK_Q64 = (64, 65, 190)
 
 
 @pytest.mark.parametrize("kernel", KERNELS, ids=_kernel_id)
-@pytest.mark.parametrize("q_len,lens", [(1, SMALL_Q1), (2, SMALL_Q2)], ids=["q1", "q2"])
+@pytest.mark.parametrize("q_len,lens", [(1, SMALL_Q1), (2, SMALL_Q2), (4, SMALL_Q4), (8, SMALL_Q8),
+                                        (64, CHUNK_Q64)], ids=["q1", "q2", "q4", "q8", "q64"])
 def test_v2_bf16_small_ragged(kernel, q_len, lens):
     wl = W.scaled(W.WORKLOADS["v2_b32_s4096"], lens, name=f"v2_small_q{q_len}", q_len=q_len,
                   new_from_h=q_len)
@@ -239,6 +245,83 @@ def test_append_from_h_values():
             assert np.max(np.abs(g - rows[p])) <= 1e-2 * np.max(np.abs(rows)) + 1e-3
 
 
+def _nearest_e4m3_ok(codes, v, slack):
+    """Each e4m3 code is a nearest code (saturating at 448) to some value within ``slack`` of
+    the exact value v, all in code units: the device rounds its fp32 result, which differs
+    from v by at most the slack, so where v lies that close to the midpoint of two codes
+    either one is accepted. The sign must match unless the code is zero."""
+    table = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))     # increasing
+    a = np.minimum(np.abs(v), 448.0)
+    i = np.searchsorted(table, a)
+    best = np.minimum(np.abs(table[np.minimum(i, len(table) - 1)] - a),
+                      np.abs(table[np.maximum(i - 1, 0)] - a))
+    got = oracle.e4m3_decode(codes)
+    ok_sign = (got == 0) | (np.sign(got) == np.sign(v))
+    return ok_sign & (np.abs(np.abs(got) - a) <= best + 2.0 * slack)
+
+
+@pytest.mark.parametrize("cache_kind", ["bf16", "fp8_e4m3"])
+def test_append_prefill_chunks_from_h(cache_kind):
+    # Chunked prefill: every position of three requests comes from h through the append
+    # projection, in two calls of 1500 and 501 rows whose rows mix the requests in random
+    # order. The projection GEMM spans several 256-token tiles and a ragged tail.
+    wl = W.scaled(W.WORKLOADS["v2_b32_s4096"], (700, 1, 1300), name="v2_prefill_" + cache_kind,
+                  fill="h", cache=cache_kind)
+    fp8 = cache_kind == "fp8_e4m3"
+    cfg = Hn.config(wl, cache_scale=6.0 / 448.0 if fp8 else None)
+    act = Hn.torch_act(wl)
+    wts = W.weights(wl)
+    W_d = Hn.to_dev(wts["W_DKV_KR"], act, DEV)
+    bt, num_pages = W.page_table(wl)
+    cache = Hn.alloc_cache(wl, num_pages, DEV)
+    bt_d = Hn.to_dev(bt, torch.int32, DEV)
+    hs, reqs, poss = [], [], []
+    for b, S in enumerate(wl.seq_lens):
+        hs.append(W.hidden(wl, b, S))
+        r_, p_ = W.append_batch(wl, b, 0, S)
+        reqs.append(r_)
+        poss.append(p_)
+    h, req, pos = np.concatenate(hs), np.concatenate(reqs), np.concatenate(poss)
+    perm = np.random.default_rng(12).permutation(len(req))
+    h, req, pos = h[perm], req[perm], pos[perm]
+    status = torch.zeros(4, dtype=torch.int32, device=DEV)
+    for lo, hi in ((0, 1500), (1500, len(req))):
+        ws = torch.empty(M.mla_append_cache_workspace_size(cfg, hi - lo), dtype=torch.uint8, device=DEV)
+        M.mla_append_cache(cfg, Hn.to_dev(h[lo:hi], act, DEV), W_d,
+                           Hn.to_dev(req[lo:hi], torch.int32, DEV), Hn.to_dev(pos[lo:hi], torch.int32, DEV),
+                           bt_d, cache, dev_status=status, workspace=ws)
+    assert M.mla_read_device_status(status) == M.MLA_OK
+    D, P = wl.dims.d_cache, wl.dims.page_size
+    if fp8:
+        raw = cache.cpu().numpy().reshape(num_pages, P, D)
+        fill = np.uint8(Hn.SENTINEL["fp8_e4m3"])
+    else:
+        raw = cache.view(torch.int16).cpu().numpy().view(np.uint16).reshape(num_pages, P, D)
+        fill = np.uint16(Hn.SENTINEL["bf16"])
+    written = np.zeros((num_pages, P), bool)
+    for b, S in enumerate(wl.seq_lens):
+        c, kraw = oracle.project_latent(W.hidden(wl, b, S).astype(np.float64), wts["W_DKV_KR"],
+                                        wl.dims.d_latent)
+        ref = np.concatenate([c, oracle.rope(kraw, np.arange(S), wl.rope_theta)], axis=1)
+        pg, sl = bt[b, np.arange(S) // P], np.arange(S) % P
+        written[pg, sl] = True
+        if fp8:
+            # fp32 error of the device's dot products: a small multiple of the unit roundoff
+            # times sum_k |h_k W_kj| (the rotation adds the bounds of a pair), plus the
+            # rotation's own relative error
+            hb = np.abs(W.hidden(wl, b, S)).astype(np.float64) @ np.abs(wts["W_DKV_KR"]).astype(np.float64)
+            kb = np.repeat(hb[:, wl.dims.d_latent::2] + hb[:, wl.dims.d_latent + 1::2], 2, axis=1)
+            v = ref / cfg.cache_scale
+            slack = 1e-6 * np.concatenate([hb[:, :wl.dims.d_latent], kb], axis=1) / cfg.cache_scale
+            ok = _nearest_e4m3_ok(raw[pg, sl], v, slack + 1e-5 * np.abs(v))
+            assert ok.all(), f"request {b}: {int((~ok).sum())} codes are not a nearest e4m3 code"
+        else:
+            got = raw[pg, sl].astype(np.uint32) << 16
+            got = got.view(np.float32).astype(np.float64)
+            _check(wl, got, ref, f"cache rows of request {b}")
+    assert (raw[~written] == fill).all(), "a slot no append wrote lost its sentinel"
+
+
 # ----------------------------------------------------------------------------- guards
 
 def test_device_guard_skips_bad_pages_and_lengths():
@@ -274,6 +357,7 @@ FULL = [
     ("v2_long_splitkv", [0, 3], list(range(0, 128, 4))),
     ("v2_ragged_spec", [0, 101, 255], None),
     ("v2_fp8_b128_s8192", [0, 64, 127], None),
+    ("v2_spec_q4", [0, 37, 63], None),
 ]
 
 

@@ -324,15 +324,23 @@ def test_dominant_key_wins():
     assert hit >= 1
 
 
-def test_causal_token_equals_shorter_request():
-    # query token 0 of a 2-token step sees exactly the keys a 1-token step one shorter sees.
-    T = _tiny_case(seed=15, S=29, q=2)
+@pytest.mark.parametrize("S,q", [(29, 2), (29, 5), (40, 8), (8, 8)])
+def test_causal_token_equals_shorter_request(S, q):
+    # Speculative decoding (secrett2633.cloud "[vLLM] Multi-head Latent Attention", the
+    # reshape_query_for_spec_decode step) with the causal reading: query token t of a q-token
+    # step sees exactly the keys a 1-token step of length S - q + t + 1 sees. (8, 8) is a step
+    # whose every token is new: its first token sees only key 0.
+    T = _tiny_case(seed=15, S=S, q=q)
     W_UK_abs, _ = oracle.absorb_weights(T["W_UK"], T["W_UV"], T["W_O"], T["H"])
-    o2, l2 = oracle.decode_absorbed(T["c"], T["k_rot"], T["q_nope"], T["q_pe"], W_UK_abs,
+    oq, lq = oracle.decode_absorbed(T["c"], T["k_rot"], T["q_nope"], T["q_pe"], W_UK_abs,
                                     T["scale"])
-    o1, l1 = oracle.decode_absorbed(T["c"][:28], T["k_rot"][:28], T["q_nope"][:1],
-                                    T["q_pe"][:1], W_UK_abs, T["scale"])
-    assert np.array_equal(o2[0], o1[0]) and np.array_equal(l2[0], l1[0])
+    for t in range(q):
+        n = S - q + t + 1
+        o1, l1 = oracle.decode_absorbed(T["c"][:n], T["k_rot"][:n], T["q_nope"][t:t + 1],
+                                        T["q_pe"][t:t + 1], W_UK_abs, T["scale"])
+        assert np.array_equal(oq[t], o1[0]) and np.array_equal(lq[t], l1[0])
+    if S == q:
+        assert np.array_equal(oq[0], np.broadcast_to(T["c"][0], oq[0].shape))
 
 
 def test_empty_request():

@@ -111,6 +111,11 @@ WORKLOADS = {
         seed=3, fill="latent", new_from_h=2,
         description="ragged large-batch speculative decode, bf16: batch 256, lognormal lengths "
                     "(median 2048, clipped 512..8192), 2 query tokens, 2 tokens appended from h"),
+    "v2_spec_q4": Workload(
+        name="v2_spec_q4", dims=V2, act="bf16", cache="bf16", seq_lens=(4096,) * 64, q_len=4,
+        seed=5, fill="latent", new_from_h=4,
+        description="multi-token speculative decode, bf16: batch 64, seq_len 4096, 4 causal "
+                    "query tokens per request, the 4 new tokens appended from h"),
     "v2_fp8_b128_s8192": Workload(
         name="v2_fp8_b128_s8192", dims=V2, act="bf16", cache="fp8_e4m3", seq_lens=(8192,) * 128,
         q_len=1, seed=4, fill="latent",
