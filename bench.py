@@ -251,20 +251,23 @@ def kernel_work(wl):
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture
-# of the kernel (summaries under profiles/), valid only while the kernel's source file is
-# the one captured: each entry carries that file's sha256 and reads as null otherwise.
+# of the kernel on one workload (summaries under profiles/), valid only for that workload and
+# while the kernel's source file is the one captured: each entry carries the workload's name
+# and that file's sha256, and reads as null otherwise.
 NCU_TRAFFIC = {
-    "attn": {"bytes": 155789824 + 2767104, "source": "mla_latent_kv_04_gb300/csrc/decode_tc.cu",
+    "attn": {"bytes": 155789824 + 2767104, "workload": "v2_b32_s4096",
+             "source": "mla_latent_kv_04_gb300/csrc/decode_tc.cu",
              "sha256": "74b359452a6386f8d9d758d5b5deca41f055b1bfbec54fad4d68c2abf039e66b"},
-    "oproj": {"bytes": 676009728 + 2774528, "source": "mla_latent_kv_04_gb300/csrc/gemm_tc.cu",
+    "oproj": {"bytes": 676009728 + 2774528, "workload": "v2_b32_s4096",
+              "source": "mla_latent_kv_04_gb300/csrc/gemm_tc.cu",
               "sha256": "beea09b47825d73a81f70bf3be30b51c3aef29343d76b00171c9457511693a89"},
 }
 
 
-def ncu_traffic(part):
+def ncu_traffic(part, workload="v2_b32_s4096"):
     import hashlib
     e = NCU_TRAFFIC.get(part)
-    if not e:
+    if not e or e["workload"] != workload:
         return None
     try:
         with open(os.path.join(ROOT, e["source"]), "rb") as f:
@@ -542,7 +545,9 @@ def main():
              "append": "mla_append_cache"}
     roof = dict(rl[dom])
     roof["kernel"] = names[dom]
-    roof["traffic"] = ncu_traffic(dom)
+    roof["traffic"] = ncu_traffic(dom, wl.name)
+    cache_mb = wl.total_tokens * wl.dims.d_cache * W.elt_bytes(wl.cache) / 1e6
+    wcomb_mb = wl.dims.num_heads * wl.dims.d_latent * wl.dims.d_model * W.elt_bytes(wl.act) / 1e6
     roof["peak_source"] = peaks["source"] + (" (sustained bf16)" if roof["bound"] == "tensor" else "")
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -555,11 +560,11 @@ def main():
                    "launch": "the step captured once as a CUDA graph and replayed (its kernels, "
                              "memsets and programmatic launch dependencies); ms_per_step_stream "
                              "is the same step issued call by call",
-                   "l2": "inputs larger than L2: the step streams the 151 MB cache and the "
-                         "671 MB folded W_comb"},
+                   "l2": f"inputs larger than L2: the step streams the {cache_mb:.0f} MB cache "
+                         f"and the {wcomb_mb:.0f} MB folded W_comb"},
         "roofline": roof,
         "decode_roofline": dict(rl["attn"], kernel="mla_decode attention kernel",
-                                traffic=ncu_traffic("attn")),
+                                traffic=ncu_traffic("attn", wl.name)),
         "parts_ms": {k: round(v, 4) for k, v in parts.items()},
         "decode_alone_ms": round(decode_alone_ms, 4),
         "ms_per_step_stream": round(ms_stream, 4),
