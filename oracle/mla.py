@@ -37,7 +37,8 @@ import numpy as np
 __all__ = [
     "softmax_scale", "rope", "project_latent", "decompress", "decode_decompressed",
     "absorb_weights", "absorbed_query", "decode_absorbed", "output_projection",
-    "lift_latent", "mha_output", "e4m3_encode", "e4m3_decode", "cache_image", "cache_elems_per_token",
+    "lift_latent", "mha_output", "compress_query", "merge_query_weights", "merged_query",
+    "e4m3_encode", "e4m3_decode", "cache_image", "cache_elems_per_token",
     "cache_bytes", "combine_partials",
 ]
 
@@ -75,6 +76,41 @@ def project_latent(h, W_DKV_KR, d_latent: int):
     """
     P = np.asarray(h, np.float64) @ np.asarray(W_DKV_KR, np.float64)
     return P[:, :d_latent], P[:, d_latent:]
+
+
+def compress_query(h, W_DQ, W_UQ, W_QR, num_heads: int):
+    """The query side: c^Q_t = h_t W^DQ and q^C_{t,i} = c^Q_t W_i^UQ ([P1] §2-2, low-rank
+    query compression), and head i's rotary query before its rotation, h_t W_i^QR ([P1] §2-3;
+    the decode rotates it at the query position).
+
+    W_DQ [d_model][d_q]; W_UQ [d_q][H*d_n], head i owning columns i*d_n..(i+1)*d_n-1; W_QR
+    [d_model][H*d_r] likewise. Returns q_nope [T][H][d_n], q_pe [T][H][d_r] (not rotated) and
+    c_q [T][d_q].
+    """
+    h = np.asarray(h, np.float64)
+    c_q = h @ np.asarray(W_DQ, np.float64)
+    q_nope = (c_q @ np.asarray(W_UQ, np.float64)).reshape(h.shape[0], num_heads, -1)
+    q_pe = (h @ np.asarray(W_QR, np.float64)).reshape(h.shape[0], num_heads, -1)
+    return q_nope, q_pe, c_q
+
+
+def merge_query_weights(W_UQ, W_UK, num_heads: int):
+    """The latent-query weight multiplied into the latent-key weight ([P4] "어텐션은 무엇을
+    캐시하는가": the two merge into one): W^UQK_i = W_i^UQ (W_i^UK)^T, so that head i's
+    absorbed query is c^Q W^UQK_i without forming q^C.
+
+    W_UQ [d_q][H*d_n], W_UK [d_c][H*d_n] -> [H][d_q][d_c].
+    """
+    W_UQ = np.asarray(W_UQ, np.float64)
+    W_UK = np.asarray(W_UK, np.float64)
+    d_n = W_UQ.shape[1] // num_heads
+    return np.stack([W_UQ[:, i * d_n:(i + 1) * d_n] @ W_UK[:, i * d_n:(i + 1) * d_n].T
+                     for i in range(num_heads)])
+
+
+def merged_query(c_q, W_UQK):
+    """q_hat_i = c^Q W^UQK_i. c_q [T][d_q], W_UQK [H][d_q][d_c] -> [T][H][d_c]."""
+    return np.einsum("tq,hqc->thc", np.asarray(c_q, np.float64), np.asarray(W_UQK, np.float64))
 
 
 def decompress(c, W_UK, W_UV, num_heads: int):

@@ -133,6 +133,69 @@ def test_project_latent_splits_columns():
     assert np.array_equal(c, h[:, :16]) and np.array_equal(k, h[:, 16:])
 
 
+def test_compress_query_by_brute_force():
+    # huny.dev "DeepSeek MLA 해부" §2-2 (c^Q = h W^DQ, q^C_i = c^Q W_i^UQ) and §2-3 (the
+    # rotary query h W_i^QR), evaluated with plain Python sums over the definitions.
+    rng = _rng(41)
+    T, d, d_q, H, d_n, d_r = 3, 7, 5, 3, 4, 2
+    h = rng.standard_normal((T, d))
+    W_DQ = rng.standard_normal((d, d_q))
+    W_UQ = rng.standard_normal((d_q, H * d_n))
+    W_QR = rng.standard_normal((d, H * d_r))
+    q_nope, q_pe, c_q = oracle.compress_query(h, W_DQ, W_UQ, W_QR, H)
+    assert q_nope.shape == (T, H, d_n) and q_pe.shape == (T, H, d_r) and c_q.shape == (T, d_q)
+    for t in range(T):
+        for i in range(H):
+            for n in range(d_n):
+                ref = 0.0
+                for r in range(d_q):
+                    cq = 0.0
+                    for k in range(d):
+                        cq += h[t, k] * W_DQ[k, r]
+                    ref += cq * W_UQ[r, i * d_n + n]
+                assert q_nope[t, i, n] == pytest.approx(ref, rel=1e-12, abs=1e-12)
+            for r in range(d_r):
+                ref = sum(h[t, k] * W_QR[k, i * d_r + r] for k in range(d))
+                assert q_pe[t, i, r] == pytest.approx(ref, rel=1e-12, abs=1e-12)
+
+
+def test_compress_query_identity_weights_pick_head_blocks():
+    # W^DQ = I and W^UQ = I: head i's content query is c^Q's i-th block of d_n features;
+    # W^QR = I: head i's rotary query is h's i-th block of d_r features.
+    rng = _rng(42)
+    H, d_n = 3, 4
+    h = rng.standard_normal((2, H * d_n))
+    q_nope, q_pe, c_q = oracle.compress_query(h, np.eye(H * d_n), np.eye(H * d_n),
+                                              np.eye(H * d_n), H)
+    assert np.array_equal(c_q, h)
+    for i in range(H):
+        assert np.array_equal(q_nope[:, i], h[:, i * d_n:(i + 1) * d_n])
+        assert np.array_equal(q_pe[:, i], h[:, i * d_n:(i + 1) * d_n])
+
+
+def test_merged_query_weights_equal_two_steps():
+    # thakicloud "어텐션은 무엇을 캐시하는가": the latent-query and latent-key weights multiply
+    # into one. (c^Q W_i^UQ) (W_i^UK)^T = c^Q (W_i^UQ (W_i^UK)^T) by associativity.
+    rng = _rng(43)
+    T, d, d_q, H, d_n, d_r, d_c = 4, 12, 6, 3, 5, 2, 7
+    h = rng.standard_normal((T, d))
+    W_DQ = rng.standard_normal((d, d_q))
+    W_UQ = rng.standard_normal((d_q, H * d_n))
+    W_QR = rng.standard_normal((d, H * d_r))
+    W_UK = rng.standard_normal((d_c, H * d_n))
+    q_nope, _, c_q = oracle.compress_query(h, W_DQ, W_UQ, W_QR, H)
+    W_UK_abs, _ = oracle.absorb_weights(W_UK, W_UK, np.zeros((H * d_n, 1)), H)
+    two_step = oracle.absorbed_query(q_nope, W_UK_abs)
+    W_UQK = oracle.merge_query_weights(W_UQ, W_UK, H)
+    assert W_UQK.shape == (H, d_q, d_c)
+    one_step = oracle.merged_query(c_q, W_UQK)
+    assert np.max(np.abs(one_step - two_step)) <= 1e-12 * np.max(np.abs(two_step))
+    # and element by element from the definition q_hat_i = q^C_i . W_i^UK rows
+    for t, i, c in ((0, 0, 0), (3, 2, 6), (1, 1, 3)):
+        ref = sum(q_nope[t, i, n] * W_UK[c, i * d_n + n] for n in range(d_n))
+        assert one_step[t, i, c] == pytest.approx(ref, rel=1e-12)
+
+
 def test_decompress_uses_head_column_blocks():
     rng = _rng(4)
     d_c, H, d_n = 8, 3, 4

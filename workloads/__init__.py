@@ -37,14 +37,17 @@ class Dims:
     d_nope: int
     d_v: int
     page_size: int = PAGE
+    d_q: int = 0            # query compression rank (c^Q width)
 
     @property
     def d_cache(self) -> int:
         return self.d_latent + self.d_rope
 
 
-V2 = Dims(num_heads=128, d_model=5120, d_latent=512, d_rope=64, d_nope=128, d_v=128)
-TINY = Dims(num_heads=16, d_model=256, d_latent=64, d_rope=16, d_nope=32, d_v=32)
+# d_q: the pages write c^Q = h W^DQ without its width; 1536 is DeepSeek-V2's, 48 = 3 d_c / 4
+# keeps the tiny shape's proportion between the query and latent ranks.
+V2 = Dims(num_heads=128, d_model=5120, d_latent=512, d_rope=64, d_nope=128, d_v=128, d_q=1536)
+TINY = Dims(num_heads=16, d_model=256, d_latent=64, d_rope=16, d_nope=32, d_v=32, d_q=48)
 
 
 @dataclass(frozen=True)
@@ -180,6 +183,22 @@ def weights(wl: Workload) -> dict:
         "W_UV": normal(wl, "W_UV", (d.d_latent, H * d.d_v), 1.0 / math.sqrt(d.d_latent)),
         "W_O": normal(wl, "W_O", (H * d.d_v, d.d_model), 1.0 / math.sqrt(H * d.d_v)),
     }
+
+
+def query_weights(wl: Workload) -> dict:
+    """Query-side weights, each N(0, 1/fan_in), in the activation dtype: W_DQ_QR = [W^DQ | W^QR]
+    [d_model][d_q + H*d_r] (both read h) and W_UQ [d_q][H*d_n]."""
+    d = wl.dims
+    H = d.num_heads
+    return {
+        "W_DQ_QR": normal(wl, "W_DQ_QR", (d.d_model, d.d_q + H * d.d_rope), 1.0 / math.sqrt(d.d_model)),
+        "W_UQ": normal(wl, "W_UQ", (d.d_q, H * d.d_nope), 1.0 / math.sqrt(d.d_q)),
+    }
+
+
+def query_hidden(wl: Workload, rows: int) -> np.ndarray:
+    """Hidden states [rows][d_model] ~ N(0,1) of the step's query tokens."""
+    return normal(wl, "h_q", (rows, wl.dims.d_model))
 
 
 def queries(wl: Workload) -> dict:
