@@ -191,12 +191,19 @@ def setup(wl, dev):
                        device=dev)
     n_a = M.mla_append_cache_workspace_size(cfg, rows)
     ws_a = torch.zeros(n_a, dtype=torch.uint8, device=dev) if n_a else None
+    # the query side from h (low-rank query compression), timed beside the step
+    qdw = {k: up(v) for k, v in W.query_weights(wl).items()}
+    query = {"w": qdw, "h": up(W.query_hidden(wl, rows)),
+             "q_nope": torch.empty(rows * H * d.d_nope, dtype=act, device=dev),
+             "q_pe": torch.empty(rows * H * d.d_rope, dtype=act, device=dev),
+             "ws": torch.zeros(M.mla_query_workspace_size(cfg, d.d_q, rows), dtype=torch.uint8,
+                               device=dev)}
     torch.cuda.synchronize()
     return {"cfg": cfg, "dw": dw, "cache": cache, "bt_d": bt_d, "W_UK_abs": W_UK_abs,
             "W_comb": W_comb, "host": host, "dev_in": dev_in,
             "new_req": up(new_req, torch.int32), "new_pos": up(new_pos, torch.int32),
             "out_lat": out_lat, "lse": lse, "out": out, "ws": ws, "ws_o": ws_o, "ws_u": ws_u,
-            "ws_a": ws_a,
+            "ws_a": ws_a, "query": query,
             "status": status}
 
 
@@ -243,6 +250,12 @@ def kernel_work(wl):
         "append": {"bytes": rows * d.d_model * ea + d.d_model * d.d_cache * ea
                    + rows * d.d_cache * W.elt_bytes(wl.cache),
                    "flops": 2.0 * rows * d.d_model * d.d_cache},
+        # the step's queries from h: W_DQ, W_UQ, W_QR, h in, q_nope and q_pe out (c_q, an
+        # intermediate, is not counted)
+        "query": {"bytes": (d.d_model * d.d_q + d.d_q * H * d.d_nope + d.d_model * H * d.d_rope) * ea
+                  + rows * d.d_model * ea + rows * H * (d.d_nope + d.d_rope) * ea,
+                  "flops": 2.0 * rows * (d.d_model * d.d_q + d.d_q * H * d.d_nope
+                                         + d.d_model * H * d.d_rope)},
         # the unfolded output path: W_UV and W_O instead of W_comb (not part of the step)
         "oproj_unfolded": {"bytes": (d.d_latent * H * d.d_v + H * d.d_v * d.d_model) * ea
                            + rows * K * ea + rows * d.d_model * ea,
@@ -484,6 +497,16 @@ def main():
     u1.record()
     torch.cuda.synchronize()
     oproj_unfolded_ms = u0.elapsed_time(u1) / K
+    # the queries from h (c^Q = h W^DQ, q^C = c^Q W^UQ, q^R = h W^QR), alone, back to back
+    qj = st["query"]
+    v0, v1 = mk()
+    v0.record()
+    for i in range(K):
+        M.mla_query_from_hidden(st["cfg"], wl.dims.d_q, qj["h"], qj["w"]["W_DQ"], qj["w"]["W_UQ"],
+                                qj["w"]["W_QR"], qj["q_nope"], qj["q_pe"], qj["ws"])
+    v1.record()
+    torch.cuda.synchronize()
+    query_ms = v0.elapsed_time(v1) / K
     if world > 1:
         tt = torch.tensor([ms], dtype=torch.float64)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
@@ -568,6 +591,11 @@ def main():
         "parts_ms": {k: round(v, 4) for k, v in parts.items()},
         "decode_alone_ms": round(decode_alone_ms, 4),
         "ms_per_step_stream": round(ms_stream, 4),
+        "query_from_hidden": dict(roofline_entry(work["query"], query_ms, peaks, tpk),
+                                  ms=round(query_ms, 4),
+                                  note="the step's queries from h: c^Q = h W^DQ, q^C = c^Q W^UQ, "
+                                       "q^R = h W^QR (mla_query_from_hidden); timed alone, not "
+                                       "part of the step, whose q_nope and q_pe are inputs"),
         "oproj_unfolded": dict(roofline_entry(work["oproj_unfolded"], oproj_unfolded_ms, peaks, tpk),
                                ms=round(oproj_unfolded_ms, 4),
                                note="alternative to the step's folded output projection: "

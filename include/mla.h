@@ -215,6 +215,29 @@ mla_status mla_output_proj_unfolded(const mla_config* cfg, const void* out_laten
                                     const void* W_O, int rows, void* out, void* workspace,
                                     size_t workspace_bytes, void* stream);
 
+/* Bytes of workspace mla_query_from_hidden needs for T query rows and query rank d_q. */
+mla_status mla_query_workspace_size(const mla_config* cfg, int d_q, int T, size_t* bytes);
+
+/* The step's queries from the hidden states, by low-rank query compression (huny.dev
+ * "DeepSeek MLA 해부" §2-2) and the per-head rotary query (§2-3):
+ *   c_q[t]       = h[t] W_DQ                              (d -> d_q, rounded to the act dtype)
+ *   q_nope[t][i] = c_q[t] W_UQ[:, i*d_n : (i+1)*d_n]
+ *   q_pe[t][i]   = h[t] W_QR[:, i*d_r : (i+1)*d_r]       (not rotated: mla_decode rotates it
+ *                                                          at the query position)
+ *   h [T][d]; W_DQ [d][d_q]; W_UQ [d_q][H*d_n]; W_QR [d][H*d_r]; outputs q_nope [T][H][d_n]
+ *   and q_pe [T][H][d_r], the layouts mla_decode reads (row b*q_len + t), all in the act
+ *   dtype, fp32 accumulation. W_UQ stays separate from W_UK: merging them per head
+ *   (W_i^UQ (W_i^UK)^T, d_q x d_c) would make the step read H*d_q*d_c weight elements (201 MB at
+ *   DeepSeek-V2 shapes) instead of H*d_q*d_n + H*d_n*d_c (67 MB).
+ *   workspace: 256-byte aligned device buffer of mla_query_workspace_size bytes (an fp32
+ *   accumulator, a status word and c_q). d_q > 0; T == 0 is a no-op. Errors: MLA_ERR_INVALID
+ *   (null pointers, bad sizes), MLA_ERR_WORKSPACE, MLA_ERR_CUDA; nothing is launched on an
+ *   error found on the host. */
+mla_status mla_query_from_hidden(const mla_config* cfg, int d_q, const void* h, const void* W_DQ,
+                                 const void* W_UQ, const void* W_QR, int T, void* q_nope,
+                                 void* q_pe, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
 /* Wait for `stream`, then read the device status word at `status_word` (a decode
  * workspace or an append dev_status) into *code (an mla_status value, MLA_OK if clean)
  * and reset it to 0. */

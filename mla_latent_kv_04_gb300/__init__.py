@@ -76,6 +76,8 @@ _SIGNATURES = {
     "mla_output_proj": (_I, [_CFG, _P, _P, _I, _P, _P, _SZ, _P]),
     "mla_output_proj_unfolded_workspace_size": (_I, [_CFG, _I, ctypes.POINTER(_SZ)]),
     "mla_output_proj_unfolded": (_I, [_CFG, _P, _P, _P, _I, _P, _P, _SZ, _P]),
+    "mla_query_workspace_size": (_I, [_CFG, _I, _I, ctypes.POINTER(_SZ)]),
+    "mla_query_from_hidden": (_I, [_CFG, _I, _P, _P, _P, _P, _I, _P, _P, _P, _SZ, _P]),
     "mla_read_device_status": (_I, [_P, _P, ctypes.POINTER(_I)]),
     "mla_status_string": (ctypes.c_char_p, [_I]),
     "mla_last_error": (ctypes.c_char_p, []),
@@ -338,6 +340,26 @@ def mla_output_proj_unfolded(cfg, out_latent, W_UV, W_O, out, workspace, stream=
         _ptr(out, "out", a, rows * cfg.d_model),
         _ptr(workspace, "workspace", (_torch().uint8,)), workspace.numel(), _stream(stream)),
         "mla_output_proj_unfolded")
+
+
+def mla_query_workspace_size(cfg, d_q, T) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().mla_query_workspace_size(ctypes.byref(cfg), int(d_q), int(T), ctypes.byref(n)),
+           "mla_query_workspace_size")
+    return int(n.value)
+
+
+def mla_query_from_hidden(cfg, d_q, h, W_DQ, W_UQ, W_QR, q_nope, q_pe, workspace, stream=None):
+    """h [T][d_model] -> q_nope [T][H][d_n], q_pe [T][H][d_r] (not rotated)."""
+    a = (_act_dtype(cfg),)
+    d, H = cfg.d_model, cfg.num_heads
+    T = h.numel() // d
+    _check(lib().mla_query_from_hidden(
+        ctypes.byref(cfg), int(d_q), _ptr(h, "h", a, T * d), _ptr(W_DQ, "W_DQ", a, d * d_q),
+        _ptr(W_UQ, "W_UQ", a, d_q * H * cfg.d_nope), _ptr(W_QR, "W_QR", a, d * H * cfg.d_rope), T,
+        _ptr(q_nope, "q_nope", a, T * H * cfg.d_nope), _ptr(q_pe, "q_pe", a, T * H * cfg.d_rope),
+        _ptr(workspace, "workspace", (_torch().uint8,)), workspace.numel(), _stream(stream)),
+        "mla_query_from_hidden")
 
 
 def mla_read_device_status(status_word, stream=None) -> int:

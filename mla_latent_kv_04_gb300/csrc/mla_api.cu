@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 #include <string>
 
@@ -487,6 +488,65 @@ mla_status mla_output_proj_unfolded(const mla_config* cfg, const void* out_laten
       e = launch_output_proj_simt_ws(cfg->act_dtype, u, W_O, rows, H * d_v, d, out, acc, s);
   }
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_output_proj_unfolded");
+}
+
+// Query side: three GEMMs through fp32 accumulators, one accumulator region reused in stream
+// order (each GEMM zeroes it after the previous conversion has read it).
+static size_t query_acc_bytes(const mla_config* c, int d_q, int T) {
+  const size_t w = std::max<size_t>((size_t)d_q,
+                                    std::max((size_t)c->num_heads * c->d_rope,
+                                             (size_t)c->num_heads * c->d_nope));
+  return align256((size_t)T * w * 4);
+}
+static size_t query_cq_bytes(const mla_config* c, int d_q, int T) {
+  return align256((size_t)T * d_q * act_size(c->act_dtype));
+}
+
+mla_status mla_query_workspace_size(const mla_config* cfg, int d_q, int T, size_t* bytes) {
+  mla_status st = check_config(cfg);
+  if (st != MLA_OK) return st;
+  if (d_q <= 0 || T < 0 || !bytes) return invalid("d_q must be positive, T >= 0, bytes non-NULL");
+  *bytes = query_acc_bytes(cfg, d_q, T) + 256 + query_cq_bytes(cfg, d_q, T);
+  return MLA_OK;
+}
+
+mla_status mla_query_from_hidden(const mla_config* cfg, int d_q, const void* h, const void* W_DQ,
+                                 const void* W_UQ, const void* W_QR, int T, void* q_nope,
+                                 void* q_pe, void* workspace, size_t workspace_bytes,
+                                 void* stream) {
+  mla_status st = check_config(cfg);
+  if (st != MLA_OK) return st;
+  if (d_q <= 0 || T < 0) return invalid("d_q must be positive and T >= 0");
+  if (T == 0) return MLA_OK;
+  if (!h || !W_DQ || !W_UQ || !W_QR || !q_nope || !q_pe) return invalid("null pointer");
+  const size_t acc_bytes = query_acc_bytes(cfg, d_q, T);
+  if (!workspace || workspace_bytes < acc_bytes + 256 + query_cq_bytes(cfg, d_q, T)) {
+    g_last_error = "workspace smaller than mla_query_workspace_size";
+    return MLA_ERR_WORKSPACE;
+  }
+  if (((uintptr_t)workspace & 255) != 0) return invalid("workspace must be 256-byte aligned");
+  cudaStream_t s = (cudaStream_t)stream;
+  float* acc = (float*)workspace;
+  int32_t* status = (int32_t*)((char*)workspace + acc_bytes);
+  void* c_q = (char*)workspace + acc_bytes + 256;
+  const int H = cfg->num_heads, d = cfg->d_model;
+  const int n_pe = H * cfg->d_rope, n_nope = H * cfg->d_nope;
+  // tensor maps need 16-byte row strides: every row length a multiple of 8 bf16 elements
+  const bool tc = cfg->act_dtype == MLA_BF16 && d % 8 == 0 && d_q % 8 == 0 && n_pe % 8 == 0 &&
+                  n_nope % 8 == 0;
+  cudaError_t e;
+  if (tc) {
+    e = launch_output_proj_tc(h, W_DQ, T, d, d_q, c_q, acc, status, s);
+    if (e == cudaSuccess) e = launch_output_proj_tc(h, W_QR, T, d, n_pe, q_pe, acc, status, s);
+    if (e == cudaSuccess) e = launch_output_proj_tc(c_q, W_UQ, T, d_q, n_nope, q_nope, acc, status, s);
+  } else {
+    e = launch_output_proj_simt_ws(cfg->act_dtype, h, W_DQ, T, d, d_q, c_q, acc, s);
+    if (e == cudaSuccess)
+      e = launch_output_proj_simt_ws(cfg->act_dtype, h, W_QR, T, d, n_pe, q_pe, acc, s);
+    if (e == cudaSuccess)
+      e = launch_output_proj_simt_ws(cfg->act_dtype, c_q, W_UQ, T, d_q, n_nope, q_nope, acc, s);
+  }
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_query_from_hidden");
 }
 
 mla_status mla_read_device_status(const void* status_word, void* stream, int* code) {

@@ -188,6 +188,33 @@ def test_output_projection_unfolded(wl_name, rows):
     _check(wl, got, ref, "unfolded output projection")
 
 
+# ----------------------------------------------------------------------------- query side
+
+@pytest.mark.parametrize("wl_name,rows", [("v2_b32_s4096", 3), ("v2_b32_s4096", 40),
+                                          ("tiny_f32", 5)], ids=["v2_3rows", "v2_40rows", "tiny_f32"])
+def test_query_from_hidden(wl_name, rows):
+    # c^Q = h W^DQ, q^C_i = c^Q W_i^UQ, un-rotated q^R_i = h W_i^QR against the oracle
+    wl = W.WORKLOADS[wl_name]
+    d = wl.dims
+    H = d.num_heads
+    cfg = Hn.config(wl)
+    act = Hn.torch_act(wl)
+    qw = W.query_weights(wl)
+    h = W.query_hidden(wl, rows)
+    dw = {k: Hn.to_dev(v, act, DEV) for k, v in qw.items()}
+    q_nope = torch.empty(rows * H * d.d_nope, dtype=act, device=DEV)
+    q_pe = torch.empty(rows * H * d.d_rope, dtype=act, device=DEV)
+    ws = torch.zeros(M.mla_query_workspace_size(cfg, d.d_q, rows), dtype=torch.uint8, device=DEV)
+    M.mla_query_from_hidden(cfg, d.d_q, Hn.to_dev(h, act, DEV), dw["W_DQ"], dw["W_UQ"], dw["W_QR"],
+                            q_nope, q_pe, ws)
+    torch.cuda.synchronize()
+    ref_n, ref_p, _ = oracle.compress_query(h, qw["W_DQ"], qw["W_UQ"], qw["W_QR"], H)
+    got_n = q_nope.float().cpu().numpy().astype(np.float64).reshape(rows, H, d.d_nope)
+    got_p = q_pe.float().cpu().numpy().astype(np.float64).reshape(rows, H, d.d_rope)
+    _check(wl, got_n, ref_n, "q_nope from h")
+    _check(wl, got_p, ref_p, "q_pe from h")
+
+
 # ----------------------------------------------------------------------------- placement
 
 @pytest.mark.parametrize("wl_name", ["tiny_f32", "v2_b32_s4096", "v2_fp8_b128_s8192"])

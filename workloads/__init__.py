@@ -186,13 +186,14 @@ def weights(wl: Workload) -> dict:
 
 
 def query_weights(wl: Workload) -> dict:
-    """Query-side weights, each N(0, 1/fan_in), in the activation dtype: W_DQ_QR = [W^DQ | W^QR]
-    [d_model][d_q + H*d_r] (both read h) and W_UQ [d_q][H*d_n]."""
+    """Query-side weights, each N(0, 1/fan_in), in the activation dtype: W_DQ [d_model][d_q],
+    W_UQ [d_q][H*d_n] and W_QR [d_model][H*d_r] (head i owns columns i*d_n.. / i*d_r..)."""
     d = wl.dims
     H = d.num_heads
     return {
-        "W_DQ_QR": normal(wl, "W_DQ_QR", (d.d_model, d.d_q + H * d.d_rope), 1.0 / math.sqrt(d.d_model)),
+        "W_DQ": normal(wl, "W_DQ", (d.d_model, d.d_q), 1.0 / math.sqrt(d.d_model)),
         "W_UQ": normal(wl, "W_UQ", (d.d_q, H * d.d_nope), 1.0 / math.sqrt(d.d_q)),
+        "W_QR": normal(wl, "W_QR", (d.d_model, H * d.d_rope), 1.0 / math.sqrt(d.d_model)),
     }
 
 
