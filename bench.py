@@ -359,9 +359,36 @@ def cpu_oracle(wl, budget_s, max_requests=10 ** 9, warm=0):
     return tps, threads, desc, res
 
 
+# ----------------------------------------------------------------------------- ranks
+
+def rank_env():
+    """(world, rank, local_rank) from torchrun's environment; (1, 0, 0) without it."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """The largest x over all ranks (the slowest replica sets the job's time). Needs the
+    process group when world > 1."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank_step: int, world: int, ms: float) -> float:
+    """Whole-job tokens/s: the tokens every replica processes in one step over the slowest
+    replica's step time."""
+    return tokens_per_rank_step * world / (ms * 1e-3)
+
+
 def run_reference(args):
-    """The reference arm: the CPU oracle on this host, one request of the workload per step."""
-    rank = int(os.environ.get("RANK", "0"))
+    """The reference arm: the CPU oracle on this host, one request of the workload per step.
+    Under torchrun only rank 0 works and prints; the other ranks return at once."""
+    _, rank, _ = rank_env()
     if rank != 0:
         return
     wl = W.WORKLOADS[args.workload]
@@ -403,9 +430,7 @@ def main():
     import torch
     import mla_latent_kv_04_gb300 as M
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("gloo")
@@ -507,12 +532,8 @@ def main():
     v1.record()
     torch.cuda.synchronize()
     query_ms = v0.elapsed_time(v1) / K
-    if world > 1:
-        tt = torch.tensor([ms], dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
-    tokens_per_step = wl.batch * wl.q_len * world
-    value = tokens_per_step / (ms * 1e-3)
+    ms = max_over_ranks(ms, world)
+    value = job_throughput(wl.batch * wl.q_len, world, ms)
     code = M.mla_read_device_status(st["status"])
     code2 = M.mla_read_device_status(st["ws"])
     assert code == M.MLA_OK and code2 == M.MLA_OK, (code, code2)
@@ -552,10 +573,7 @@ def main():
     torch.cuda.synchronize()
     barrier()
     ms_e2e = e0.elapsed_time(e1) / K
-    if world > 1:
-        tt = torch.tensor([ms_e2e], dtype=torch.float64)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_e2e = float(tt.item())
+    ms_e2e = max_over_ranks(ms_e2e, world)
 
     if rank != 0:
         return
@@ -604,7 +622,7 @@ def main():
         "parts_roofline": rl,
         "clocks": clk,
         "gpu_launches": int(launches),
-        "e2e": {"value": round(tokens_per_step / (ms_e2e * 1e-3), 1), "unit": UNIT,
+        "e2e": {"value": round(job_throughput(wl.batch * wl.q_len, world, ms_e2e), 1), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "ms_per_step": round(ms_e2e, 4)},
     }
