@@ -120,3 +120,34 @@ def test_workspace_grows_with_batch(lib):
     assert b > a > 0
     assert M.mla_output_proj_workspace_size(c, 32) == 32 * 5120 * 4 + 256
     assert M.mla_append_cache_workspace_size(c, 32) == 32 * 576 * 4
+
+
+def test_query_call_validates_before_any_launch(lib):
+    c = _cfg()
+    n = ctypes.c_size_t(0)
+    assert lib.mla_query_workspace_size(ctypes.byref(c), 0, 4, ctypes.byref(n)) == M.MLA_ERR_INVALID
+    assert lib.mla_query_workspace_size(ctypes.byref(c), 1536, 4, ctypes.byref(n)) == M.MLA_OK
+    # an fp32 accumulator as wide as the widest of the three products, a status word, c^Q
+    assert n.value == 4 * (128 * 128) * 4 + 256 + 4 * 1536 * 2
+    fake = ctypes.c_void_p(256)
+    st = lib.mla_query_from_hidden(ctypes.byref(c), 1536, None, fake, fake, fake, 4, fake, fake,
+                                   fake, n.value, None)
+    assert st == M.MLA_ERR_INVALID
+    st = lib.mla_query_from_hidden(ctypes.byref(c), 1536, fake, fake, fake, fake, 4, fake, fake,
+                                   None, 0, None)
+    assert st == M.MLA_ERR_WORKSPACE
+    st = lib.mla_query_from_hidden(ctypes.byref(c), 1536, fake, fake, fake, fake, 4, fake, fake,
+                                   ctypes.c_void_p(256 + 16), n.value, None)
+    assert st == M.MLA_ERR_INVALID          # workspace not 256-byte aligned
+    # T == 0 is a no-op that touches nothing
+    st = lib.mla_query_from_hidden(ctypes.byref(c), 1536, None, None, None, None, 0, None, None,
+                                   None, 0, None)
+    assert st == M.MLA_OK
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    # no silent fallback: a missing libmla.so is an error at the first call
+    monkeypatch.setattr(M, "LIB_PATH", str(tmp_path / "missing" / "libmla.so"))
+    monkeypatch.setattr(M, "_lib_handle", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        M.lib()
