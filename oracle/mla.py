@@ -38,8 +38,8 @@ __all__ = [
     "softmax_scale", "rope", "project_latent", "decompress", "decode_decompressed",
     "absorb_weights", "absorbed_query", "decode_absorbed", "output_projection",
     "lift_latent", "mha_output", "compress_query", "merge_query_weights", "merged_query",
-    "e4m3_encode", "e4m3_decode", "cache_image", "cache_elems_per_token",
-    "cache_bytes", "combine_partials",
+    "e4m3_encode", "e4m3_decode", "e4m3_block_quantize", "e4m3_block_dequantize",
+    "cache_image", "cache_elems_per_token", "cache_bytes", "combine_partials",
 ]
 
 
@@ -327,6 +327,39 @@ def e4m3_encode(x):
     out = code.astype(np.uint8)
     # the sign bit is kept even when the magnitude rounds to zero (-0 is 0x80)
     return np.where(np.signbit(x), out | 0x80, out).astype(np.uint8)
+
+
+def e4m3_block_quantize(x, block: int = 128):
+    """Block-wise dynamic e4m3 quantisation of latent rows, the fp8 cache [P1] §6 describes
+    for DeepSeek-V3: the latent vector in fp8 with a scale per block, computed from the
+    values when they are written (the decoupled rotary key stays in bf16 and is not passed
+    here). The pages give no block size; a block is `block` consecutive elements of one
+    token's row.
+
+    Per block: scale = fp32(amax |x|) / 448 rounded once to fp32; codes = e4m3_encode of the
+    fp32 quotient fp32(x) / scale (each quotient rounded once to fp32, then encoded exactly).
+    A block of zeros has scale 0 and codes 0. x [n][d], d a multiple of block -> (codes uint8
+    [n][d], scales float32 [n][d / block]).
+    """
+    x32 = np.asarray(x, dtype=np.float32)
+    n, d = x32.shape
+    assert d % block == 0
+    xb = x32.reshape(n, d // block, block)
+    amax = np.max(np.abs(xb), axis=2).astype(np.float32)
+    scales = (amax / np.float32(448.0)).astype(np.float32)
+    safe = np.where(scales > 0, scales, np.float32(1.0)).astype(np.float32)
+    quot = (xb / safe[..., None]).astype(np.float32)
+    codes = e4m3_encode(quot)
+    codes = np.where((scales > 0)[..., None], codes, np.uint8(0)).astype(np.uint8)
+    return codes.reshape(n, d), scales
+
+
+def e4m3_block_dequantize(codes, scales, block: int = 128):
+    """Value of block-quantised rows: code value times its block's scale (float64)."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    n, d = codes.shape
+    v = e4m3_decode(codes).reshape(n, d // block, block)
+    return (v * np.asarray(scales, np.float64)[..., None]).reshape(n, d)
 
 
 # ----------------------------------------------------------------------------- paged cache

@@ -485,6 +485,55 @@ def test_e4m3_round_trip_is_exact_on_codes():
 
 # ----------------------------------------------------------------------------- paged cache
 
+def test_block_quantize_round_trips_codes_times_a_power_of_two():
+    # huny.dev §6 (fp8 latent with per-block dynamic scales): rows built as e4m3 code values
+    # times a power-of-two scale, each block holding a +-448 code, come back bit for bit.
+    rng = _rng(51)
+    n, d, block = 6, 512, 128
+    codes = rng.integers(0, 0x7F, size=(n, d), dtype=np.uint8) | (rng.integers(0, 2, (n, d)) << 7).astype(np.uint8)
+    codes[:, ::block] = 0x7E                           # 448 in every block
+    s = 2.0 ** rng.integers(-12, 4, size=(n, d // block))
+    x = oracle.e4m3_decode(codes).reshape(n, d // block, block) * s[..., None]
+    got_c, got_s = oracle.e4m3_block_quantize(x.reshape(n, d), block)
+    assert np.array_equal(got_s, s.astype(np.float32))
+    # -0 and +0 both decode to 0: compare values
+    assert np.array_equal(oracle.e4m3_decode(got_c), oracle.e4m3_decode(codes))
+
+
+def test_block_quantize_error_bound_and_amax():
+    rng = _rng(52)
+    x = rng.standard_normal((40, 512)) * np.exp(rng.standard_normal((40, 1)) * 3)
+    codes, scales = oracle.e4m3_block_quantize(x, 128)
+    deq = oracle.e4m3_block_dequantize(codes, scales, 128)
+    xb = np.abs(x.astype(np.float32)).reshape(40, 4, 128)
+    # the largest magnitude of every block lands on the largest code
+    big = np.argmax(xb, axis=2)
+    cb = codes.reshape(40, 4, 128)
+    assert ((np.take_along_axis(cb, big[..., None], 2)[..., 0] & 0x7F) == 0x7E).all()
+    # half a unit in the last place of e4m3 (3 mantissa bits), relative to the element's
+    # binade, or half the subnormal step 2^-9, in units of the block's scale
+    q = np.abs(x.astype(np.float32)).reshape(40, 4, 128) / scales[..., None].astype(np.float64)
+    e = np.floor(np.log2(np.maximum(q, 2.0 ** -6)))
+    half_ulp = 0.5 * 2.0 ** (e - 3)
+    err = np.abs(deq - x.astype(np.float32)).reshape(40, 4, 128) / scales[..., None]
+    assert (err <= half_ulp * (1 + 1e-6) + 1e-12).all()
+
+
+def test_block_quantize_blocks_are_independent_and_zero_blocks_stay_zero():
+    rng = _rng(53)
+    x = rng.standard_normal((3, 256))
+    x[1, 128:] = 0.0
+    c0, s0 = oracle.e4m3_block_quantize(x, 128)
+    assert s0[1, 1] == 0 and not c0[1, 128:].any()
+    assert not oracle.e4m3_block_dequantize(c0, s0, 128)[1, 128:].any()
+    y = x.copy()
+    y[0, :128] *= 2.0 ** 5                              # only block (0, 0) changes
+    c1, s1 = oracle.e4m3_block_quantize(y, 128)
+    assert s1[0, 0] == s0[0, 0] * 2.0 ** 5
+    assert np.array_equal(c1, c0)
+    assert np.array_equal(np.delete(s1.ravel(), 0), np.delete(s0.ravel(), 0))
+
+
 def test_cache_image_hand_example():
     # page size 4 for a hand-checkable case: request 0 owns pages [2, 0], request 1 owns [1].
     bt = np.array([[2, 0], [1, -1]], dtype=np.int32)
