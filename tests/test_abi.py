@@ -151,3 +151,32 @@ def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(M, "_lib_handle", None)
     with pytest.raises(RuntimeError, match="not built"):
         M.lib()
+
+
+def test_decode_options_are_validated(lib):
+    fake = ctypes.c_void_p(256)
+    args = lambda c, o: (ctypes.byref(c), fake, fake, fake, fake, 4, fake, 1, fake, 1, 1, fake, fake,  # noqa: E731
+                         fake, 1 << 20, ctypes.byref(o), None)
+    bad_kernel = M.MlaDecodeOpts(num_workers=0, kernel=7)
+    assert lib.mla_decode_ex(*args(_cfg(), bad_kernel)) == M.MLA_ERR_INVALID
+    bad_workers = M.MlaDecodeOpts(num_workers=-1, kernel=0)
+    assert lib.mla_decode_ex(*args(_cfg(), bad_workers)) == M.MLA_ERR_INVALID
+    # the tensor-core kernel asked for on a shape it does not cover
+    tc_on_f32 = M.MlaDecodeOpts(num_workers=0, kernel=M.KERNEL_TC)
+    c32 = M.make_config(W.TINY, "f32", "f32")
+    assert lib.mla_decode_ex(*args(c32, tc_on_f32)) == M.MLA_ERR_UNSUPPORTED
+
+
+def test_unfolded_projection_validates_before_any_launch(lib):
+    c = _cfg()
+    fake = ctypes.c_void_p(256)
+    n = ctypes.c_size_t(0)
+    assert lib.mla_output_proj_unfolded_workspace_size(ctypes.byref(c), 3, ctypes.byref(n)) == M.MLA_OK
+    # an fp32 accumulator [rows][d], a status word and u [rows][H*d_v] (bf16), each 256-aligned
+    assert n.value == 3 * 5120 * 4 + 256 + 3 * 128 * 128 * 2
+    assert lib.mla_output_proj_unfolded(ctypes.byref(c), None, fake, fake, 3, fake, fake, n.value,
+                                        None) == M.MLA_ERR_INVALID
+    assert lib.mla_output_proj_unfolded(ctypes.byref(c), fake, fake, fake, 3, fake, fake, n.value - 1,
+                                        None) == M.MLA_ERR_WORKSPACE
+    assert lib.mla_output_proj_unfolded(ctypes.byref(c), None, None, None, 0, None, None, 0,
+                                        None) == M.MLA_OK
