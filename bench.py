@@ -137,9 +137,10 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- set-up
 
-def setup(wl, dev):
+def setup(wl, dev, workers=0):
     """Seeded workload on the device: weights (folded once), the filled paged cache, the
-    step's inputs. Uses only the library's calls; inputs are generated on the host."""
+    step's inputs. Uses only the library's calls; inputs are generated on the host.
+    workers: decode workers (0: the library's default, one per CTA pair)."""
     import torch
     import mla_latent_kv_04_gb300 as M
 
@@ -185,7 +186,8 @@ def setup(wl, dev):
     out_lat = torch.empty(rows * H * d.d_latent, dtype=act, device=dev)
     lse = torch.empty(rows * H, dtype=torch.float32, device=dev)
     out = torch.empty(rows * d.d_model, dtype=act, device=dev)
-    ws = torch.zeros(M.mla_decode_workspace_size(cfg, B, q), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(M.mla_decode_workspace_size(cfg, B, q, num_workers=workers), dtype=torch.uint8,
+                     device=dev)
     ws_o = torch.zeros(M.mla_output_proj_workspace_size(cfg, rows), dtype=torch.uint8, device=dev)
     ws_u = torch.zeros(M.mla_output_proj_unfolded_workspace_size(cfg, rows), dtype=torch.uint8,
                        device=dev)
@@ -203,7 +205,7 @@ def setup(wl, dev):
             "W_comb": W_comb, "host": host, "dev_in": dev_in,
             "new_req": up(new_req, torch.int32), "new_pos": up(new_pos, torch.int32),
             "out_lat": out_lat, "lse": lse, "out": out, "ws": ws, "ws_o": ws_o, "ws_u": ws_u,
-            "ws_a": ws_a, "query": query,
+            "ws_a": ws_a, "query": query, "workers": workers,
             "status": status}
 
 
@@ -220,7 +222,7 @@ def step(st, inp, ev=None):
         ev["append"][1].record()
         ev["decode"][0].record()
     M.mla_decode(cfg, inp["q_nope"], inp["q_pe"], st["W_UK_abs"], st["cache"], st["bt_d"],
-                 inp["seq_lens"], st["out_lat"], st["lse"], st["ws"],
+                 inp["seq_lens"], st["out_lat"], st["lse"], st["ws"], num_workers=st["workers"],
                  attn_events=ev["attn"] if ev else None)
     if ev:
         ev["decode"][1].record()
@@ -420,6 +422,8 @@ def main():
                     help="seconds of fp64 oracle work for the cpu_baseline field")
     ap.add_argument("--reference-budget", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workers", type=int, default=0,
+                    help="decode workers (0: the library's default, one per CTA pair)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -438,7 +442,7 @@ def main():
     dev = torch.device("cuda", local)
     M.lib()
     wl = W.WORKLOADS[args.workload]
-    st = setup(wl, dev)
+    st = setup(wl, dev, args.workers)
     inp = st["dev_in"]
 
     def barrier():
@@ -508,7 +512,7 @@ def main():
     d0.record()
     for i in range(K):
         M.mla_decode(st["cfg"], inp["q_nope"], inp["q_pe"], st["W_UK_abs"], st["cache"], st["bt_d"],
-                     inp["seq_lens"], st["out_lat"], st["lse"], st["ws"])
+                     inp["seq_lens"], st["out_lat"], st["lse"], st["ws"], num_workers=st["workers"])
     d1.record()
     torch.cuda.synchronize()
     decode_alone_ms = d0.elapsed_time(d1) / K
@@ -598,6 +602,7 @@ def main():
                    "seq_len": wl.seq_lens[0], "q_len": wl.q_len, "heads": wl.dims.num_heads,
                    "cache_dtype": wl.cache, "page_size": wl.dims.page_size,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "decode_workers": args.workers if args.workers > 0 else "library default",
                    "launch": "the step captured once as a CUDA graph and replayed (its kernels, "
                              "memsets and programmatic launch dependencies); ms_per_step_stream "
                              "is the same step issued call by call",
