@@ -388,24 +388,33 @@ def job_throughput(tokens_per_rank_step: int, world: int, ms: float) -> float:
 
 
 def run_reference(args):
-    """The reference arm: the CPU oracle on this host, one request of the workload per step.
+    """The reference arm: the CPU oracle on this host, one request of the workload per step:
+    ``warmup`` untimed requests, then ``steps`` timed ones (fewer only if they would take more
+    than --reference-budget seconds; the line's ``steps`` is the number actually timed).
     Under torchrun only rank 0 works and prints; the other ranks return at once."""
     _, rank, _ = rank_env()
     if rank != 0:
         return
     wl = W.WORKLOADS[args.workload]
-    tps, threads, desc, res = cpu_oracle(wl, 0.0, max_requests=args.steps, warm=args.warmup)
-    ms = res["seconds"] / max(1, res["requests"]) * 1e3
+    tps, threads, desc, res = cpu_oracle(wl, args.reference_budget, max_requests=args.steps,
+                                         warm=args.warmup)
+    timed = int(res["requests"])
+    ms = res["seconds"] / max(1, timed) * 1e3
     line = {"impl": "reference", "metric": METRIC, "value": round(tps, 3), "unit": UNIT,
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "n_gpus": args.gpus, "steps": timed, "warmup": args.warmup,
             "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl.name, "batch": wl.batch, "seq_len": wl.seq_lens[0],
-                       "q_len": wl.q_len, "step_sample": "1 request of the batch per step"},
+                       "q_len": wl.q_len,
+                       "step_sample": "each step is 1 request of the batch (requests taken in "
+                                      "turn), the oracle's whole step for it: append projection, "
+                                      "absorbed decode, folded output projection"},
             "cpu_baseline": {"value": round(tps, 3), "unit": UNIT, "cores": threads,
                              "kind": "oracle", "sample": desc},
             "e2e": {"value": round(tps, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
+    if timed != args.steps:
+        line["steps_requested"] = args.steps
     print(json.dumps(line), flush=True)
 
 
@@ -420,7 +429,8 @@ def main():
     ap.add_argument("--workload", default="v2_b32_s4096", choices=list(W.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of fp64 oracle work for the cpu_baseline field")
-    ap.add_argument("--reference-budget", type=float, default=60.0)
+    ap.add_argument("--reference-budget", type=float, default=180.0,
+                    help="seconds of timed oracle work the reference arm may spend")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workers", type=int, default=0,
                     help="decode workers (0: the library's default, one per CTA pair)")

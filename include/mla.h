@@ -178,11 +178,21 @@ mla_status mla_decode_ex(const mla_config* cfg, const void* q_nope, const void* 
  * (cudaGetSymbolAddress) with that device current: make it outside any stream capture.
  * All calls share the array, so calls whose GPU work overlaps (other streams, unordered
  * host threads) race; order them on one stream. Nothing in the array needs to start at
- * zero. Arguments and results are those of mla_decode. */
+ * zero. Arguments and results are those of mla_decode; the call's device status (its
+ * guards) is read with mla_decode_noalloc_status. */
 mla_status mla_decode_noalloc(const mla_config* cfg, const void* q_nope, const void* q_pe,
                               const void* W_UK_abs, const void* cache, int num_pages,
                               const int32_t* block_table, int max_pages, const int32_t* seq_lens,
                               int batch, int q_len, void* out_latent, float* lse, void* stream);
+
+/* The device status of the last mla_decode_noalloc on the current device: waits for
+ * `stream`, then reads the status word at the start of the library's scratch array into
+ * *code (MLA_OK, or MLA_ERR_DEVICE_GUARD when that call's guards skipped a request) and
+ * resets it to 0. The pages have no counterpart to this call. The array's address is looked
+ * up once per device and kept: neither call may be used on a device after a
+ * cudaDeviceReset of it in the same process. Errors: MLA_ERR_INVALID (code is NULL),
+ * MLA_ERR_CUDA. */
+mla_status mla_decode_noalloc_status(void* stream, int* code);
 
 /* Bytes of workspace mla_output_proj needs for `rows` rows (may be 0). */
 mla_status mla_output_proj_workspace_size(const mla_config* cfg, int rows, size_t* bytes);

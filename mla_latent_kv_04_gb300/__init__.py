@@ -72,6 +72,7 @@ _SIGNATURES = {
     "mla_decode_ex": (_I, [_CFG, _P, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P, _P, _P, _SZ,
                            ctypes.POINTER(MlaDecodeOpts), _P]),
     "mla_decode_noalloc": (_I, [_CFG, _P, _P, _P, _P, _I, _P, _I, _P, _I, _I, _P, _P, _P]),
+    "mla_decode_noalloc_status": (_I, [_P, ctypes.POINTER(_I)]),
     "mla_output_proj_workspace_size": (_I, [_CFG, _I, ctypes.POINTER(_SZ)]),
     "mla_output_proj": (_I, [_CFG, _P, _P, _I, _P, _P, _SZ, _P]),
     "mla_output_proj_unfolded_workspace_size": (_I, [_CFG, _I, ctypes.POINTER(_SZ)]),
@@ -301,6 +302,15 @@ def mla_decode_noalloc(cfg, q_nope, q_pe, W_UK_abs, cache, block_table, seq_lens
         _ptr(seq_lens, "seq_lens", _i32(0), batch), batch, q_len,
         _ptr(out_latent, "out_latent", a, batch * q_len * H * d_c),
         _ptr(lse, "lse", (t.float32,), batch * q_len * H), _stream(stream)), "mla_decode_noalloc")
+
+
+def mla_decode_noalloc_status(stream=None) -> int:
+    """Synchronises the stream and returns (then clears) the device status of the last
+    mla_decode_noalloc on the current device."""
+    code = ctypes.c_int(0)
+    _check(lib().mla_decode_noalloc_status(_stream(stream), ctypes.byref(code)),
+           "mla_decode_noalloc_status")
+    return int(code.value)
 
 
 def mla_output_proj_workspace_size(cfg, rows) -> int:

@@ -10,11 +10,17 @@
 //
 // The array is set up once per device: the first call on a device, with that device
 // current, looks up the array's device address with cudaGetSymbolAddress. Make that first
-// call outside any stream capture. The array lives as long as the library is loaded, on
-// every GPU that loads it, and every call shares it: two calls whose work overlaps on the
-// GPU (different streams, or different host threads without ordering) race on it. The
-// decode needs no zeroed scratch (each call clears the status word it uses), so the
-// contents left by the previous call are harmless.
+// call outside any stream capture. The address is kept for the life of the process, so the
+// library must not outlive a cudaDeviceReset of a device it has decoded on (the reset
+// unloads the module that holds the array). The array lives as long as the library is
+// loaded, on every GPU that loads it, and every call shares it: two calls whose work
+// overlaps on the GPU (different streams, or different host threads without ordering) race
+// on it. The decode needs no zeroed scratch (each call clears the status word it uses), so
+// the contents left by the previous call are harmless.
+//
+// The decode's device guards (a block-table entry outside the cache, a seq_len above the
+// block-table row) report through a status word at the start of the array, which the caller
+// cannot address; mla_decode_noalloc_status reads and clears it.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -77,4 +83,16 @@ extern "C" mla_status mla_decode_noalloc(const mla_config* cfg, const void* q_no
   if (st != MLA_OK) return st;
   return mla_decode(cfg, q_nope, q_pe, W_UK_abs, cache, num_pages, block_table, max_pages,
                     seq_lens, batch, q_len, out_latent, lse, scratch, kScratchBytes, stream);
+}
+
+extern "C" mla_status mla_decode_noalloc_status(void* stream, int* code) {
+  if (!code) {
+    mla::set_last_error("mla_decode_noalloc_status: code is NULL");
+    return MLA_ERR_INVALID;
+  }
+  void* scratch = nullptr;
+  const mla_status st = scratch_of_current_device(&scratch);
+  if (st != MLA_OK) return st;
+  // the decode's status word is the first int32 of its workspace, here the array
+  return mla_read_device_status(scratch, stream, code);
 }

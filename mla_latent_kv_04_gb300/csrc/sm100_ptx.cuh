@@ -1,6 +1,6 @@
 // Inline-PTX wrappers for the sm_100-family features the tensor-core decode kernel uses:
 // mbarriers (with bounded waits), TMA tensor loads, thread-block-cluster primitives,
-// asynchronous remote stores, and the tcgen05 tensor-memory / MMA instructions.
+// bulk copies between CTAs, and the tcgen05 tensor-memory / MMA instructions.
 #pragma once
 #include <cuda.h>
 #include <stdint.h>
@@ -26,11 +26,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
 }
-// Arrive on an mbarrier of another CTA of the cluster (address from mapa).
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
-               : "memory");
-}
 // Relaxed arrive on another CTA's mbarrier. `dep` must be computed from every value whose
 // read has to complete first: the instruction reads it, so in-order issue cannot send the
 // arrive before those reads returned.
@@ -47,27 +42,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-  return ok != 0;
-}
-// The same, with the thread suspended for up to `hint_ns` (it resumes as soon as the phase
-// completes): a waiting warp then takes no issue slots from the warps doing the work.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_try_wait_cluster_sleep(uint32_t bar, uint32_t parity,
-                                                            uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
   return ok != 0;
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
@@ -95,15 +69,6 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local_addr, uint32_t ra
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
   return r;
 }
-// 16-byte asynchronous store into another CTA's shared memory; completion is counted in
-// bytes on that CTA's mbarrier.
-__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, float a, float b, float c, float d,
-                                            uint32_t remote_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
-      ::"r"(remote_addr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar) : "memory");
-}
-
 // Bulk copy (TMA engine) from this CTA's shared memory into another CTA's; the bytes are
 // counted on that CTA's mbarrier. Both addresses 16-byte aligned, size a multiple of 16.
 __device__ __forceinline__ void bulk_s2s(uint32_t remote_dst, uint32_t local_src, uint32_t bytes,
@@ -125,13 +90,6 @@ __device__ __forceinline__ void bulk_wait_read_le1() {
 }
 
 // ---- TMA ------------------------------------------------------------------------------
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar) : "memory");
-}
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
                                             uint32_t bar) {
   asm volatile(
@@ -269,25 +227,12 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                ::"r"(bar) : "memory");
 }
 
-// Arrive (once) on the mbarrier at the same shared-memory offset in every CTA of the cluster
-// named by cta_mask, when every previously issued tcgen05 op of this thread is done.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
-      ::"r"(bar), "h"(cta_mask) : "memory");
-}
-
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, dense.
 //   bits [4,6) D format (1 = f32); [7,10) A format (1 = bf16); [10,13) B format (1 = bf16);
 //   bit 15 A major (0 = K-major, 1 = MN-major); bit 16 B major; [17,23) N >> 3; [24,29) M >> 4.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-// Same with fp16 A and B (format code 0 in both fields), both K-major.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
-  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor (sm_100 form):
@@ -346,13 +291,6 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 __device__ __forceinline__ void griddep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-
-// max of three floats in one instruction (sm_100 three-input max.f32)
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float y;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
-  return y;
 }
 
 __device__ __forceinline__ uint64_t globaltimer() {
