@@ -345,7 +345,7 @@ __device__ void send_warps(const Shared& sh, const DecodeParams& p, uint32_t tme
   const int row = 32 * quarter + lane;
   const uint32_t t_row = tmem + ((uint32_t)(32 * quarter) << 16);
   const uint32_t peer = (uint32_t)(rank ^ 1);
-  const uint32_t peer_x_warp = ptx::map_to_rank(sh.xbuf(0), peer) + quarter * 4096;
+  const uint32_t peer_x = ptx::map_to_rank(sh.xbuf(0), peer);
   const uint32_t peer_xfull0 = ptx::map_to_rank(sh.bar(B_XFULL0), peer);
   const int sw = row & 7;                                // 16-byte chunk swizzle of 128-byte rows
   PageCursor cur;
@@ -372,10 +372,11 @@ __device__ void send_warps(const Shared& sh, const DecodeParams& p, uint32_t tme
     int ok = 1;
     if (lane == 0) {
       ptx::mbar_arrive(sh.bar(B_SFREE));
-      // staging buffer j: our softmax has read page n - kXB from it and that page's copy
-      // has read it too
-      ok = wait_bar(sh, sh.bar(B_STGFREE0 + j), xpar ^ 1, p.status) ? 1 : 0;
-      if (kXB == 1) ptx::bulk_wait_read_all(); else ptx::bulk_wait_read_le1();
+      // staging buffer j: our softmax has read page n - kXB from it, and the peer has read
+      // its receive buffer j (so the copy of page n - kXB out of staging j has landed)
+      ok = wait_bar(sh, sh.bar(B_STGFREE0 + j), xpar ^ 1, p.status) &&
+                   wait_bar(sh, sh.bar(B_XEMPTY0 + j), xpar ^ 1, p.status, true)
+               ? 1 : 0;
     }
     if (!__shfl_sync(0xffffffffu, ok, 0)) return;
     // columns past the last token (rows that may hold anything) go out as 0, and finite
@@ -399,11 +400,14 @@ __device__ void send_warps(const Shared& sh, const DecodeParams& p, uint32_t tme
     __syncwarp();
     if (lane == 0) {
       ptx::mbar_arrive(sh.bar(B_STGREADY0 + j));
-      ok = wait_bar(sh, sh.bar(B_XEMPTY0 + j), xpar ^ 1, p.status, true) ? 1 : 0;
-      if (ok) {
-        ptx::bulk_s2s(peer_x_warp + j * kXBytes, sh.stg(j) + quarter * 4096, 4096,
-                      peer_xfull0 + 8 * j);
-        ptx::bulk_commit();
+      // one 16 KB copy per page once all four quarters are staged: a bulk copy between
+      // CTAs costs about the same fixed time whatever its size up to 16 KB
+      if (quarter == 0) {
+        ok = wait_bar(sh, sh.bar(B_STGREADY0 + j), xpar, p.status) ? 1 : 0;
+        if (ok) {
+          ptx::bulk_s2s(peer_x + j * kXBytes, sh.stg(j), kXBytes, peer_xfull0 + 8 * j);
+          ptx::bulk_commit();
+        }
       }
     }
     if (!__shfl_sync(0xffffffffu, ok, 0)) return;
