@@ -156,8 +156,10 @@ def setup(wl, dev, workers=0):
     wts = W.weights(wl)
     dw = {k: up(v) for k, v in wts.items()}
     bt, num_pages = W.page_table(wl)
-    cdt = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8}[wl.cache]
-    cache = torch.zeros(num_pages * d.page_size * D, dtype=cdt, device=dev)
+    cdt = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8_e4m3": torch.uint8,
+           "fp8_e4m3_b128": torch.uint8}[wl.cache]
+    row = W.cache_row_bytes(wl) // torch.tensor([], dtype=cdt).element_size()
+    cache = torch.zeros(num_pages * d.page_size * row, dtype=cdt, device=dev)
     bt_d = up(bt, torch.int32)
     status = torch.zeros(4, dtype=torch.int32, device=dev)
     for b in range(wl.batch):
@@ -250,7 +252,7 @@ def kernel_work(wl):
         "oproj": {"bytes": K * d.d_model * ea + rows * K * ea + rows * d.d_model * ea,
                   "flops": 2.0 * rows * K * d.d_model},
         "append": {"bytes": rows * d.d_model * ea + d.d_model * d.d_cache * ea
-                   + rows * d.d_cache * W.elt_bytes(wl.cache),
+                   + rows * W.cache_row_bytes(wl),
                    "flops": 2.0 * rows * d.d_model * d.d_cache},
         # the step's queries from h: W_DQ, W_UQ, W_QR, h in, q_nope and q_pe out (c_q, an
         # intermediate, is not counted)
@@ -601,7 +603,7 @@ def main():
     roof = dict(rl[dom])
     roof["kernel"] = names[dom]
     roof["traffic"] = ncu_traffic(dom, wl.name)
-    cache_mb = wl.total_tokens * wl.dims.d_cache * W.elt_bytes(wl.cache) / 1e6
+    cache_mb = wl.total_tokens * W.cache_row_bytes(wl) / 1e6
     wcomb_mb = wl.dims.num_heads * wl.dims.d_latent * wl.dims.d_model * W.elt_bytes(wl.act) / 1e6
     roof["peak_source"] = peaks["source"] + (" (sustained bf16)" if roof["bound"] == "tensor" else "")
     line = {

@@ -36,10 +36,19 @@
  *     status word, which mla_read_device_status returns.
  *
  * Dtypes: act_dtype (activations, weights, queries, outputs) is MLA_F32 or
- * MLA_BF16; cache_dtype is MLA_F32 (only with MLA_F32 activations), MLA_BF16 or
- * MLA_FP8_E4M3 (only with MLA_BF16 activations). bf16 and fp8 values are
- * rounded to nearest-even; fp8 saturates to +-448 and is dequantised as
- * code * cache_scale (one per-tensor scale).
+ * MLA_BF16; cache_dtype is MLA_F32 (only with MLA_F32 activations), MLA_BF16,
+ * MLA_FP8_E4M3 or MLA_FP8_E4M3_B128 (the last two only with MLA_BF16 activations).
+ * bf16 and fp8 values are rounded to nearest-even; fp8 saturates to +-448.
+ *   - MLA_FP8_E4M3: c_kv and k_pe as e4m3 codes, dequantised as code * cache_scale
+ *     (one per-tensor scale).
+ *   - MLA_FP8_E4M3_B128: the fp8 cache huny.dev §6 describes for DeepSeek-V3. c_kv is in
+ *     e4m3 with one fp32 scale per 128 consecutive latent elements of each token, computed
+ *     from the values when the token is written: scale = amax|x| / 448 and
+ *     code = e4m3(x / scale), both divisions in IEEE fp32; a block of zeros has scale 0 and
+ *     codes 0. The rotated k_pe stays in bf16. A cache row holds d_c code bytes, then d_c/128
+ *     fp32 scales, then d_r bf16 values: d_c + d_c/32 + 2 d_r bytes (656 at DeepSeek-V2
+ *     shapes; mla_cache_row_bytes). d_c must be a multiple of 128, and cache_scale is
+ *     ignored.
  */
 #ifndef MLA_H_
 #define MLA_H_
@@ -61,7 +70,7 @@ typedef enum {
   MLA_ERR_TIMEOUT = 6       /* a bounded device-side wait gave up; the work was skipped */
 } mla_status;
 
-typedef enum { MLA_F32 = 0, MLA_BF16 = 1, MLA_FP8_E4M3 = 2 } mla_dtype;
+typedef enum { MLA_F32 = 0, MLA_BF16 = 1, MLA_FP8_E4M3 = 2, MLA_FP8_E4M3_B128 = 3 } mla_dtype;
 
 /* Model dimensions and numeric options of one MLA layer.
  *   num_heads H, d_model d, d_latent d_c (c_kv width), d_rope d_r (k_pe width),
@@ -97,7 +106,8 @@ mla_status mla_absorb_weights(const mla_config* cfg, const void* W_UK, const voi
  *   h [T][d], W_DKV_KR [d][d_c + d_r] = [W^DKV | W^KR]   (act dtype)
  *   req_ids [T], positions [T]          int32 (device)
  *   block_table [batch][max_pages]      int32 (device)
- *   cache [num_pages][P][d_c + d_r]     cache dtype, updated in place
+ *   cache [num_pages][P][d_c + d_r]     cache dtype, updated in place (MLA_FP8_E4M3_B128:
+ *                                       bytes, [num_pages][P][mla_cache_row_bytes])
  *   dev_status                          optional int32 device word (may be NULL):
  *                                       MLA_ERR_DEVICE_GUARD is OR-ed in for skipped rows.
  *   workspace                           device buffer of mla_append_cache_workspace_size
@@ -109,6 +119,10 @@ mla_status mla_append_cache(const mla_config* cfg, const void* h, const void* W_
                             const int32_t* block_table, int batch, int max_pages, void* cache,
                             int num_pages, int32_t* dev_status, void* workspace,
                             size_t workspace_bytes, void* stream);
+
+/* Bytes of one token's row in the paged cache: (d_c + d_r) * element size, or
+ * d_c + d_c/32 + 2 d_r for MLA_FP8_E4M3_B128. A page is P rows. */
+mla_status mla_cache_row_bytes(const mla_config* cfg, size_t* bytes);
 
 /* Bytes of workspace mla_append_cache needs for T rows (0 for fp32 activations). */
 mla_status mla_append_cache_workspace_size(const mla_config* cfg, int T, size_t* bytes);

@@ -25,12 +25,14 @@ MLA_ERR_TIMEOUT = 6
 MLA_F32 = 0
 MLA_BF16 = 1
 MLA_FP8_E4M3 = 2
+MLA_FP8_E4M3_B128 = 3
 
 KERNEL_AUTO = 0
 KERNEL_SIMT = 1
 KERNEL_TC = 2
 
-_DTYPE_CODES = {"f32": MLA_F32, "bf16": MLA_BF16, "fp8_e4m3": MLA_FP8_E4M3}
+_DTYPE_CODES = {"f32": MLA_F32, "bf16": MLA_BF16, "fp8_e4m3": MLA_FP8_E4M3,
+                "fp8_e4m3_b128": MLA_FP8_E4M3_B128}
 
 
 class MlaError(RuntimeError):
@@ -77,6 +79,7 @@ _SIGNATURES = {
     "mla_output_proj": (_I, [_CFG, _P, _P, _I, _P, _P, _SZ, _P]),
     "mla_output_proj_unfolded_workspace_size": (_I, [_CFG, _I, ctypes.POINTER(_SZ)]),
     "mla_output_proj_unfolded": (_I, [_CFG, _P, _P, _P, _I, _P, _P, _SZ, _P]),
+    "mla_cache_row_bytes": (_I, [_CFG, ctypes.POINTER(_SZ)]),
     "mla_query_workspace_size": (_I, [_CFG, _I, _I, ctypes.POINTER(_SZ)]),
     "mla_query_from_hidden": (_I, [_CFG, _I, _P, _P, _P, _P, _I, _P, _P, _P, _SZ, _P]),
     "mla_read_device_status": (_I, [_P, _P, ctypes.POINTER(_I)]),
@@ -156,6 +159,14 @@ def _cache_dtypes(cfg):
     return (t.uint8, t.float8_e4m3fn)
 
 
+def _cache_row_elems(cfg):
+    """Elements of the cache tensor per token row: d_c + d_r, or the row's bytes for the
+    block-scaled fp8 cache (a uint8 tensor)."""
+    if cfg.cache_dtype == MLA_FP8_E4M3_B128:
+        return cfg.d_latent + cfg.d_latent // 32 + 2 * cfg.d_rope
+    return cfg.d_latent + cfg.d_rope
+
+
 def _ptr(x, name, dtypes=None, numel=None, allow_none=False):
     if x is None:
         if allow_none:
@@ -221,12 +232,12 @@ def mla_append_cache(cfg, h, W_DKV_KR, req_ids, positions, block_table, cache, d
     T = req_ids.numel()
     D = cfg.d_latent + cfg.d_rope
     batch, max_pages = block_table.shape
-    num_pages = cache.numel() // (cfg.page_size * D)
+    num_pages = cache.numel() // (cfg.page_size * _cache_row_elems(cfg))
     _check(lib().mla_append_cache(
         ctypes.byref(cfg), _ptr(h, "h", a, T * cfg.d_model), _ptr(W_DKV_KR, "W_DKV_KR", a, cfg.d_model * D),
         T, _ptr(req_ids, "req_ids", _i32(0), T), _ptr(positions, "positions", _i32(0), T),
         _ptr(block_table, "block_table", _i32(0)), batch, max_pages,
-        _ptr(cache, "cache", _cache_dtypes(cfg), num_pages * cfg.page_size * D), num_pages,
+        _ptr(cache, "cache", _cache_dtypes(cfg), num_pages * cfg.page_size * _cache_row_elems(cfg)), num_pages,
         _ptr(dev_status, "dev_status", _i32(0), allow_none=True),
         _ptr(workspace, "workspace", (_torch().uint8,), allow_none=True),
         0 if workspace is None else workspace.numel(), _stream(stream)),
@@ -239,12 +250,12 @@ def mla_append_cache_latent(cfg, c_kv, k_pe, req_ids, positions, block_table, ca
     T = req_ids.numel()
     D = cfg.d_latent + cfg.d_rope
     batch, max_pages = block_table.shape
-    num_pages = cache.numel() // (cfg.page_size * D)
+    num_pages = cache.numel() // (cfg.page_size * _cache_row_elems(cfg))
     _check(lib().mla_append_cache_latent(
         ctypes.byref(cfg), _ptr(c_kv, "c_kv", a, T * cfg.d_latent), _ptr(k_pe, "k_pe", a, T * cfg.d_rope),
         T, _ptr(req_ids, "req_ids", _i32(0), T), _ptr(positions, "positions", _i32(0), T),
         _ptr(block_table, "block_table", _i32(0)), batch, max_pages,
-        _ptr(cache, "cache", _cache_dtypes(cfg), num_pages * cfg.page_size * D), num_pages,
+        _ptr(cache, "cache", _cache_dtypes(cfg), num_pages * cfg.page_size * _cache_row_elems(cfg)), num_pages,
         1 if rotate else 0, _ptr(dev_status, "dev_status", _i32(0), allow_none=True),
         _stream(stream)), "mla_append_cache_latent")
 
@@ -265,14 +276,14 @@ def mla_decode(cfg, q_nope, q_pe, W_UK_abs, cache, block_table, seq_lens, out_la
     batch, q_len = q_nope.shape[0], q_nope.shape[1]
     H, d_c, d_r, d_n = cfg.num_heads, cfg.d_latent, cfg.d_rope, cfg.d_nope
     D = d_c + d_r
-    num_pages = cache.numel() // (cfg.page_size * D)
+    num_pages = cache.numel() // (cfg.page_size * _cache_row_elems(cfg))
     max_pages = block_table.shape[1]
     o = _opts(num_workers, kernel, attn_events)
     _check(lib().mla_decode_ex(
         ctypes.byref(cfg), _ptr(q_nope, "q_nope", a, batch * q_len * H * d_n),
         _ptr(q_pe, "q_pe", a, batch * q_len * H * d_r),
         _ptr(W_UK_abs, "W_UK_abs", a, H * d_n * d_c),
-        _ptr(cache, "cache", _cache_dtypes(cfg), num_pages * cfg.page_size * D), num_pages,
+        _ptr(cache, "cache", _cache_dtypes(cfg), num_pages * cfg.page_size * _cache_row_elems(cfg)), num_pages,
         _ptr(block_table, "block_table", _i32(0), batch * max_pages), max_pages,
         _ptr(seq_lens, "seq_lens", _i32(0), batch), batch, q_len,
         _ptr(out_latent, "out_latent", a, batch * q_len * H * d_c),
@@ -291,13 +302,13 @@ def mla_decode_noalloc(cfg, q_nope, q_pe, W_UK_abs, cache, block_table, seq_lens
     batch, q_len = q_nope.shape[0], q_nope.shape[1]
     H, d_c, d_r, d_n = cfg.num_heads, cfg.d_latent, cfg.d_rope, cfg.d_nope
     D = d_c + d_r
-    num_pages = cache.numel() // (cfg.page_size * D)
+    num_pages = cache.numel() // (cfg.page_size * _cache_row_elems(cfg))
     max_pages = block_table.shape[1]
     _check(lib().mla_decode_noalloc(
         ctypes.byref(cfg), _ptr(q_nope, "q_nope", a, batch * q_len * H * d_n),
         _ptr(q_pe, "q_pe", a, batch * q_len * H * d_r),
         _ptr(W_UK_abs, "W_UK_abs", a, H * d_n * d_c),
-        _ptr(cache, "cache", _cache_dtypes(cfg), num_pages * cfg.page_size * D), num_pages,
+        _ptr(cache, "cache", _cache_dtypes(cfg), num_pages * cfg.page_size * _cache_row_elems(cfg)), num_pages,
         _ptr(block_table, "block_table", _i32(0), batch * max_pages), max_pages,
         _ptr(seq_lens, "seq_lens", _i32(0), batch), batch, q_len,
         _ptr(out_latent, "out_latent", a, batch * q_len * H * d_c),
@@ -350,6 +361,12 @@ def mla_output_proj_unfolded(cfg, out_latent, W_UV, W_O, out, workspace, stream=
         _ptr(out, "out", a, rows * cfg.d_model),
         _ptr(workspace, "workspace", (_torch().uint8,)), workspace.numel(), _stream(stream)),
         "mla_output_proj_unfolded")
+
+
+def mla_cache_row_bytes(cfg) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().mla_cache_row_bytes(ctypes.byref(cfg), ctypes.byref(n)), "mla_cache_row_bytes")
+    return int(n.value)
 
 
 def mla_query_workspace_size(cfg, d_q, T) -> int:

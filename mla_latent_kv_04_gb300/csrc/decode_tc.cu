@@ -61,6 +61,13 @@ constexpr int kKTileC = 64 * 64 * 2;                     // one 64-dim SW128 chu
 constexpr int kKTilePE = 64 * 32 * 2;                    // the 32-dim SW64 k_pe half
 constexpr int kStageBytes = 4 * kKTileC + kKTilePE;      // 36864
 constexpr int kXBytes = 128 * 64 * 2;                    // one fp16 partial-score buffer
+// Block-scaled fp8 cache rows: [512 e4m3 codes][4 fp32 scales][64 bf16 k_pe] = 656 bytes.
+// A stage receives this CTA's 256 codes (16 KB, unswizzled, over the back half of the
+// latent tiles), the row's 4 scales (1 KB, just below them) and its 32 k_pe values straight
+// into the SW64 rope tile.
+constexpr int kB128RowBytes = kDC + kDC / 32 + 2 * kDR;    // 656
+constexpr int kB128Codes = 16384;                          // stage offset of the codes
+constexpr int kB128Scales = kB128Codes - 64 * 16;          // stage offset of the scales
 constexpr int kQPeBytes = 128 * 32 * 2;                  // Q_r k_pe part, SW64 [128][32]
 constexpr int kOffStage = 0;
 constexpr int kOffX = kOffStage + kNS * kStageBytes;     // receive buffers (the peer's partial)
@@ -165,11 +172,11 @@ struct PageCursor {
 // load, issued when a stage frees up, reads L2 rather than HBM.
 // An fp8 cache lands as e4m3 bytes (18 KB, unswizzled) in the back half of the stage, for
 // the converter warps to expand into the bf16 layout the MMAs read.
-template <bool kFp8>
+template <bool kFp8, bool kB128>
 __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensorMap* tm_kc,
-                         const CUtensorMap* tm_kpe, const CUtensorMap* tm_qpe, int worker,
-                         int rank) {
-  constexpr int kElt = kFp8 ? 1 : 2;                     // cache bytes per element
+                         const CUtensorMap* tm_kpe, const CUtensorMap* tm_qpe,
+                         const CUtensorMap* tm_sc, int worker, int rank) {
+  constexpr int kRowBytes = kB128 ? kB128RowBytes : kD * (kFp8 ? 1 : 2);   // cache bytes per row
   const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
   const uint8_t* cache = reinterpret_cast<const uint8_t*>(p.cache);
   // the cache is read once: its lines go first out of L2, so that what this decode reads
@@ -181,7 +188,7 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
     if (rank != 0 || !ahead.valid()) return;
     const int page = p.block_table[(long long)(ahead.item.group / p.q_len) * p.max_pages + ahead.pg];
     if (page >= 0 && page < p.num_pages)
-      ptx::bulk_prefetch_l2_hint(cache + (long long)page * (kP * kD * kElt), kP * kD * kElt, pol);
+      ptx::bulk_prefetch_l2_hint(cache + (long long)page * (kP * kRowBytes), kP * kRowBytes, pol);
     ahead.next();
   };
   for (int i = 0; i < kL2Ahead; ++i) ahead.next();      // pages 0..kL2Ahead-1 load directly
@@ -211,7 +218,15 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
       }
       if (!wait_bar(sh, sh.bar(B_EMPTY0 + stage), (wrap & 1) ^ 1, p.status)) return;
       const uint32_t full = sh.bar(B_FULL0 + stage);
-      if constexpr (kFp8) {
+      if constexpr (kB128) {
+        const uint32_t st = sh.stage(stage);
+        ptx::mbar_arrive_expect_tx(full, 16384 + 64 * 16 + kKTilePE);
+        ptx::tma_load_2d_hint(st + kB128Codes, tm_kc, 256 * rank, page * kP, full, pol);
+        ptx::tma_load_2d_hint(st + kB128Codes + 8192, tm_kc, 256 * rank + 128, page * kP, full, pol);
+        ptx::tma_load_2d_hint(st + kB128Scales, tm_sc, kDC, page * kP, full, pol);
+        ptx::tma_load_2d_hint(st + 4 * kKTileC, tm_kpe, kDC + kDC / 32 + 64 * rank, page * kP, full,
+                              pol);
+      } else if constexpr (kFp8) {
         const uint32_t land = sh.stage(stage) + kStageBytes / 2;
         ptx::mbar_arrive_expect_tx(full, kStageBytes / 2);
         ptx::tma_load_2d_hint(land, tm_kc, 256 * rank, page * kP, full, pol);
@@ -680,6 +695,23 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t v16) {
   return out;
 }
 
+// Two e4m3 codes (low byte first) times a block scale -> two bf16, rounded to nearest
+// even: the codes convert exactly to fp16 and then fp32, and only the product is rounded.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint32_t v16, float s) {
+  uint32_t h2;
+  asm("{\n\t.reg .b16 x;\n\tcvt.u16.u32 x, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, x;\n\t}" : "=r"(h2) : "r"(v16));
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * s, f.y * s);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+__device__ __forceinline__ void e4m3x16_to_bf16_scaled(const uint4& in, float s, uint4& lo, uint4& hi) {
+  lo = make_uint4(e4m3x2_to_bf16x2_scaled(in.x & 0xFFFFu, s), e4m3x2_to_bf16x2_scaled(in.x >> 16, s),
+                  e4m3x2_to_bf16x2_scaled(in.y & 0xFFFFu, s), e4m3x2_to_bf16x2_scaled(in.y >> 16, s));
+  hi = make_uint4(e4m3x2_to_bf16x2_scaled(in.z & 0xFFFFu, s), e4m3x2_to_bf16x2_scaled(in.z >> 16, s),
+                  e4m3x2_to_bf16x2_scaled(in.w & 0xFFFFu, s), e4m3x2_to_bf16x2_scaled(in.w >> 16, s));
+}
+
 // 16 e4m3 bytes -> 16 bf16 as two 16-byte vectors (elements in order).
 __device__ __forceinline__ void e4m3x16_to_bf16(const uint4& in, uint4& lo, uint4& hi) {
   lo = make_uint4(e4m3x2_to_bf16x2(in.x & 0xFFFFu), e4m3x2_to_bf16x2(in.x >> 16),
@@ -695,7 +727,12 @@ __device__ __forceinline__ void e4m3x16_to_bf16(const uint4& in, uint4& lo, uint
 // The bf16 writes overlap the e4m3 bytes, so every converter reads its share first and the
 // four warps meet at a barrier before any writes. Thread t reads eight 16-byte units of the
 // c boxes (a warp covers 4 rows x 128 bytes, conflict-free) and one of the rope box.
-__device__ void convert_warps(const Shared& sh, const DecodeParams& p, int worker, int warp, int lane) {
+// Block-scaled cache (kB128): the 256 codes of each row are read with the row's two scales
+// of this CTA's dims (blocks 2 rank, 2 rank + 1), converted as code * scale rounded to bf16,
+// and written like the per-tensor codes; k_pe arrived in bf16 and is not touched.
+template <bool kB128>
+__device__ void convert_warps(const Shared& sh, const DecodeParams& p, int worker, int rank, int warp,
+                              int lane) {
   const int t = 32 * (warp - kWarpConv0) + lane;         // 0..127
   PageCursor cur;
   cur.init(p, p.worker_off[worker], p.worker_off[worker + 1]);
@@ -704,18 +741,26 @@ __device__ void convert_warps(const Shared& sh, const DecodeParams& p, int worke
   while (cur.valid()) {
     if (!wait_bar(sh, sh.bar(B_FULL0 + stage), wrap & 1, p.status)) return;
     uint8_t* st = sh.base + kOffStage + stage * kStageBytes;
-    const uint8_t* land = st + kStageBytes / 2;
+    const uint8_t* land = st + (kB128 ? kB128Codes : kStageBytes / 2);
     uint4 in[9];
+    float scl[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int i = t + 128 * k, j = i >> 9, r = (i >> 3) & 63, u = i & 7;
       in[k] = *reinterpret_cast<const uint4*>(land + 8192 * j + 128 * r + 16 * u);
+      if constexpr (kB128)
+        scl[k] = reinterpret_cast<const float*>(st + kB128Scales)[4 * r + 2 * rank + j];
     }
-    in[8] = *reinterpret_cast<const uint4*>(land + 16384 + 32 * (t >> 1) + 16 * (t & 1));
+    if constexpr (kB128) in[8] = in[0];
+    else in[8] = *reinterpret_cast<const uint4*>(land + 16384 + 32 * (t >> 1) + 16 * (t & 1));
     // every lane's reads have returned (their values are used) before the warp reports
     uint32_t dep = 0;
 #pragma unroll
     for (int k = 0; k < 9; ++k) dep ^= in[k].x;
+    if constexpr (kB128) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) dep ^= __float_as_uint(scl[k]);
+    }
     const uint32_t all = __ballot_sync(0xffffffffu, dep != 0x7fc00001u);
     if (lane == 0 && all != 0x12345678u) ptx::mbar_arrive(sh.bar(B_CVREAD));
     if (!wait_bar(sh, sh.bar(B_CVREAD), n & 1, p.status)) return;
@@ -726,11 +771,12 @@ __device__ void convert_warps(const Shared& sh, const DecodeParams& p, int worke
       uint8_t* row = st + (2 * j + (u >> 2)) * kKTileC + 128 * r;
       const int cb = 2 * (u & 3);
       uint4 lo, hi;
-      e4m3x16_to_bf16(in[k], lo, hi);
+      if constexpr (kB128) e4m3x16_to_bf16_scaled(in[k], scl[k], lo, hi);
+      else e4m3x16_to_bf16(in[k], lo, hi);
       *reinterpret_cast<uint4*>(row + ((cb ^ (r & 7)) * 16)) = lo;
       *reinterpret_cast<uint4*>(row + (((cb + 1) ^ (r & 7)) * 16)) = hi;
     }
-    {
+    if constexpr (!kB128) {
       // rope dims 16 u .. +15 of row r -> 16-byte units 2 u, +1 of the 64-byte SW64 row
       // (64-byte swizzle: unit ^= (row >> 1) & 3)
       const int r = t >> 1, cb = 2 * (t & 1);
@@ -752,11 +798,12 @@ __device__ void convert_warps(const Shared& sh, const DecodeParams& p, int worke
   }
 }
 
-template <bool kFp8>
+template <bool kFp8, bool kB128>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 : kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kc,
                      const __grid_constant__ CUtensorMap tm_kpe,
-                     const __grid_constant__ CUtensorMap tm_qpe, const DecodeParams p) {
+                     const __grid_constant__ CUtensorMap tm_qpe,
+                     const __grid_constant__ CUtensorMap tm_sc, const DecodeParams p) {
   extern __shared__ uint8_t smem_raw[];
   Shared sh;
   const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -805,6 +852,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
     ptx::prefetch_tensormap(&tm_kc);
     ptx::prefetch_tensormap(&tm_kpe);
     ptx::prefetch_tensormap(&tm_qpe);
+    if (kB128) ptx::prefetch_tensormap(&tm_sc);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(sh.tmem_slot), kTmemCols);
@@ -821,11 +869,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
   ptx::griddep_wait();
 
   if (warp == 0) {
-    if (lane == 0) producer<kFp8>(sh, p, &tm_kc, &tm_kpe, &tm_qpe, worker, rank);
+    if (lane == 0) producer<kFp8, kB128>(sh, p, &tm_kc, &tm_kpe, &tm_qpe, &tm_sc, worker, rank);
   } else if (warp == 1) {
     if (lane == 0) qk_issuer<kFp8>(sh, p, tmem, worker);
   } else if (kFp8 && warp >= kWarpConv0) {
-    convert_warps(sh, p, worker, warp, lane);
+    convert_warps<kB128>(sh, p, worker, rank, warp, lane);
   } else if (warp <= 5) {
     send_warps(sh, p, tmem, worker, rank, warp, lane);
   } else if (warp <= 13) {
@@ -901,6 +949,21 @@ bool make_map_u8(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_c
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over a block-scaled fp8 cache viewed as bytes [rows][656]; box = box_cols x
+// box_rows bytes, with the given swizzle.
+bool make_map_b128(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_cols, uint32_t box_rows,
+                   CUtensorMapSwizzle swz) {
+  auto enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kB128RowBytes, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kB128RowBytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D map over the rotated query parts of the planar query ([groups][128][64] bf16 at
 // element offset 512 * 128 of each 128 x 576 group block); box = 32 columns x 128 heads.
 bool make_qpe_map(CUtensorMap* m, const void* q_lat, uint64_t groups) {
@@ -920,7 +983,8 @@ bool make_qpe_map(CUtensorMap* m, const void* q_lat, uint64_t groups) {
 
 bool tc_decode_supported(const mla_config* c) {
   return c && c->act_dtype == MLA_BF16 &&
-         (c->cache_dtype == MLA_BF16 || c->cache_dtype == MLA_FP8_E4M3) && c->num_heads == tc::kH &&
+         (c->cache_dtype == MLA_BF16 || c->cache_dtype == MLA_FP8_E4M3 ||
+          c->cache_dtype == MLA_FP8_E4M3_B128) && c->num_heads == tc::kH &&
          c->d_latent == tc::kDC && c->d_rope == tc::kDR && c->page_size == tc::kP;
 }
 
@@ -931,7 +995,7 @@ int tc_decode_max_workers() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (cached[dev] == 0) {
-    if (cudaFuncSetAttribute(tc::decode_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tc::decode_tc_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              tc::kSmemBytes) != cudaSuccess)
       return 0;
     cudaLaunchConfig_t cfg = {};
@@ -946,7 +1010,7 @@ int tc_decode_max_workers() {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc::decode_tc_kernel<false>, &cfg) != cudaSuccess || n <= 0)
+    if (cudaOccupancyMaxActiveClusters(&n, tc::decode_tc_kernel<false, false>, &cfg) != cudaSuccess || n <= 0)
       return 0;
     cached[dev] = n;
   }
@@ -954,18 +1018,28 @@ int tc_decode_max_workers() {
 }
 
 cudaError_t launch_decode_tc(mla_dtype cache, const DecodeParams& p, cudaStream_t s) {
-  if (cache != MLA_BF16 && cache != MLA_FP8_E4M3) return cudaErrorNotSupported;
-  const bool fp8 = (cache == MLA_FP8_E4M3);
-  CUtensorMap kc, kpe, qpe;
+  if (cache != MLA_BF16 && cache != MLA_FP8_E4M3 && cache != MLA_FP8_E4M3_B128)
+    return cudaErrorNotSupported;
+  const bool b128 = (cache == MLA_FP8_E4M3_B128);
+  const bool fp8 = (cache == MLA_FP8_E4M3) || b128;
+  CUtensorMap kc, kpe, qpe, sc;
   const uint64_t cache_rows = (uint64_t)p.num_pages * tc::kP;
   const uint64_t groups = (uint64_t)p.batch * p.q_len;
-  const bool maps =
-      fp8 ? (tc::make_map_u8(&kc, p.cache, cache_rows, 128, 64) &&
-             tc::make_map_u8(&kpe, p.cache, cache_rows, 32, 64))
-          : (tc::make_map(&kc, p.cache, cache_rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
-             tc::make_map(&kpe, p.cache, cache_rows, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B));
+  bool maps;
+  if (b128)
+    maps = tc::make_map_b128(&kc, p.cache, cache_rows, 128, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           tc::make_map_b128(&sc, p.cache, cache_rows, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           tc::make_map_b128(&kpe, p.cache, cache_rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_64B);
+  else if (fp8)
+    maps = tc::make_map_u8(&kc, p.cache, cache_rows, 128, 64) &&
+           tc::make_map_u8(&kpe, p.cache, cache_rows, 32, 64);
+  else
+    maps = tc::make_map(&kc, p.cache, cache_rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           tc::make_map(&kpe, p.cache, cache_rows, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B);
   if (!maps || !tc::make_qpe_map(&qpe, p.q_lat, groups)) return cudaErrorInvalidValue;
-  auto kern = fp8 ? tc::decode_tc_kernel<true> : tc::decode_tc_kernel<false>;
+  if (!b128) sc = kc;                                       // unused by the other layouts
+  auto kern = b128 ? tc::decode_tc_kernel<true, true>
+                   : (fp8 ? tc::decode_tc_kernel<true, false> : tc::decode_tc_kernel<false, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -978,7 +1052,7 @@ cudaError_t launch_decode_tc(mla_dtype cache, const DecodeParams& p, cudaStream_
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, kern, kc, kpe, qpe, p);
+  e = cudaLaunchKernelEx(&cfg, kern, kc, kpe, qpe, sc, p);
   note_launch();
   return e;
 }

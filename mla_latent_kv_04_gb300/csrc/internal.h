@@ -54,6 +54,7 @@ struct DecodeParams {
   int max_pages, num_pages;
   int batch, q_len;
   int H, d_c, d_r, D, P;
+  long long row_bytes;        // bytes of one cache row (token)
   float scale_log2;           // softmax_scale * log2(e) (* cache_scale for fp8)
   float out_scale;            // cache_scale for an fp8 cache, else 1
   void* out_latent;           // [groups][H][d_c] act dtype

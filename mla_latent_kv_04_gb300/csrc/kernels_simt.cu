@@ -172,6 +172,59 @@ __global__ void __launch_bounds__(128) append_latent_kernel(
   }
 }
 
+// One block (128 threads) per token row, block-scaled fp8 cache: the latent in e4m3 with
+// one fp32 scale per 128 elements (amax / 448, then code = e4m3(x / scale), both IEEE
+// divisions; a block of zeros keeps scale 0 and codes 0), then the rotated k_pe in bf16.
+// Row bytes: [d_c codes][d_c / 128 fp32 scales][d_r bf16]. Warp w encodes latent blocks
+// w, w + 4, ...: four consecutive elements per lane, the block maximum by warp shuffles.
+template <typename AT>
+__global__ void __launch_bounds__(128) append_latent_b128_kernel(
+    const AT* __restrict__ c_kv, const AT* __restrict__ k_pe, long long ld_c, long long ld_k,
+    const int32_t* req_ids, const int32_t* positions, const int32_t* block_table, int batch,
+    int max_pages, uint8_t* __restrict__ cache, int num_pages, int P, int d_c, int d_r, int rotate,
+    RopeTable rt, int32_t* status) {
+  const int r = blockIdx.x;
+  int pos = 0;
+  const long long slot = append_slot(req_ids, positions, block_table, batch, max_pages, num_pages,
+                                     P, r, (threadIdx.x == 0) ? status : nullptr, &pos);
+  ptx::griddep_launch_dependents();
+  if (slot < 0) return;
+  ptx::griddep_wait();
+  const long long row_bytes = (long long)d_c + d_c / 32 + 2LL * d_r;
+  uint8_t* dst = cache + slot * row_bytes;
+  float* scales = reinterpret_cast<float*>(dst + d_c);
+  __nv_bfloat162* kdst = reinterpret_cast<__nv_bfloat162*>(dst + d_c + d_c / 32);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int blk = warp; blk < d_c / 128; blk += 4) {
+    const int c0 = 128 * blk + 4 * lane;
+    float x[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = to_f32(c_kv[(long long)r * ld_c + c0 + i]);
+    const float amax = warp_max(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
+    const float scale = amax / 448.f;
+    uint32_t packed = 0u;
+    if (scale > 0.f) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) packed |= (uint32_t)f32_to_fp8(x[i] / scale) << (8 * i);
+    }
+    *reinterpret_cast<uint32_t*>(dst + c0) = packed;
+    if (lane == 0) scales[blk] = scale;
+  }
+  for (int e = threadIdx.x; e < d_r / 2; e += blockDim.x) {
+    float x0 = to_f32(k_pe[(long long)r * ld_k + 2 * e]);
+    float x1 = to_f32(k_pe[(long long)r * ld_k + 2 * e + 1]);
+    if (rotate) {
+      float sn, cs;
+      rope_sincos(rt, e, pos, &sn, &cs);
+      const float y0 = x0 * cs - x1 * sn;
+      const float y1 = x0 * sn + x1 * cs;
+      x0 = y0;
+      x1 = y1;
+    }
+    kdst[e] = __floats2bfloat162_rn(x0, x1);
+  }
+}
+
 // GEMM epilogue of the append from hidden states: row r of [c | k_raw] = h_r W.
 template <typename CT>
 struct AppendEpi {
@@ -272,21 +325,21 @@ __global__ void __launch_bounds__(256) prep_kernel(PlanParams pp, const T* __res
 // lanes own tokens for the scores and latent dims for the output accumulation.
 template <typename CT> struct PageElem;
 template <> struct PageElem<float> {
-  __device__ __forceinline__ static float get(const uint32_t* row, int k) {
+  __device__ __forceinline__ static float get(const uint32_t* row, int k, int) {
     return __uint_as_float(row[k]);
   }
-  __device__ __forceinline__ static float dot(const uint32_t* row, const float* q, int D) {
+  __device__ __forceinline__ static float dot(const uint32_t* row, const float* q, int D, int) {
     float acc = 0.f;
     for (int w = 0; w < D; ++w) acc = fmaf(q[w], __uint_as_float(row[w]), acc);
     return acc;
   }
 };
 template <> struct PageElem<bf16> {
-  __device__ __forceinline__ static float get(const uint32_t* row, int k) {
+  __device__ __forceinline__ static float get(const uint32_t* row, int k, int) {
     const uint32_t w = row[k >> 1];
     return __uint_as_float((k & 1) ? (w & 0xFFFF0000u) : (w << 16));
   }
-  __device__ __forceinline__ static float dot(const uint32_t* row, const float* q, int D) {
+  __device__ __forceinline__ static float dot(const uint32_t* row, const float* q, int D, int) {
     float acc = 0.f;
     for (int w = 0; w < D / 2; ++w) {
       const uint32_t v = row[w];
@@ -297,15 +350,41 @@ template <> struct PageElem<bf16> {
   }
 };
 template <> struct PageElem<uint8_t> {
-  __device__ __forceinline__ static float get(const uint32_t* row, int k) {
+  __device__ __forceinline__ static float get(const uint32_t* row, int k, int) {
     return fp8_to_f32((uint8_t)(row[k >> 2] >> (8 * (k & 3))));
   }
-  __device__ __forceinline__ static float dot(const uint32_t* row, const float* q, int D) {
+  __device__ __forceinline__ static float dot(const uint32_t* row, const float* q, int D, int) {
     float acc = 0.f;
     for (int w = 0; w < D / 4; ++w) {
       const uint32_t v = row[w];
 #pragma unroll
       for (int b = 0; b < 4; ++b) acc = fmaf(q[4 * w + b], fp8_to_f32((uint8_t)(v >> (8 * b))), acc);
+    }
+    return acc;
+  }
+};
+// Block-scaled fp8 rows: d_c e4m3 codes, d_c / 128 fp32 scales, d_r bf16 (k_pe).
+struct E4m3B128 {};
+template <> struct PageElem<E4m3B128> {
+  __device__ __forceinline__ static float get(const uint32_t* row, int k, int d_c) {
+    return fp8_to_f32((uint8_t)(row[k >> 2] >> (8 * (k & 3)))) * __uint_as_float(row[(d_c >> 2) + (k >> 7)]);
+  }
+  __device__ __forceinline__ static float dot(const uint32_t* row, const float* q, int D, int d_c) {
+    float acc = 0.f;
+    for (int blk = 0; blk < d_c / 128; ++blk) {
+      float part = 0.f;
+      for (int w = 32 * blk; w < 32 * blk + 32; ++w) {
+        const uint32_t v = row[w];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) part = fmaf(q[4 * w + b], fp8_to_f32((uint8_t)(v >> (8 * b))), part);
+      }
+      acc = fmaf(part, __uint_as_float(row[(d_c >> 2) + blk]), acc);
+    }
+    const uint32_t* kr = row + (d_c >> 2) + (d_c >> 7);
+    for (int w = 0; w < (D - d_c) / 2; ++w) {
+      const uint32_t v = kr[w];
+      acc = fmaf(q[d_c + 2 * w], __uint_as_float(v << 16), acc);
+      acc = fmaf(q[d_c + 2 * w + 1], __uint_as_float(v & 0xFFFF0000u), acc);
     }
     return acc;
   }
@@ -317,14 +396,14 @@ template <typename QT, typename CT, int VPL>
 __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeParams p) {
   extern __shared__ __align__(16) uint32_t smem_simt[];
   const int D = p.D, P = p.P;
-  const int row_words = (int)((D * sizeof(CT) + 3) / 4);
+  const int row_words = (int)((p.row_bytes + 3) / 4);
   const int stride = row_words | 1;
   uint32_t* page_s = smem_simt;                                   // [P][stride]
   float* q_s = reinterpret_cast<float*>(smem_simt + P * stride);   // [SIMT_HEADS][D]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * SIMT_HEADS + warp;
   const bool head_ok = h < p.H;
-  const CT* cache = reinterpret_cast<const CT*>(p.cache);
+  const uint8_t* cache = reinterpret_cast<const uint8_t*>(p.cache);
   const QT* q_lat = reinterpret_cast<const QT*>(p.q_lat);
   const int it0 = p.worker_off[blockIdx.x], it1 = p.worker_off[blockIdx.x + 1];
   for (int it = it0; it < it1; ++it) {
@@ -346,7 +425,7 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeParams p) {
       const int ntok = min(P, kv - pg * P);
       __syncthreads();
       if (page_ok) {
-        const uint32_t* src = reinterpret_cast<const uint32_t*>(cache + (long long)page_id * P * D);
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(cache + (long long)page_id * P * p.row_bytes);
         for (int i = threadIdx.x; i < ntok * row_words; i += blockDim.x)
           page_s[(i / row_words) * stride + i % row_words] = src[i];
       } else if (threadIdx.x == 0) {
@@ -356,8 +435,8 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeParams p) {
       if (!page_ok || !head_ok) continue;
       const float* qh = q_s + warp * D;
       float s0 = -INFINITY, s1 = -INFINITY;
-      if (lane < ntok) s0 = PageElem<CT>::dot(page_s + lane * stride, qh, D) * p.scale_log2;
-      if (lane + 32 < ntok) s1 = PageElem<CT>::dot(page_s + (lane + 32) * stride, qh, D) * p.scale_log2;
+      if (lane < ntok) s0 = PageElem<CT>::dot(page_s + lane * stride, qh, D, p.d_c) * p.scale_log2;
+      if (lane + 32 < ntok) s1 = PageElem<CT>::dot(page_s + (lane + 32) * stride, qh, D, p.d_c) * p.scale_log2;
       const float m_new = fmaxf(m, warp_max(fmaxf(s0, s1)));
       const float alpha = exp2f(m - m_new);
       const float p0 = exp2f(s0 - m_new), p1 = exp2f(s1 - m_new);
@@ -370,7 +449,7 @@ __global__ void __launch_bounds__(256) decode_simt_kernel(DecodeParams p) {
 #pragma unroll
         for (int i = 0; i < VPL; ++i) {
           const int k = lane + 32 * i;
-          if (k < p.d_c) o[i] = fmaf(pj, PageElem<CT>::get(row, k), o[i]);
+          if (k < p.d_c) o[i] = fmaf(pj, PageElem<CT>::get(row, k, p.d_c), o[i]);
         }
       }
       m = m_new;
@@ -638,7 +717,7 @@ cudaError_t launch_query_prologue(mla_dtype act, const void* q_nope, const void*
 
 template <typename QT, typename CT, int VPL>
 static cudaError_t decode_simt_t(const DecodeParams& p, cudaStream_t s) {
-  const int row_words = (int)((p.D * sizeof(CT) + 3) / 4);
+  const int row_words = (int)((p.row_bytes + 3) / 4);
   const int stride = row_words | 1;
   const size_t smem = (size_t)p.P * stride * 4 + (size_t)SIMT_HEADS * p.D * 4;
   auto kern = decode_simt_kernel<QT, CT, VPL>;
@@ -665,6 +744,7 @@ cudaError_t launch_decode_simt(mla_dtype act, mla_dtype cache, const DecodeParam
                                cudaStream_t s) {
   if (act == MLA_F32) return decode_simt_vpl<float, float>(p, s);
   if (cache == MLA_BF16) return decode_simt_vpl<bf16, bf16>(p, s);
+  if (cache == MLA_FP8_E4M3_B128) return decode_simt_vpl<bf16, E4m3B128>(p, s);
   return decode_simt_vpl<bf16, uint8_t>(p, s);
 }
 
@@ -719,6 +799,15 @@ cudaError_t launch_append_latent(mla_dtype act, mla_dtype cache, const void* c_k
     return append_latent_t<float, float>(c_kv, k_pe, T, req_ids, positions, block_table, batch,
                                          max_pages, cache_ptr, num_pages, P, d_c, d_r, rotate, rt,
                                          cache_scale, status, s);
+  if (cache == MLA_FP8_E4M3_B128) {
+    if (T <= 0) return cudaSuccess;
+    append_latent_b128_kernel<bf16><<<T, 128, 0, s>>>(
+        reinterpret_cast<const bf16*>(c_kv), reinterpret_cast<const bf16*>(k_pe), (long long)d_c,
+        (long long)d_r, req_ids, positions, block_table, batch, max_pages,
+        reinterpret_cast<uint8_t*>(cache_ptr), num_pages, P, d_c, d_r, rotate, rt, status);
+    note_launch();
+    return cudaGetLastError();
+  }
   if (cache == MLA_BF16)
     return append_latent_t<bf16, bf16>(c_kv, k_pe, T, req_ids, positions, block_table, batch,
                                        max_pages, cache_ptr, num_pages, P, d_c, d_r, rotate, rt,
@@ -748,7 +837,12 @@ cudaError_t launch_append_finish(mla_dtype cache, const float* acc, int T, const
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   cudaError_t e;
-  if (cache == MLA_BF16)
+  if (cache == MLA_FP8_E4M3_B128)
+    e = cudaLaunchKernelEx(&cfg, append_latent_b128_kernel<float>, (const float*)acc,
+                           (const float*)(acc + d_c), ld, ld, req_ids, positions, block_table, batch,
+                           max_pages, reinterpret_cast<uint8_t*>(cache_ptr), num_pages, P, d_c, d_r, 1,
+                           rt, status);
+  else if (cache == MLA_BF16)
     e = cudaLaunchKernelEx(&cfg, append_latent_kernel<float, bf16>, (const float*)acc,
                            (const float*)(acc + d_c), ld, ld, req_ids, positions, block_table, batch,
                            max_pages, reinterpret_cast<bf16*>(cache_ptr), num_pages, P, d_c, d_r, 1, rt,

@@ -72,14 +72,23 @@ mla_status check_config(const mla_config* c) {
   if (c->act_dtype == MLA_F32) {
     if (c->cache_dtype != MLA_F32) return unsupported("fp32 activations need an fp32 cache");
   } else if (c->act_dtype == MLA_BF16) {
-    if (c->cache_dtype != MLA_BF16 && c->cache_dtype != MLA_FP8_E4M3)
-      return unsupported("bf16 activations need a bf16 or fp8_e4m3 cache");
+    if (c->cache_dtype != MLA_BF16 && c->cache_dtype != MLA_FP8_E4M3 &&
+        c->cache_dtype != MLA_FP8_E4M3_B128)
+      return unsupported("bf16 activations need a bf16, fp8_e4m3 or fp8_e4m3_b128 cache");
+    if (c->cache_dtype == MLA_FP8_E4M3_B128 && c->d_latent % 128)
+      return unsupported("the block-scaled fp8 cache needs d_latent a multiple of 128");
   } else {
     return invalid("act_dtype must be MLA_F32 or MLA_BF16");
   }
   if (c->cache_dtype == MLA_FP8_E4M3 && !(c->cache_scale > 0.f && isfinite(c->cache_scale)))
     return invalid("fp8 cache needs a positive finite cache_scale");
   return MLA_OK;
+}
+
+size_t cache_row_bytes(const mla_config* c) {
+  if (c->cache_dtype == MLA_FP8_E4M3_B128)
+    return (size_t)c->d_latent + (size_t)c->d_latent / 32 + 2 * (size_t)c->d_rope;
+  return (size_t)(c->d_latent + c->d_rope) * cache_size(c->cache_dtype);
 }
 
 float softmax_scale_of(const mla_config* c) {
@@ -182,6 +191,14 @@ static mla_status check_append(const mla_config* cfg, int T, const int32_t* req_
     return invalid("null pointer");
   if (batch <= 0 || max_pages <= 0 || num_pages <= 0)
     return invalid("batch, max_pages and num_pages must be positive");
+  return MLA_OK;
+}
+
+mla_status mla_cache_row_bytes(const mla_config* cfg, size_t* bytes) {
+  mla_status st = check_config(cfg);
+  if (st != MLA_OK) return st;
+  if (!bytes) return invalid("bytes is NULL");
+  *bytes = cache_row_bytes(cfg);
   return MLA_OK;
 }
 
@@ -368,6 +385,7 @@ mla_status mla_decode_ex(const mla_config* cfg, const void* q_nope, const void* 
   dp.d_r = cfg->d_rope;
   dp.D = D;
   dp.P = cfg->page_size;
+  dp.row_bytes = (long long)cache_row_bytes(cfg);
   const float cs = cfg->cache_dtype == MLA_FP8_E4M3 ? cfg->cache_scale : 1.f;
   dp.scale_log2 = tc ? cs : softmax_scale_of(cfg) * cs * kLog2e;   // tc: query pre-scaled
   dp.out_scale = cs;

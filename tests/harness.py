@@ -13,7 +13,7 @@ import mla_latent_kv_04_gb300 as M
 import oracle
 import workloads as W
 
-SENTINEL = {"f32": 0x7FC0DEAD, "bf16": 0x7FC1, "fp8_e4m3": 0x7F}   # NaN patterns
+SENTINEL = {"f32": 0x7FC0DEAD, "bf16": 0x7FC1, "fp8_e4m3": 0x7F, "fp8_e4m3_b128": 0x7F}   # NaN patterns
 
 
 def torch_act(wl):
@@ -34,6 +34,12 @@ def config(wl, cache_scale=None):
 def alloc_cache(wl, num_pages, dev, fill=True):
     D = wl.dims.d_cache
     n = num_pages * wl.dims.page_size * D
+    if wl.cache == "fp8_e4m3_b128":
+        t = torch.empty(num_pages * wl.dims.page_size * W.cache_row_bytes(wl), dtype=torch.uint8,
+                        device=dev)
+        if fill:
+            t.fill_(SENTINEL["fp8_e4m3_b128"])
+        return t
     if wl.cache == "f32":
         t = torch.empty(n, dtype=torch.int32, device=dev)
         if fill:
@@ -129,6 +135,10 @@ def cached_rows(wl, b, weights, cache_scale=None):
     k = np.concatenate(ks) if ks else np.zeros((0, d.d_rope))
     if wl.cache == "bf16":
         c = W.round_bf16(c.astype(np.float32)).astype(np.float64) if n_h else c
+        k = W.round_bf16(k.astype(np.float32)).astype(np.float64)
+    elif wl.cache == "fp8_e4m3_b128":
+        # the device quantises its fp32 rows directly (latent rows are bf16 values already)
+        c = oracle.e4m3_block_dequantize(*oracle.e4m3_block_quantize(c.astype(np.float32), 128), 128)
         k = W.round_bf16(k.astype(np.float32)).astype(np.float64)
     elif wl.cache == "fp8_e4m3":
         s = np.float32(cache_scale)

@@ -180,3 +180,15 @@ def test_unfolded_projection_validates_before_any_launch(lib):
                                         None) == M.MLA_ERR_WORKSPACE
     assert lib.mla_output_proj_unfolded(ctypes.byref(c), None, None, None, 0, None, None, 0,
                                         None) == M.MLA_OK
+
+
+def test_block_scaled_fp8_cache_rows(lib):
+    c = _cfg(cache_dtype=M.MLA_FP8_E4M3_B128)
+    assert M.mla_cache_row_bytes(c) == 512 + 4 * 4 + 2 * 64        # codes, 4 fp32 scales, bf16 k_pe
+    assert M.mla_cache_row_bytes(_cfg()) == 576 * 2
+    n = ctypes.c_size_t(0)
+    odd = _cfg(cache_dtype=M.MLA_FP8_E4M3_B128, d_latent=320)
+    assert lib.mla_cache_row_bytes(ctypes.byref(odd), ctypes.byref(n)) == M.MLA_ERR_UNSUPPORTED
+    f32 = M.make_config(W.TINY, "f32", "f32")
+    f32.cache_dtype = M.MLA_FP8_E4M3_B128
+    assert lib.mla_cache_row_bytes(ctypes.byref(f32), ctypes.byref(n)) == M.MLA_ERR_UNSUPPORTED

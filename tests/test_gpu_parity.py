@@ -113,9 +113,12 @@ def test_split_count_invariance(kernel):
 
 
 @pytest.mark.parametrize("kernel", KERNELS, ids=_kernel_id)
-def test_fp8_cache_small(kernel):
-    # partial pages, several pages, splits; e4m3 codes in the cache, one per-tensor scale
-    wl = W.scaled(W.WORKLOADS["v2_fp8_b128_s8192"], (5, 64, 300, 1, 1000), name="v2_fp8_small")
+@pytest.mark.parametrize("wl_name", ["v2_fp8_b128_s8192", "v2_fp8block_b128_s8192"],
+                         ids=["per_tensor", "block128"])
+def test_fp8_cache_small(kernel, wl_name):
+    # partial pages, several pages, splits; e4m3 codes in the cache with one per-tensor scale,
+    # or one scale per 128 latent elements of each token and k_pe in bf16
+    wl = W.scaled(W.WORKLOADS[wl_name], (5, 64, 300, 1, 1000), name=wl_name + "_small")
     st = Hn.build_state(wl, DEV)
     for nw in (0, 3):
         r = Hn.run_decode(wl, st, DEV, kernel=kernel, num_workers=nw)
@@ -218,7 +221,8 @@ def test_query_from_hidden(wl_name, rows):
 
 # ----------------------------------------------------------------------------- placement
 
-@pytest.mark.parametrize("wl_name", ["tiny_f32", "v2_b32_s4096", "v2_fp8_b128_s8192"])
+@pytest.mark.parametrize("wl_name", ["tiny_f32", "v2_b32_s4096", "v2_fp8_b128_s8192",
+                                     "v2_fp8block_b128_s8192"])
 def test_append_placement_is_bit_exact(wl_name):
     base = W.WORKLOADS[wl_name]
     wl = W.scaled(base, (70, 1, 128, 200), name=wl_name + "_place")
@@ -244,7 +248,16 @@ def test_append_placement_is_bit_exact(wl_name):
     torch.cuda.synchronize()
     rows = np.concatenate([c, k], axis=1)
     D = wl.dims.d_cache
-    if wl.cache == "f32":
+    if wl.cache == "fp8_e4m3_b128":
+        # [codes | fp32 block scales | bf16 k_pe] bytes, the oracle's quantiser on the same values
+        codes, scales = oracle.e4m3_block_quantize(c.astype(np.float32), 128)
+        kb = (k.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        enc = np.concatenate([codes, scales.astype(np.float32).view(np.uint8),
+                              kb.view(np.uint8)], axis=1)
+        got = cache.cpu().numpy()
+        fill = np.uint8(Hn.SENTINEL["fp8_e4m3_b128"])
+        D = W.cache_row_bytes(wl)
+    elif wl.cache == "f32":
         enc = rows.astype(np.float32).view(np.uint32)
         got = cache.view(torch.int32).cpu().numpy().view(np.uint32)
         fill = np.uint32(Hn.SENTINEL["f32"])
@@ -288,7 +301,7 @@ def _nearest_e4m3_ok(codes, v, slack):
     return ok_sign & (np.abs(np.abs(got) - a) <= best + 2.0 * slack)
 
 
-@pytest.mark.parametrize("cache_kind", ["bf16", "fp8_e4m3"])
+@pytest.mark.parametrize("cache_kind", ["bf16", "fp8_e4m3", "fp8_e4m3_b128"])
 def test_append_prefill_chunks_from_h(cache_kind):
     # Chunked prefill: every position of three requests comes from h through the append
     # projection, in two calls of 1500 and 501 rows whose rows mix the requests in random
@@ -320,7 +333,11 @@ def test_append_prefill_chunks_from_h(cache_kind):
                            bt_d, cache, dev_status=status, workspace=ws)
     assert M.mla_read_device_status(status) == M.MLA_OK
     D, P = wl.dims.d_cache, wl.dims.page_size
-    if fp8:
+    d_c = wl.dims.d_latent
+    if cache_kind == "fp8_e4m3_b128":
+        raw = cache.cpu().numpy().reshape(num_pages, P, W.cache_row_bytes(wl))
+        fill = np.uint8(Hn.SENTINEL["fp8_e4m3_b128"])
+    elif fp8:
         raw = cache.cpu().numpy().reshape(num_pages, P, D)
         fill = np.uint8(Hn.SENTINEL["fp8_e4m3"])
     else:
@@ -333,7 +350,22 @@ def test_append_prefill_chunks_from_h(cache_kind):
         ref = np.concatenate([c, oracle.rope(kraw, np.arange(S), wl.rope_theta)], axis=1)
         pg, sl = bt[b, np.arange(S) // P], np.arange(S) % P
         written[pg, sl] = True
-        if fp8:
+        if cache_kind == "fp8_e4m3_b128":
+            rows_b = raw[pg, sl]
+            scales = np.ascontiguousarray(rows_b[:, d_c:d_c + d_c // 32]).view(np.float32).astype(np.float64)
+            hb = np.abs(W.hidden(wl, b, S)).astype(np.float64) @ np.abs(wts["W_DKV_KR"]).astype(np.float64)
+            # each block's scale is the device's fp32 amax / 448: within the fp32 error of the
+            # largest element's dot product of the exact one
+            amax = np.abs(ref[:, :d_c]).reshape(S, -1, 128).max(axis=2)
+            bound = hb[:, :d_c].reshape(S, -1, 128).max(axis=2)
+            assert (np.abs(scales * 448.0 - amax) <= 1e-6 * bound + 1e-6 * amax).all()
+            v = ref[:, :d_c] / np.repeat(scales, 128, axis=1)
+            slack = 1e-6 * hb[:, :d_c] / np.repeat(scales, 128, axis=1) + 1e-5 * np.abs(v)
+            ok = _nearest_e4m3_ok(rows_b[:, :d_c], v, slack)
+            assert ok.all(), f"request {b}: {int((~ok).sum())} codes are not a nearest e4m3 code"
+            kbits = np.ascontiguousarray(rows_b[:, d_c + d_c // 32:]).view(np.uint16).astype(np.uint32) << 16
+            _check(wl, kbits.view(np.float32).astype(np.float64), ref[:, d_c:], f"k_pe rows of request {b}")
+        elif fp8:
             # fp32 error of the device's dot products: a small multiple of the unit roundoff
             # times sum_k |h_k W_kj| (the rotation adds the bounds of a pair), plus the
             # rotation's own relative error
@@ -380,7 +412,8 @@ def test_device_guard_skips_bad_pages_and_lengths():
 
 # ----------------------------------------------------------------------------- full sizes
 
-FULL = ["v2_b32_s4096", "v2_long_splitkv", "v2_ragged_spec", "v2_fp8_b128_s8192", "v2_spec_q4"]
+FULL = ["v2_b32_s4096", "v2_long_splitkv", "v2_ragged_spec", "v2_fp8_b128_s8192", "v2_spec_q4",
+        "v2_fp8block_b128_s8192"]
 
 
 @pytest.mark.parametrize("name", FULL)

@@ -124,6 +124,11 @@ WORKLOADS = {
         q_len=1, seed=4, fill="latent",
         description="fp8 e4m3 latent cache with one per-tensor scale, bf16 q/out: batch 128, "
                     "seq_len 8192"),
+    "v2_fp8block_b128_s8192": Workload(
+        name="v2_fp8block_b128_s8192", dims=V2, act="bf16", cache="fp8_e4m3_b128",
+        seq_lens=(8192,) * 128, q_len=1, seed=6, fill="latent",
+        description="block-scaled fp8 latent cache (e4m3 with one scale per 128 latent elements "
+                    "of each token, k_pe in bf16), bf16 q/out: batch 128, seq_len 8192"),
 }
 
 
@@ -288,7 +293,16 @@ def decode_flops(wl: Workload) -> float:
 
 
 def elt_bytes(dtype: str) -> int:
-    return {"f32": 4, "bf16": 2, "fp8_e4m3": 1}[dtype]
+    return {"f32": 4, "bf16": 2, "fp8_e4m3": 1, "fp8_e4m3_b128": 1}[dtype]
+
+
+def cache_row_bytes(wl: Workload) -> int:
+    """Bytes of one token's cache row: (d_c + d_r) elements, or for the block-scaled fp8
+    cache d_c codes, one fp32 scale per 128 latent elements and d_r bf16 values."""
+    d = wl.dims
+    if wl.cache == "fp8_e4m3_b128":
+        return d.d_latent + 4 * (d.d_latent // 128) + 2 * d.d_rope
+    return d.d_cache * elt_bytes(wl.cache)
 
 
 def decode_bytes(wl: Workload) -> dict:
@@ -296,10 +310,9 @@ def decode_bytes(wl: Workload) -> dict:
     d = wl.dims
     H, B, q = d.num_heads, wl.batch, wl.q_len
     ea = elt_bytes(wl.act)
-    ec = elt_bytes(wl.cache)
     kv_tokens = sum(int(s) for s in wl.seq_lens)
     return {
-        "cache": kv_tokens * d.d_cache * ec,
+        "cache": kv_tokens * cache_row_bytes(wl),
         "W_UK_abs": H * d.d_nope * d.d_latent * ea,
         "q": B * q * H * (d.d_nope + d.d_rope) * ea,
         "out_latent": B * q * H * d.d_latent * ea,
