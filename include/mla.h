@@ -140,11 +140,20 @@ mla_status mla_append_cache_latent(const mla_config* cfg, const void* c_kv, cons
  * share the key pages (0 = one per SM pair on this GPU); kernel: 0 = best available,
  * 1 = the SIMT kernel, 2 = the tensor-core (tcgen05) kernel. attn_events: optional
  * pair of cudaEvent_t (as void*) recorded on `stream` right before and right after
- * the attention kernel, for timing it alone; NULL entries are ignored. */
+ * the attention kernel, for timing it alone; NULL entries are ignored.
+ * Testing hooks of the tensor-core kernel's failure path (zero-initialise them otherwise):
+ * wait_limit_us: how long any of its barrier waits may last before the kernel gives up,
+ * records MLA_ERR_TIMEOUT in the status word, releases its tensor memory and exits
+ * (0 = the default, 2 s); withhold_page: when >= 1, the page of index withhold_page - 1 in
+ * worker 0's sequence is never loaded, so that the wait for it runs out (0 = off). Both
+ * leave every other worker's results intact; the call's status then reads
+ * MLA_ERR_TIMEOUT and its outputs for worker 0's requests are undefined. */
 typedef struct {
   int num_workers;
   int kernel;
   void* attn_events[2];
+  int wait_limit_us;
+  int withhold_page;
 } mla_decode_opts;
 
 /* Bytes of workspace mla_decode needs for this batch on the current device. */

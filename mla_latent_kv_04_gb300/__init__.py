@@ -53,7 +53,8 @@ class MlaConfig(ctypes.Structure):
 
 class MlaDecodeOpts(ctypes.Structure):
     _fields_ = [("num_workers", ctypes.c_int), ("kernel", ctypes.c_int),
-                ("attn_events", ctypes.c_void_p * 2)]
+                ("attn_events", ctypes.c_void_p * 2), ("wait_limit_us", ctypes.c_int),
+                ("withhold_page", ctypes.c_int)]
 
 
 _lib_handle = None
@@ -191,8 +192,10 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _opts(num_workers, kernel, attn_events=None):
+def _opts(num_workers, kernel, attn_events=None, wait_limit_us=0, withhold_page=0):
     o = MlaDecodeOpts(int(num_workers), int(kernel))
+    o.wait_limit_us = int(wait_limit_us)
+    o.withhold_page = int(withhold_page)
     if attn_events is not None:
         o.attn_events[0] = attn_events[0].cuda_event
         o.attn_events[1] = attn_events[1].cuda_event
@@ -269,8 +272,11 @@ def mla_decode_workspace_size(cfg, batch, q_len, num_workers=0, kernel=KERNEL_AU
 
 
 def mla_decode(cfg, q_nope, q_pe, W_UK_abs, cache, block_table, seq_lens, out_latent, lse,
-               workspace, num_workers=0, kernel=KERNEL_AUTO, stream=None, attn_events=None):
-    """attn_events: optional pair of torch.cuda.Event recorded around the attention kernel."""
+               workspace, num_workers=0, kernel=KERNEL_AUTO, stream=None, attn_events=None,
+               wait_limit_us=0, withhold_page=0):
+    """attn_events: optional pair of torch.cuda.Event recorded around the attention kernel.
+    wait_limit_us, withhold_page: testing hooks of the tensor-core kernel's failure path
+    (see mla_decode_opts in include/mla.h)."""
     a = (_act_dtype(cfg),)
     t = _torch()
     batch, q_len = q_nope.shape[0], q_nope.shape[1]
@@ -278,7 +284,7 @@ def mla_decode(cfg, q_nope, q_pe, W_UK_abs, cache, block_table, seq_lens, out_la
     D = d_c + d_r
     num_pages = cache.numel() // (cfg.page_size * _cache_row_elems(cfg))
     max_pages = block_table.shape[1]
-    o = _opts(num_workers, kernel, attn_events)
+    o = _opts(num_workers, kernel, attn_events, wait_limit_us, withhold_page)
     _check(lib().mla_decode_ex(
         ctypes.byref(cfg), _ptr(q_nope, "q_nope", a, batch * q_len * H * d_n),
         _ptr(q_pe, "q_pe", a, batch * q_len * H * d_r),

@@ -90,7 +90,6 @@ constexpr int kThreadsFp8 = kThreads + 4 * 32;
 constexpr int kSoftmaxWarps = 8;                         // two per head row (column halves)
 constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, 256, false, true);
-constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 // mbarrier slots (8 bytes each) at kOffBar
 enum {
@@ -109,6 +108,7 @@ struct Shared {
   uint8_t* base;       // 1 KB aligned
   uint32_t base_u32;
   volatile int* abort;
+  uint64_t limit_ns;   // how long a barrier wait may last (default 2 s)
   uint32_t* tmem_slot;
   __device__ uint32_t bar(int i) const { return base_u32 + kOffBar + 8 * i; }
   __device__ uint32_t stage(int s) const { return base_u32 + kOffStage + s * kStageBytes; }
@@ -129,7 +129,7 @@ __device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_
   while (true) {
     if (probe()) return true;
     if (*sh.abort) return false;
-    if (ptx::globaltimer() - t0 > kTimeoutNs) {
+    if (ptx::globaltimer() - t0 > sh.limit_ns) {
       *sh.abort = 1;
       flag_status(status, MLA_ERR_TIMEOUT);
       return false;
@@ -193,7 +193,7 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
   };
   for (int i = 0; i < kL2Ahead; ++i) ahead.next();      // pages 0..kL2Ahead-1 load directly
   int stage = 0;
-  uint32_t wrap = 0, q_iter = 0;
+  uint32_t wrap = 0, q_iter = 0, np_seq = 0;
   for (int it = it0; it < it1; ++it) {
     const WorkItem item = p.items[it];
     const int g = item.group, b = g / p.q_len;
@@ -218,6 +218,17 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
       }
       if (!wait_bar(sh, sh.bar(B_EMPTY0 + stage), (wrap & 1) ^ 1, p.status)) return;
       const uint32_t full = sh.bar(B_FULL0 + stage);
+      // testing hook: this page of worker 0 is never loaded, so the wait for it runs out
+      if (worker == 0 && p.withhold_page > 0 && np_seq == (uint32_t)(p.withhold_page - 1)) {
+        prefetch_next();
+        ++np_seq;
+        if (++stage == kNS) {
+          stage = 0;
+          ++wrap;
+        }
+        continue;
+      }
+      ++np_seq;
       if constexpr (kB128) {
         const uint32_t st = sh.stage(stage);
         ptx::mbar_arrive_expect_tx(full, 16384 + 64 * 16 + kKTilePE);
@@ -812,6 +823,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
   sh.base_u32 = aligned;
   sh.abort = reinterpret_cast<volatile int*>(sh.base + kOffBar + kBarArea - 16);
   sh.tmem_slot = reinterpret_cast<uint32_t*>(sh.base + kOffBar + kBarArea - 8);
+  sh.limit_ns = p.wait_limit_ns;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (int)ptx::cluster_ctarank();
   const int worker = blockIdx.x >> 1;
@@ -890,7 +902,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
   if (warp == 1) {
     if (lane == 0) {
       const uint64_t t0 = ptx::globaltimer();
-      while (!ptx::mbar_try_wait(sh.bar(B_TEARDOWN), 0) && ptx::globaltimer() - t0 < kTimeoutNs) {
+      while (!ptx::mbar_try_wait(sh.bar(B_TEARDOWN), 0) && ptx::globaltimer() - t0 < sh.limit_ns) {
       }
     }
     __syncwarp();

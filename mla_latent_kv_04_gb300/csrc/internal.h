@@ -68,6 +68,10 @@ struct DecodeParams {
   float* part_lse;            // [items][H]
   int32_t* status;
   int workers;
+  // tensor-core kernel: the limit of every barrier wait, in ns, and the testing hook that
+  // withholds page withhold_page - 1 of worker 0 (0 = off)
+  unsigned long long wait_limit_ns;
+  int withhold_page;
   // 0: part_o is fp32 [items][H][d_c]; 1: bf16 [items][d_c / 8][H][8] (eight latent dims of
   // every head contiguous, so a warp of consecutive heads writes one 512-byte run)
   int part_planar;

@@ -151,7 +151,7 @@ void set_last_error(const std::string& what) { g_last_error = what; }
 
 extern "C" {
 
-int mla_version(void) { return 100; }
+int mla_version(void) { return 101; }
 
 uint64_t mla_kernel_launches(void) { return (uint64_t)mla::g_launches.load(); }
 
@@ -401,6 +401,9 @@ mla_status mla_decode_ex(const mla_config* cfg, const void* q_nope, const void* 
   dp.status = pp.status;
   dp.workers = w.workers;
   dp.part_planar = tc ? 1 : 0;
+  dp.wait_limit_ns = (opts && opts->wait_limit_us > 0) ? 1000ull * (unsigned long long)opts->wait_limit_us
+                                                       : 2000000000ull;
+  dp.withhold_page = (opts && opts->withhold_page > 0) ? opts->withhold_page : 0;
   if (opts && opts->attn_events[0]) {
     e = cudaEventRecord((cudaEvent_t)opts->attn_events[0], s);
     if (e != cudaSuccess) return cuda_fail(e, "mla_decode (timing event)");

@@ -119,3 +119,39 @@ def test_tc_rescale_on_growing_scores(workers):
             tol = Hn.tolerance(wl, ref)
             assert err <= tol, f"request {b} {what}: max err {err:.3e} > {tol:.3e}"
     assert rescales > 100, rescales
+
+
+@pytest.mark.parametrize("cache", ["bf16", "fp8_e4m3"])
+def test_tc_wait_limit_reports_timeout_and_recovers(cache):
+    # The kernel's failure path, exercised without any fault: worker 0's first page is never
+    # loaded (a testing hook of mla_decode_opts), so one of its barrier waits runs out after
+    # the 200 us limit. The kernel records MLA_ERR_TIMEOUT, every role leaves its loop, the
+    # tensor memory is released and the CTA pair meets at its final barrier; the call's status
+    # reads the timeout. The next call in the same process, without the hook, must match the
+    # oracle (a leaked tensor-memory allocation or a stuck CTA would stall or break it).
+    base = W.WORKLOADS["v2_b32_s4096"] if cache == "bf16" else W.WORKLOADS["v2_fp8_b128_s8192"]
+    wl = W.scaled(base, (200, 130, 64), name="tc_timeout_" + cache)
+    st = Hn.build_state(wl, DEV)
+    q = W.queries(wl)
+    act = torch.bfloat16
+    B, H, d_c = wl.batch, 128, 512
+    out = torch.empty(B * H * d_c, dtype=act, device=DEV)
+    lse = torch.empty(B * H, dtype=torch.float32, device=DEV)
+    ws = torch.zeros(M.mla_decode_workspace_size(st["cfg"], B, 1, num_workers=3, kernel=M.KERNEL_TC),
+                     dtype=torch.uint8, device=DEV)
+    M.mla_decode(st["cfg"], Hn.to_dev(q["q_nope"], act, DEV), Hn.to_dev(q["q_pe"], act, DEV),
+                 st["W_UK_abs"], st["cache"], st["bt_d"], st["seq_lens_d"], out, lse, ws,
+                 num_workers=3, kernel=M.KERNEL_TC, wait_limit_us=200, withhold_page=1)
+    assert M.mla_read_device_status(ws) == M.MLA_ERR_TIMEOUT
+    # the same process, the same buffers, no hook: a clean call that matches the oracle
+    r = Hn.run_decode(wl, st, DEV, q=q, kernel=M.KERNEL_TC, num_workers=3)
+    assert r["status"] == M.MLA_OK
+    W_UK_abs64 = oracle.absorb_weights(st["weights"]["W_UK"], st["weights"]["W_UV"],
+                                       st["weights"]["W_O"], 128)[0]
+    for b in range(wl.batch):
+        o, l = Hn.expected_request(wl, b, st["weights"], q, W_UK_abs64,
+                                   cache_scale=st["cfg"].cache_scale)
+        for got, ref, what in ((r["out_latent"][b], o, "out_latent"), (r["lse"][b], l, "lse")):
+            err = Hn.max_err(got, ref)
+            tol = Hn.tolerance(wl, ref)
+            assert err <= tol, f"request {b} {what}: max err {err:.3e} > {tol:.3e}"
