@@ -111,8 +111,9 @@ mla_status mla_absorb_weights(const mla_config* cfg, const void* W_UK, const voi
  *   dev_status                          optional int32 device word (may be NULL):
  *                                       MLA_ERR_DEVICE_GUARD is OR-ed in for skipped rows.
  *   workspace                           device buffer of mla_append_cache_workspace_size
- *                                       bytes (256-byte aligned; may be NULL when that is 0)
- *                                       holding the fp32 projection before encoding.
+ *                                       bytes (may be NULL when that is 0, as it is now for
+ *                                       every configuration: the bf16 path sums its split-K
+ *                                       partials on chip and encodes in the same kernel).
  * Rows must not share a (request, position); T == 0 is a no-op. */
 mla_status mla_append_cache(const mla_config* cfg, const void* h, const void* W_DKV_KR, int T,
                             const int32_t* req_ids, const int32_t* positions,
@@ -124,7 +125,7 @@ mla_status mla_append_cache(const mla_config* cfg, const void* h, const void* W_
  * d_c + d_c/32 + 2 d_r for MLA_FP8_E4M3_B128. A page is P rows. */
 mla_status mla_cache_row_bytes(const mla_config* cfg, size_t* bytes);
 
-/* Bytes of workspace mla_append_cache needs for T rows (0 for fp32 activations). */
+/* Bytes of workspace mla_append_cache needs for T rows (currently 0). */
 mla_status mla_append_cache_workspace_size(const mla_config* cfg, int T, size_t* bytes);
 
 /* Append T tokens given their latent c_kv [T][d_c] and raw k_pe [T][d_r] (act dtype).
@@ -224,7 +225,8 @@ mla_status mla_output_proj_workspace_size(const mla_config* cfg, int rows, size_
  *   out[r] = sum_i out_latent[r][i] W_comb[i*d_c : (i+1)*d_c]
  *   out_latent [rows][H*d_c], W_comb [H*d_c][d], out [rows][d]  (act dtype),
  *   fp32 accumulation. workspace: 256-byte aligned device buffer of
- *   mla_output_proj_workspace_size bytes (an fp32 accumulator plus a status word). */
+ *   mla_output_proj_workspace_size bytes (an fp32 accumulator, used with fp32 activations,
+ *   plus a status word). */
 mla_status mla_output_proj(const mla_config* cfg, const void* out_latent, const void* W_comb,
                            int rows, void* out, void* workspace, size_t workspace_bytes,
                            void* stream);
@@ -242,8 +244,8 @@ mla_status mla_output_proj_unfolded_workspace_size(const mla_config* cfg, int ro
  *   out [rows][d]  (act dtype), fp32 accumulation. It streams H*d_c*d_v + H*d_v*d weight
  *   elements instead of W_comb's H*d_c*d (185 MB instead of 671 MB at DeepSeek-V2 shapes);
  *   equal to mla_output_proj up to the rounding of u. workspace: 256-byte aligned device
- *   buffer of mla_output_proj_unfolded_workspace_size bytes (an fp32 accumulator, a status
- *   word and u). Errors as mla_output_proj. */
+ *   buffer of mla_output_proj_unfolded_workspace_size bytes (an fp32 accumulator, used with
+ *   fp32 activations, a status word and u). Errors as mla_output_proj. */
 mla_status mla_output_proj_unfolded(const mla_config* cfg, const void* out_latent, const void* W_UV,
                                     const void* W_O, int rows, void* out, void* workspace,
                                     size_t workspace_bytes, void* stream);
@@ -263,7 +265,7 @@ mla_status mla_query_workspace_size(const mla_config* cfg, int d_q, int T, size_
  *   (W_i^UQ (W_i^UK)^T, d_q x d_c) would make the step read H*d_q*d_c weight elements (201 MB at
  *   DeepSeek-V2 shapes) instead of H*d_q*d_n + H*d_n*d_c (67 MB).
  *   workspace: 256-byte aligned device buffer of mla_query_workspace_size bytes (an fp32
- *   accumulator, a status word and c_q). d_q > 0; T == 0 is a no-op. Errors: MLA_ERR_INVALID
+ *   accumulator, used with fp32 activations, a status word and c_q). d_q > 0; T == 0 is a no-op. Errors: MLA_ERR_INVALID
  *   (null pointers, bad sizes), MLA_ERR_WORKSPACE, MLA_ERR_CUDA; nothing is launched on an
  *   error found on the host. */
 mla_status mla_query_from_hidden(const mla_config* cfg, int d_q, const void* h, const void* W_DQ,

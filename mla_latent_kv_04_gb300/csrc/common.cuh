@@ -80,4 +80,23 @@ __device__ __forceinline__ void flag_status(int32_t* status, int code) {
   if (status) atomicOr(status, 1 << code);
 }
 
+// Validates one append row; returns the destination row of the cache or -1.
+__device__ __forceinline__ long long append_slot(const int32_t* req_ids, const int32_t* positions,
+                                                 const int32_t* block_table, int batch,
+                                                 int max_pages, int num_pages, int P, int r,
+                                                 int32_t* status, int* pos_out) {
+  const int b = req_ids[r], pos = positions[r];
+  if (b < 0 || b >= batch || pos < 0 || pos / P >= max_pages) {
+    flag_status(status, MLA_ERR_DEVICE_GUARD);
+    return -1;
+  }
+  const int page = block_table[(long long)b * max_pages + pos / P];
+  if (page < 0 || page >= num_pages) {
+    flag_status(status, MLA_ERR_DEVICE_GUARD);
+    return -1;
+  }
+  *pos_out = pos;
+  return (long long)page * P + pos % P;
+}
+
 }  // namespace mla

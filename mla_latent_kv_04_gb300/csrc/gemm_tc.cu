@@ -1,16 +1,25 @@
 // tcgen05 GEMM for the dense contractions around the attention: the folded output
 // projection (huny.dev "DeepSeek MLA 해부" §3-2), the cache-append projection h W_DKV_KR
-// (§2-1, §2-3) and the per-head query absorption q_nope W_UK^T (§3-1).
+// (§2-1, §2-3), the per-head query absorption q_nope W_UK^T (§3-1), the query-side
+// compression (§2-2) and the one-time W^UV W^O fold (§3-2).
 //
-// All three have a short "rows" side (the batch's tokens) and a long weight side, so the
+// All of them have a short "rows" side (the batch's tokens) or a per-head weight, so the
 // kernel computes the transposed product D^T = W^T X^T ("swap AB"): the weight dimension
 // is the MMA's M = 128 (one TMEM lane per weight column), the tokens are N. Per 64-deep
 // K block a CTA TMA-loads the weight tile (MN-major, 128-byte swizzle, two 64-column
 // boxes) and the token tile (K-major, 128-byte swizzle) into a multi-stage ring; one
 // thread issues 4 MMAs (K = 16 each) per block into a TMEM accumulator; the four warps
-// then read the accumulator (tcgen05.ld) and hand each fp32 value to an epilogue functor.
-// Long K ranges are split across CTAs; split partial sums are added with fp32 atomics
-// into a workspace accumulator and finished by a small conversion kernel.
+// then read the accumulator (tcgen05.ld).
+//
+// Two kernels share that K loop:
+//   * tc_gemm_kernel: one CTA per output tile, the accumulator handed element by element
+//     to an epilogue functor (query absorption, lift, fold);
+//   * tc_gemm_cluster_kernel: long K ranges split across the CTAs of a thread-block
+//     cluster (up to 16); each CTA parks its fp32 partial tile in its own shared memory,
+//     and after a cluster barrier CTA r sums column slice r of the tile over every CTA of
+//     the cluster (distributed shared memory, in rank order, so the sum is deterministic)
+//     and hands the sums to a finishing functor (bf16 store; or RoPE, cache encoding and
+//     the page scatter of an append). No zeroed accumulator, no atomics, one launch.
 #include <cudaTypedefs.h>
 
 #include "internal.h"
@@ -47,8 +56,14 @@ struct Cfg {
   static constexpr int kBBytes = BN * kBK * 2;            // BN rows of 128 bytes
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = NS;
-  static constexpr int kBarOff = kStages * kStageBytes;
-  static constexpr int kSmem = kBarOff + 256 + 1024;
+  // the cluster kernel parks its fp32 partial tile [BN][128] over the idle ring
+  static constexpr int kPartBytes = BN * kBM * 4;
+  static constexpr int kBarOff =
+      kStages * kStageBytes > kPartBytes ? kStages * kStageBytes : kPartBytes;
+  // after the barriers: 4 KB in which a finishing functor may keep per-column values that
+  // it looks up while the K loop runs (up to 256 columns of 16 bytes)
+  static constexpr int kScratchOff = kBarOff + 256;
+  static constexpr int kSmem = kScratchOff + 4096 + 1024;
   static constexpr uint32_t kTmemCols = (BN <= 32) ? 32 : (BN <= 64 ? 64 : (BN <= 128 ? 128 : 256));
   static constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, BN, true, false);
 };
@@ -66,6 +81,53 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
       return false;
     }
   }
+}
+
+// The K loop: warp 0 lane 0 streams the A (weight) and B (token) tiles of K blocks
+// [kb0, kb1) through the ring; warp 1 lane 0 issues the MMAs and, after the last, commits
+// `done` (at once if the range is empty). A wait that runs out sets *abort and the status.
+template <int BN, int NS>
+__device__ __forceinline__ void k_loop(const CUtensorMap* tmA, const CUtensorMap* tmB, uint32_t base,
+                                       uint32_t tmem, int m0, int n0, int z, int kb0, int kb1,
+                                       volatile int* abort, int32_t* status) {
+  using C = Cfg<BN, NS>;
+  auto full = [&](int s) { return base + C::kBarOff + 8 * s; };
+  auto empty = [&](int s) { return base + C::kBarOff + 8 * (C::kStages + s); };
+  const uint32_t done = base + C::kBarOff + 8 * (2 * C::kStages);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0 && lane == 0) {
+    // every A operand here is a weight read once per decode step: its lines go first out of L2
+    const uint64_t pol = ptx::l2_policy_evict_first();
+    int stage = 0;
+    uint32_t wrap = 0;
+    for (int kb = kb0; kb < kb1; ++kb) {
+      if (!wait_bar(empty(stage), (wrap & 1) ^ 1, abort, status)) break;
+      const uint32_t st = base + stage * C::kStageBytes;
+      ptx::mbar_arrive_expect_tx(full(stage), C::kStageBytes);
+      ptx::tma_load_3d_hint(st, tmA, m0, kb * kBK, z, full(stage), pol);
+      ptx::tma_load_3d_hint(st + 8192, tmA, m0 + 64, kb * kBK, z, full(stage), pol);
+      ptx::tma_load_3d(st + C::kABytes, tmB, kb * kBK, n0, z, full(stage));
+      if (++stage == C::kStages) { stage = 0; ++wrap; }
+    }
+  } else if (warp == 1 && lane == 0) {
+    int stage = 0;
+    uint32_t wrap = 0;
+    for (int kb = kb0; kb < kb1; ++kb) {
+      if (!wait_bar(full(stage), wrap & 1, abort, status)) break;
+      ptx::tc_fence_after();
+      const uint32_t st = base + stage * C::kStageBytes;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint64_t a = ptx::smem_desc(st + 2048 * k, 8192, 1024, ptx::kSwizzle128);
+        const uint64_t b = ptx::smem_desc(st + C::kABytes + 32 * k, 16, 1024, ptx::kSwizzle128);
+        ptx::mma_bf16_ss(tmem, a, b, C::kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
+      }
+      ptx::mma_commit(empty(stage));
+      if (++stage == C::kStages) { stage = 0; ++wrap; }
+    }
+    ptx::mma_commit(done);
+  }
+  __syncwarp();
 }
 
 // D^T[z][m][n] = sum_k A[z][k][m] * B[z][n][k]; A is the MN-major weight, B the K-major
@@ -146,39 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (gp.wait_first) ptx::griddep_wait();   // the inputs (the token operand) are the previous kernels'
   bool ok = true;
 
-  if (warp == 0 && lane == 0) {
-    // every A operand here is a weight read once per decode step: its lines go first out of L2
-    const uint64_t pol = ptx::l2_policy_evict_first();
-    int stage = 0;
-    uint32_t wrap = 0;
-    for (int kb = kb0; kb < kb1; ++kb) {
-      if (!wait_bar(empty(stage), (wrap & 1) ^ 1, abort, gp.status)) break;
-      const uint32_t st = base + stage * C::kStageBytes;
-      ptx::mbar_arrive_expect_tx(full(stage), C::kStageBytes);
-      ptx::tma_load_3d_hint(st, &tmA, m0, kb * kBK, z, full(stage), pol);
-      ptx::tma_load_3d_hint(st + 8192, &tmA, m0 + 64, kb * kBK, z, full(stage), pol);
-      ptx::tma_load_3d(st + C::kABytes, &tmB, kb * kBK, n0, z, full(stage));
-      if (++stage == C::kStages) { stage = 0; ++wrap; }
-    }
-  } else if (warp == 1 && lane == 0) {
-    int stage = 0;
-    uint32_t wrap = 0;
-    for (int kb = kb0; kb < kb1; ++kb) {
-      if (!wait_bar(full(stage), wrap & 1, abort, gp.status)) break;
-      ptx::tc_fence_after();
-      const uint32_t st = base + stage * C::kStageBytes;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint64_t a = ptx::smem_desc(st + 2048 * k, 8192, 1024, ptx::kSwizzle128);
-        const uint64_t b = ptx::smem_desc(st + C::kABytes + 32 * k, 16, 1024, ptx::kSwizzle128);
-        ptx::mma_bf16_ss(tmem, a, b, C::kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
-      }
-      ptx::mma_commit(empty(stage));
-      if (++stage == C::kStages) { stage = 0; ++wrap; }
-    }
-    ptx::mma_commit(done);
-  }
-  __syncwarp();
+  k_loop<BN, NS>(&tmA, &tmB, base, tmem, m0, n0, z, kb0, kb1, abort, gp.status);
   // epilogue: every thread owns one TMEM lane = one row m of D^T
   ok = wait_bar(done, 0, abort, gp.status);
   ptx::tc_fence_after();
@@ -210,14 +240,110 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::griddep_wait();
 }
 
-// ------------------------------------------------------------------------------ epilogues
-struct EpiAtomic {            // acc[n][m] += v  (split-K partial sums, fp32 workspace)
-  float* acc;
-  long long ld;
-  __device__ __forceinline__ void operator()(int, int m, int n, float v) const {
-    atomicAdd(acc + (long long)n * ld + m, v);
+// D^T[m][n] = sum_k A[k][m] * B[n][k] with the K blocks split across the CTAs of a
+// cluster (gp.k_splits of them, cluster rank = split). Cluster = one (m tile, n tile).
+// After the K loop each CTA stores its partial tile as part[n][m] (fp32) over its idle
+// ring; after a cluster barrier, CTA r sums columns [r c, (r + 1) c) of the tile over the
+// cluster's CTAs in rank order (c = ceil(BN / k_splits)) and calls, for each such column,
+// fin(m0, t, n, i, v, good, scratch) with every thread t of the CTA (m = m0 + t; i = the
+// column's index in the slice; all threads take part, so fin may synchronise the CTA);
+// good is false if a wait of this CTA ran out. fin.prepare(m0, n_begin, n_end, j, nj,
+// scratch), run by warps 2-3 (thread j of nj) during the K loop, may fill the scratch for
+// the slice's columns. A second cluster barrier keeps every CTA's partial alive until its
+// peers have read it.
+template <int BN, int NS, class Fin>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_cluster_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB, const Params gp, const Fin fin) {
+  using C = Cfg<BN, NS>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* basep = smem_raw + (base - raw);
+  volatile int* abort = reinterpret_cast<volatile int*>(basep + C::kBarOff + 200);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(basep + C::kBarOff + 208);
+  const uint32_t done = base + C::kBarOff + 8 * (2 * C::kStages);
+  const int warp = threadIdx.x >> 5, t = threadIdx.x;
+  ptx::griddep_launch_dependents();
+
+  const int KS = gp.k_splits;
+  const int rank = (int)ptx::cluster_ctarank();
+  const int tile = (int)blockIdx.x / KS;
+  const int nt = tile % gp.n_tiles, mt = tile / gp.n_tiles;
+  const int kb0 = (int)((long long)rank * gp.k_blocks / KS);
+  const int kb1 = (int)((long long)(rank + 1) * gp.k_blocks / KS);
+  const int m0 = mt * kBM, n0 = nt * BN;
+
+  if (t == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(base + C::kBarOff + 8 * s, 1);
+      ptx::mbar_init(base + C::kBarOff + 8 * (C::kStages + s), 1);
+    }
+    ptx::mbar_init(done, 1);
+    *abort = 0;
+    ptx::fence_mbar_init();
+    ptx::prefetch_tensormap(&tmA);
+    ptx::prefetch_tensormap(&tmB);
   }
-};
+  if (warp == 0) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // launched with programmatic serialization: the token operand may be the previous
+  // kernel's output (and the weight a still earlier one's)
+  ptx::griddep_wait();
+  const int per = (BN + KS - 1) / KS;
+  const int c0 = rank * per, c1 = min(BN, c0 + per);
+  // warps 2 and 3 have nothing to do in the K loop: the functor's per-column look-ups of
+  // this CTA's columns go there (visible to every thread after the first cluster barrier)
+  void* scratch = basep + C::kScratchOff;
+  if (warp >= 2) fin.prepare(m0, n0 + c0, n0 + c1, t - 64, kThreads - 64, scratch);
+  k_loop<BN, NS>(&tmA, &tmB, base, tmem, m0, n0, 0, kb0, kb1, abort, gp.status);
+  const bool ok = wait_bar(done, 0, abort, gp.status);
+  const bool good = __syncthreads_and(ok && !*abort) != 0;
+  ptx::tc_fence_after();
+
+  // this CTA's partial tile, part[n][m], over the ring (every MMA that read it has completed)
+  float* part = reinterpret_cast<float*>(basep);
+  const uint32_t t_row = tmem + ((uint32_t)(32 * warp) << 16);
+#pragma unroll 1
+  for (int c = 0; c < BN; c += 32) {
+    uint32_t v[32];
+    if (good && kb1 > kb0) {
+      ptx::tmem_ld32(t_row + c, v);
+      ptx::tmem_wait_ld();
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = 0u;
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) part[(c + j) * kBM + t] = __uint_as_float(v[j]);
+  }
+  ptx::cluster_sync();
+
+  const uint32_t mine = ptx::smem_u32(part) + 4u * (uint32_t)t;
+  for (int c = c0; c < c1; ++c) {
+    float v = 0.f;
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+      if (r < KS) v += ptx::ld_dsmem_f32(ptx::map_to_rank(mine + 4u * (uint32_t)(c * kBM), (uint32_t)r));
+    fin(m0, t, n0 + c, c - c0, v, good, scratch);
+  }
+  ptx::cluster_sync();
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------------ epilogues
 struct EpiQLat {              // bf16(qs * v) at (group n, head z, latent dim m), row-major or planar
   bf16* q;
   int H, D;
@@ -236,6 +362,101 @@ struct EpiU {                 // bf16 u[n][z * dv + m]: head z's latent output o
   int dv;
   __device__ __forceinline__ void operator()(int z, int m, int n, float v) const {
     u[(long long)n * ld + (long long)z * dv + m] = __float2bfloat16_rn(v);
+  }
+};
+
+
+struct EpiStore {             // bf16 out[z][n][m] (leading dims ld_n, ld_z): the W^UV W^O fold
+  bf16* out;
+  long long ld_n, ld_z;
+  int M;
+  __device__ __forceinline__ void operator()(int z, int m, int n, float v) const {
+    if (m < M) out[(long long)z * ld_z + (long long)n * ld_n + m] = __float2bfloat16_rn(v);
+  }
+};
+
+// ------------------------------------------------------------------- cluster finishing
+struct FinStore {             // bf16 out[n][m] = v
+  bf16* out;
+  long long ld;
+  int M, N;
+  __device__ __forceinline__ void prepare(int, int, int, int, int, void*) const {}
+  __device__ __forceinline__ void operator()(int m0, int t, int n, int, float v, bool good,
+                                             const void*) const {
+    const int m = m0 + t;
+    if (good && m < M && n < N) out[(long long)n * ld + m] = __float2bfloat16_rn(v);
+  }
+};
+
+// Append from hidden states: v is column m of [c | k_raw] = h_n W_DKV_KR for token row n;
+// rotates the k_pe pairs (2i, 2i + 1), encodes and writes the row's element m into its page
+// slot. kMode 0: bf16 cache; 1: e4m3 with a per-tensor scale; 2: e4m3 latent with one fp32
+// scale per 128 elements (amax / 448, the block being this CTA's 128 columns) and bf16 k_pe,
+// row [d_c codes][d_c / 128 scales][d_r bf16].
+template <int kMode>
+struct FinAppend {
+  const int32_t* req_ids;
+  const int32_t* positions;
+  const int32_t* block_table;
+  int T, batch, max_pages, num_pages, P, d_c, d_r;
+  void* cache;
+  RopeTable rt;
+  float cache_scale;
+  int32_t* status;
+  // page slot and position of each token row of the slice (slot -1: row skipped)
+  __device__ __forceinline__ void prepare(int m0, int n_begin, int n_end, int j, int nj,
+                                          void* scratch) const {
+    long long* sp = reinterpret_cast<long long*>(scratch);
+    for (int i = j; i < n_end - n_begin; i += nj) {
+      const int n = n_begin + i;
+      int pos = 0;
+      long long slot = -1;
+      if (n < T)     // the CTAs of the first column tile report a bad row
+        slot = append_slot(req_ids, positions, block_table, batch, max_pages, num_pages, P, n,
+                           m0 == 0 ? status : nullptr, &pos);
+      sp[2 * i] = slot;
+      sp[2 * i + 1] = pos;
+    }
+  }
+  __device__ __forceinline__ void operator()(int m0, int t, int n, int i, float v, bool good,
+                                             const void* scratch) const {
+    __shared__ float red[kThreads / 32];
+    const int m = m0 + t, D = d_c + d_r;
+    const long long slot = reinterpret_cast<const long long*>(scratch)[2 * i];
+    const int pos = (int)reinterpret_cast<const long long*>(scratch)[2 * i + 1];
+    // the partner of a rotation pair sits in the neighbouring lane
+    const float other = __shfl_xor_sync(0xffffffffu, v, 1);
+    float y = v;
+    if (m >= d_c && m < D) {
+      const int kc = m - d_c;
+      float sn, cs;
+      rope_sincos(rt, kc >> 1, pos, &sn, &cs);
+      y = (kc & 1) ? other * sn + v * cs : v * cs - other * sn;
+    }
+    const bool live = good && slot >= 0 && m < D;
+    if (kMode == 0) {
+      if (live) reinterpret_cast<bf16*>(cache)[slot * D + m] = __float2bfloat16_rn(y);
+    } else if (kMode == 1) {
+      if (live) reinterpret_cast<uint8_t*>(cache)[slot * D + m] = CacheCodec<uint8_t>::encode(y, cache_scale);
+    } else {
+      uint8_t* dst = reinterpret_cast<uint8_t*>(cache) + slot * (long long)(d_c + d_c / 32 + 2 * d_r);
+      if (m0 < d_c) {           // a whole latent block: CTA-wide amax (uniform branch)
+        const float w = warp_max(fabsf(y));
+        __syncthreads();
+        if ((t & 31) == 0) red[t >> 5] = w;
+        __syncthreads();
+        float amax = red[0];
+#pragma unroll
+        for (int i = 1; i < kThreads / 32; ++i) amax = fmaxf(amax, red[i]);
+        const float scale = amax / 448.f;
+        if (live) {
+          dst[m] = scale > 0.f ? f32_to_fp8(y / scale) : (uint8_t)0;
+          if (t == 0) reinterpret_cast<float*>(dst + d_c)[m0 >> 7] = scale;
+        }
+      } else if (live) {
+        reinterpret_cast<bf16*>(dst + d_c + d_c / 32)[m - d_c] = __float2bfloat16_rn(y);
+      }
+    }
   }
 };
 
@@ -306,30 +527,129 @@ static cudaError_t run(const CUtensorMap& A, const CUtensorMap& B, Params gp, co
   return e;
 }
 
-// Chooses the N tile and the K split: enough CTAs to cover the SMs about once.
+// Chooses the N tile for the one-CTA-per-tile kernel (no K split).
 template <class Epi>
 static cudaError_t dispatch(const CUtensorMap& A, const CUtensorMap& Bmap32, const CUtensorMap& Bmap64,
                             const CUtensorMap& Bmap128, const CUtensorMap& Bmap256, Params gp,
-                            const Epi& epi, bool allow_split, cudaStream_t s) {
+                            const Epi& epi, cudaStream_t s) {
   int bn = gp.N <= 32 ? 32 : (gp.N <= 64 ? 64 : (gp.N <= 128 ? 128 : 256));
   gp.n_tiles = (gp.N + bn - 1) / bn;
   gp.k_blocks = (gp.K + kBK - 1) / kBK;
   gp.k_splits = 1;
-  if (allow_split) {
-    // about two CTAs per SM, each with at least 4 K blocks
-    const long long base_units = (long long)gp.batch * gp.m_tiles * gp.n_tiles;
-    const int per_sm = bn <= 64 ? 2 : 1;
-    int want = (int)(((long long)per_sm * sm_count()) / (base_units > 0 ? base_units : 1));
-    const int max_splits = gp.k_blocks / 4 > 0 ? gp.k_blocks / 4 : 1;
-    if (want > max_splits) want = max_splits;
-    gp.k_splits = want < 1 ? 1 : want;
-  }
-  const bool shallow = (gp.k_blocks + gp.k_splits - 1) / gp.k_splits <= 2;   // ring of 2 is enough
+  const bool shallow = gp.k_blocks <= 2;   // a ring of 2 is enough
   switch (bn) {
     case 32: return shallow ? run<32, 2>(A, Bmap32, gp, epi, s) : run<32, 4>(A, Bmap32, gp, epi, s);
     case 64: return shallow ? run<64, 2>(A, Bmap64, gp, epi, s) : run<64, 4>(A, Bmap64, gp, epi, s);
     case 128: return shallow ? run<128, 2>(A, Bmap128, gp, epi, s) : run<128, 5>(A, Bmap128, gp, epi, s);
     default: return shallow ? run<256, 2>(A, Bmap256, gp, epi, s) : run<256, 4>(A, Bmap256, gp, epi, s);
+  }
+}
+
+// Whether clusters of 16 CTAs of this kernel fit on the device (`need` of them at once);
+// clusters above 8 CTAs are a non-portable size that the kernel must opt in to.
+template <int BN, int NS, class Fin>
+static bool cluster16_fits(int need) {
+  static int fits = -1;        // per instantiation: number of co-resident clusters of 16
+  if (fits < 0) {
+    using C = Cfg<BN, NS>;
+    auto kern = tc_gemm_cluster_kernel<BN, NS, Fin>;
+    fits = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) ==
+            cudaSuccess &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(16, 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = C::kSmem;
+      cudaLaunchAttribute attr;
+      attr.id = cudaLaunchAttributeClusterDimension;
+      attr.val.clusterDim.x = 16;
+      attr.val.clusterDim.y = 1;
+      attr.val.clusterDim.z = 1;
+      cfg.attrs = &attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess) fits = n;
+    }
+    cudaGetLastError();        // a refused query leaves no error behind
+  }
+  return fits >= need;
+}
+
+template <int BN, int NS, class Fin>
+static cudaError_t run_cluster(const CUtensorMap& A, const CUtensorMap& B, Params gp, const Fin& fin,
+                               cudaStream_t s) {
+  using C = Cfg<BN, NS>;
+  auto kern = tc_gemm_cluster_kernel<BN, NS, Fin>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e == cudaSuccess && gp.k_splits > 8)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  const long long ctas = (long long)gp.m_tiles * gp.n_tiles * gp.k_splits;
+  if (ctas <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = (unsigned)gp.k_splits;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&cfg, kern, A, B, gp, fin);
+  note_launch();
+  return e;
+}
+
+// Tile and split choice of the cluster GEMM. Grids that fit once on the SMs with one CTA
+// per SM take a deep ring (8 stages) and the widest cluster that fits (16 where the device
+// allows, else 8, at least 2 K blocks per CTA); larger grids take a 4-stage ring (two CTAs
+// fit on an SM for N tiles up to 64) and about 1.6 CTAs per SM (at most 8 splits, at least
+// 4 K blocks per CTA). Measured at the 40-tile output projection of DeepSeek-V2 shapes
+// (W_comb, 671 MB): splits of 3, 4, 5, 6 and 7 take 117.6, 104, 100, 96.6 and 134 us;
+// clusters of 7 at two CTAs per SM do not all fit on the SMs at once.
+template <int BN, class Fin>
+static cudaError_t cluster_bn(const CUtensorMap& A, const CUtensorMap& B, Params gp, const Fin& fin,
+                              cudaStream_t s) {
+  const int sms = sm_count();
+  const int tiles = gp.m_tiles * gp.n_tiles;
+  const int kmax2 = gp.k_blocks / 2 > 0 ? gp.k_blocks / 2 : 1;
+  if constexpr (BN <= 64) {
+    if (tiles * 8 <= sms) {
+      int ks = sms / tiles;
+      if (ks > 16) ks = 16;
+      if (ks > 8 && !cluster16_fits<BN, 8, Fin>(tiles)) ks = 8;
+      if (ks > kmax2) ks = kmax2;
+      gp.k_splits = ks < 1 ? 1 : ks;
+      return run_cluster<BN, 8>(A, B, gp, fin, s);
+    }
+  }
+  int ks = (16 * sms + 5 * tiles) / (10 * tiles);     // round(1.6 sms / tiles)
+  const int kmax4 = gp.k_blocks / 4 > 0 ? gp.k_blocks / 4 : 1;
+  if (ks * tiles > 2 * sms) ks = 2 * sms / tiles;     // every CTA resident at once
+  if (ks > 8) ks = 8;
+  if (ks > kmax4) ks = kmax4;
+  gp.k_splits = ks < 1 ? 1 : ks;
+  return run_cluster<BN, 4>(A, B, gp, fin, s);
+}
+
+template <class Fin>
+static cudaError_t dispatch_cluster(const CUtensorMap (&Bm)[4], const CUtensorMap& A, Params gp,
+                                    const Fin& fin, cudaStream_t s) {
+  const int bn = gp.N <= 32 ? 32 : (gp.N <= 64 ? 64 : (gp.N <= 128 ? 128 : 256));
+  gp.n_tiles = (gp.N + bn - 1) / bn;
+  gp.k_blocks = (gp.K + kBK - 1) / kBK;
+  gp.batch = 1;
+  switch (bn) {
+    case 32: return cluster_bn<32>(A, Bm[0], gp, fin, s);
+    case 64: return cluster_bn<64>(A, Bm[1], gp, fin, s);
+    case 128: return cluster_bn<128>(A, Bm[2], gp, fin, s);
+    default: return cluster_bn<256>(A, Bm[3], gp, fin, s);
   }
 }
 
@@ -342,53 +662,26 @@ static bool b_maps(CUtensorMap (&maps)[4], const void* ptr, uint64_t K, uint64_t
   return true;
 }
 
-__global__ void finish_oproj_kernel(float* __restrict__ acc, bf16* __restrict__ out, long long n) {
-  // launched with programmatic serialization after the split-K GEMM that fills `acc`
-  ptx::griddep_wait();
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
-       i += (long long)gridDim.x * blockDim.x) {
-    out[i] = __float2bfloat16_rn(acc[i]);
-  }
-}
-
 }  // namespace gemm
 
-// out[rows][N] = o_lat[rows][K] . W_comb[K][N] (bf16), fp32 accumulator `acc` [rows][N].
-cudaError_t launch_output_proj_tc(const void* o_lat, const void* W_comb, int rows, int K, int N,
-                                  void* out, float* acc, int32_t* status, cudaStream_t s) {
+// out[rows][N] = x[rows][K] . W[K][N] (bf16 in and out, fp32 accumulation): the folded
+// output projection, the unfolded path's W_O product and the query-side GEMMs.
+cudaError_t launch_output_proj_tc(const void* x, const void* W, int rows, int K, int N, void* out,
+                                  int32_t* status, cudaStream_t s) {
   using namespace gemm;
   if (rows <= 0) return cudaSuccess;
   CUtensorMap A, Bm[4];
-  // A = W_comb as D^T's M x K: dims {N (m, contiguous), K}
-  if (!map3d(&A, W_comb, (uint64_t)N, (uint64_t)K, 1, (uint64_t)N * 2, (uint64_t)N * K * 2, 64, 64) ||
-      !b_maps(Bm, o_lat, (uint64_t)K, (uint64_t)rows, 1, (uint64_t)K * 2, (uint64_t)K * rows * 2))
+  // A = W as D^T's M x K: dims {N (m, contiguous), K}
+  if (!map3d(&A, W, (uint64_t)N, (uint64_t)K, 1, (uint64_t)N * 2, (uint64_t)N * K * 2, 64, 64) ||
+      !b_maps(Bm, x, (uint64_t)K, (uint64_t)rows, 1, (uint64_t)K * 2, (uint64_t)K * rows * 2))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaMemsetAsync(acc, 0, (size_t)rows * N * sizeof(float), s);
-  if (e != cudaSuccess) return e;
   Params gp{};
   gp.M = N;
   gp.N = rows;
   gp.K = K;
-  gp.batch = 1;
   gp.m_tiles = (N + kBM - 1) / kBM;
   gp.status = status;
-  e = dispatch(A, Bm[0], Bm[1], Bm[2], Bm[3], gp, EpiAtomic{acc, (long long)N}, true, s);
-  if (e != cudaSuccess) return e;
-  const long long n = (long long)rows * N;
-  // programmatic serialization: the conversion's blocks start while the GEMM (which signals
-  // launch_dependents at its start) ends, and wait for it before reading `acc`
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((n + 255) / 256 < 2048 ? (n + 255) / 256 : 2048), 1, 1);
-  cfg.blockDim = dim3(256, 1, 1);
-  cfg.stream = s;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr.val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, finish_oproj_kernel, acc, reinterpret_cast<bf16*>(out), n);
-  note_launch();
-  return e;
+  return dispatch_cluster(Bm, A, gp, FinStore{reinterpret_cast<bf16*>(out), (long long)N, N, rows}, s);
 }
 
 // u[r][h][0:d_v] = o_lat[r][h][:] . W_UV[:, h d_v : (h + 1) d_v]  (per head, bf16 out).
@@ -411,8 +704,37 @@ cudaError_t launch_lift_tc(const void* o_lat, const void* W_UV, int rows, int H,
   gp.batch = H;
   gp.m_tiles = (d_v + kBM - 1) / kBM;
   gp.status = status;
+  // launched with programmatic serialization; every block waits for the kernel before it
+  // (typically the decode's combine, which writes o_lat) ahead of reading any input
+  gp.pdl = 1;
+  gp.wait_first = 1;
   return dispatch(A, Bm[0], Bm[1], Bm[2], Bm[3], gp,
-                  EpiU{reinterpret_cast<bf16*>(u), (long long)H * d_v, d_v}, false, s);
+                  EpiU{reinterpret_cast<bf16*>(u), (long long)H * d_v, d_v}, s);
+}
+
+// W_comb[h][r][0:d] = W_UV[r][h d_v : (h + 1) d_v] . W_O[h d_v : (h + 1) d_v][0:d] for every
+// head h (bf16 in and out, fp32 accumulation): the one-time fold, per head a 512 x d_v by
+// d_v x d product. D^T's M is W_O's output column, N the latent row r, K the value dim.
+cudaError_t launch_fold_tc(const void* W_UV, const void* W_O, int H, int d_c, int d_v, int d,
+                           void* W_comb, int32_t* status, cudaStream_t s) {
+  using namespace gemm;
+  CUtensorMap A, Bm[4];
+  // A = W_O as head z's M x K: dims {d (m), d_v (k), H (z)}
+  if (!map3d(&A, W_O, (uint64_t)d, (uint64_t)d_v, (uint64_t)H, (uint64_t)d * 2,
+             (uint64_t)d_v * d * 2, 64, 64) ||
+      // B = W_UV as head z's N x K: dims {d_v (k), d_c (n), H (z)}
+      !b_maps(Bm, W_UV, (uint64_t)d_v, (uint64_t)d_c, (uint64_t)H, (uint64_t)H * d_v * 2,
+              (uint64_t)d_v * 2))
+    return cudaErrorInvalidValue;
+  Params gp{};
+  gp.M = d;
+  gp.N = d_c;
+  gp.K = d_v;
+  gp.batch = H;
+  gp.m_tiles = (d + kBM - 1) / kBM;
+  gp.status = status;
+  return dispatch(A, Bm[0], Bm[1], Bm[2], Bm[3], gp,
+                  EpiStore{reinterpret_cast<bf16*>(W_comb), (long long)d, (long long)d_c * d, d}, s);
 }
 
 // q_lat[g][h][0:d_c] = q_nope[g][h][:] . W_UK_abs[h]  (per head, bf16 out).
@@ -448,27 +770,50 @@ cudaError_t launch_query_absorb_tc(const void* q_nope, const void* W_UK_abs, int
   gp.rope_blocks = rope ? rope->groups * rope->hblocks : 0;
   if (rope) gp.rope = *rope;
   return dispatch(A, Bm[0], Bm[1], Bm[2], Bm[3], gp,
-                  EpiQLat{reinterpret_cast<bf16*>(q_lat), H, D, q_scale, planar}, false, s);
+                  EpiQLat{reinterpret_cast<bf16*>(q_lat), H, D, q_scale, planar}, s);
 }
 
-// acc[T][Dc] += h[T][d] . W[d][Dc]  (split-K partial sums into a zeroed fp32 buffer).
-cudaError_t launch_append_proj_tc(const void* h, const void* W, int T, int d, int Dc, float* acc,
-                                  int32_t* status, cudaStream_t s) {
+// The append from hidden states in one launch: [c | k_raw] = h W_DKV_KR (h [T][d],
+// W [d][d_c + d_r]), then per token row RoPE of k_raw at its position, the cache encoding
+// and the scatter into its page slot (the cluster GEMM's finishing step).
+cudaError_t launch_append_tc(mla_dtype cache_dtype, const void* h, const void* W, int T, int d,
+                             int d_c, int d_r, const int32_t* req_ids, const int32_t* positions,
+                             const int32_t* block_table, int batch, int max_pages, void* cache,
+                             int num_pages, int P, const RopeTable& rt, float cache_scale,
+                             int32_t* status, cudaStream_t s) {
   using namespace gemm;
+  if (T <= 0) return cudaSuccess;
+  const int Dc = d_c + d_r;
   CUtensorMap A, Bm[4];
   if (!map3d(&A, W, (uint64_t)Dc, (uint64_t)d, 1, (uint64_t)Dc * 2, (uint64_t)Dc * d * 2, 64, 64) ||
       !b_maps(Bm, h, (uint64_t)d, (uint64_t)T, 1, (uint64_t)d * 2, (uint64_t)d * T * 2))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaMemsetAsync(acc, 0, (size_t)T * Dc * sizeof(float), s);
-  if (e != cudaSuccess) return e;
   Params gp{};
   gp.M = Dc;
   gp.N = T;
   gp.K = d;
-  gp.batch = 1;
   gp.m_tiles = (Dc + kBM - 1) / kBM;
   gp.status = status;
-  return dispatch(A, Bm[0], Bm[1], Bm[2], Bm[3], gp, EpiAtomic{acc, (long long)Dc}, true, s);
+  auto fill = [&](auto f) {
+    f.req_ids = req_ids;
+    f.positions = positions;
+    f.block_table = block_table;
+    f.T = T;
+    f.batch = batch;
+    f.max_pages = max_pages;
+    f.num_pages = num_pages;
+    f.P = P;
+    f.d_c = d_c;
+    f.d_r = d_r;
+    f.cache = cache;
+    f.rt = rt;
+    f.cache_scale = cache_scale;
+    f.status = status;
+    return f;
+  };
+  if (cache_dtype == MLA_BF16) return dispatch_cluster(Bm, A, gp, fill(FinAppend<0>{}), s);
+  if (cache_dtype == MLA_FP8_E4M3) return dispatch_cluster(Bm, A, gp, fill(FinAppend<1>{}), s);
+  return dispatch_cluster(Bm, A, gp, fill(FinAppend<2>{}), s);
 }
 
 }  // namespace mla

@@ -112,8 +112,12 @@ cudaError_t launch_absorb(mla_dtype act, const void* W_UK, const void* W_UV, con
                           cudaStream_t s);
 
 // Tensor-core GEMMs (bf16 in, fp32 accumulate), gemm_tc.cu.
-cudaError_t launch_output_proj_tc(const void* o_lat, const void* W_comb, int rows, int K, int N,
-                                  void* out, float* acc, int32_t* status, cudaStream_t s);
+// out[rows][N] = x[rows][K] . W[K][N] through the cluster split-K GEMM (bf16, fp32 sums).
+cudaError_t launch_output_proj_tc(const void* x, const void* W, int rows, int K, int N, void* out,
+                                  int32_t* status, cudaStream_t s);
+// The one-time fold W_comb[h] = W_UV[:, h] . W_O[h] on the tensor cores (bf16).
+cudaError_t launch_fold_tc(const void* W_UV, const void* W_O, int H, int d_c, int d_v, int d,
+                           void* W_comb, int32_t* status, cudaStream_t s);
 // q_scale multiplies the query before its bf16 rounding (1, or the softmax scale times
 // log2(e) for the tensor-core attention, which then works in log2 units).
 // Query layouts in the workspace, per group of H heads (H * D elements each):
@@ -129,13 +133,12 @@ cudaError_t launch_query_absorb_tc(const void* q_nope, const void* W_UK_abs, int
                                    int d_n, int d_c, int D, float q_scale, int planar, void* q_lat,
                                    int32_t* status, const PlanParams* plan, const RopeJob* rope,
                                    cudaStream_t s);
-cudaError_t launch_append_proj_tc(const void* h, const void* W, int T, int d, int Dc, float* acc,
-                                  int32_t* status, cudaStream_t s);
-cudaError_t launch_append_finish(mla_dtype cache, const float* acc, int T, const int32_t* req_ids,
-                                 const int32_t* positions, const int32_t* block_table, int batch,
-                                 int max_pages, void* cache_ptr, int num_pages, int P, int d_c,
-                                 int d_r, const RopeTable& rt, float cache_scale, int32_t* status,
-                                 cudaStream_t s);
+// Append from h in one launch: projection, RoPE, encoding and page scatter (bf16 h and W).
+cudaError_t launch_append_tc(mla_dtype cache_dtype, const void* h, const void* W, int T, int d,
+                             int d_c, int d_r, const int32_t* req_ids, const int32_t* positions,
+                             const int32_t* block_table, int batch, int max_pages, void* cache,
+                             int num_pages, int P, const RopeTable& rt, float cache_scale,
+                             int32_t* status, cudaStream_t s);
 // q_pe rotation in one bf16 launch, plus (if pp.workers > 0) the status reset and the
 // planner in block 0, then as the decode's first kernel; without the planner it follows the
 // query absorption GEMM (which planned) with programmatic serialization.

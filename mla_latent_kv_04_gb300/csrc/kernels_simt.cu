@@ -109,25 +109,6 @@ struct AtomicAddEpi {
 };
 
 // ======================================================================== cache append
-// Validates one append row; returns the destination row of the cache or -1.
-__device__ __forceinline__ long long append_slot(const int32_t* req_ids, const int32_t* positions,
-                                                 const int32_t* block_table, int batch,
-                                                 int max_pages, int num_pages, int P, int r,
-                                                 int32_t* status, int* pos_out) {
-  const int b = req_ids[r], pos = positions[r];
-  if (b < 0 || b >= batch || pos < 0 || pos / P >= max_pages) {
-    flag_status(status, MLA_ERR_DEVICE_GUARD);
-    return -1;
-  }
-  const int page = block_table[(long long)b * max_pages + pos / P];
-  if (page < 0 || page >= num_pages) {
-    flag_status(status, MLA_ERR_DEVICE_GUARD);
-    return -1;
-  }
-  *pos_out = pos;
-  return (long long)page * P + pos % P;
-}
-
 // One block per token row: [c_kv | RoPE(k_pe)] encoded into its page slot.
 template <typename AT, typename CT>
 __global__ void __launch_bounds__(128) append_latent_kernel(
@@ -817,45 +798,6 @@ cudaError_t launch_append_latent(mla_dtype act, mla_dtype cache, const void* c_k
                                         cache_scale, status, s);
 }
 
-// RoPE + encode + scatter of append rows already projected into fp32 acc[T][d_c + d_r].
-cudaError_t launch_append_finish(mla_dtype cache, const float* acc, int T, const int32_t* req_ids,
-                                 const int32_t* positions, const int32_t* block_table, int batch,
-                                 int max_pages, void* cache_ptr, int num_pages, int P, int d_c,
-                                 int d_r, const RopeTable& rt, float cache_scale, int32_t* status,
-                                 cudaStream_t s) {
-  if (T <= 0) return cudaSuccess;
-  const long long ld = d_c + d_r;
-  // programmatic serialization: the blocks start while the projection GEMM (which signals
-  // launch_dependents at its start) ends, and wait for it before reading `acc`
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(T, 1, 1);
-  cfg.blockDim = dim3(128, 1, 1);
-  cfg.stream = s;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr.val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = 1;
-  cudaError_t e;
-  if (cache == MLA_FP8_E4M3_B128)
-    e = cudaLaunchKernelEx(&cfg, append_latent_b128_kernel<float>, (const float*)acc,
-                           (const float*)(acc + d_c), ld, ld, req_ids, positions, block_table, batch,
-                           max_pages, reinterpret_cast<uint8_t*>(cache_ptr), num_pages, P, d_c, d_r, 1,
-                           rt, status);
-  else if (cache == MLA_BF16)
-    e = cudaLaunchKernelEx(&cfg, append_latent_kernel<float, bf16>, (const float*)acc,
-                           (const float*)(acc + d_c), ld, ld, req_ids, positions, block_table, batch,
-                           max_pages, reinterpret_cast<bf16*>(cache_ptr), num_pages, P, d_c, d_r, 1, rt,
-                           cache_scale, status);
-  else
-    e = cudaLaunchKernelEx(&cfg, append_latent_kernel<float, uint8_t>, (const float*)acc,
-                           (const float*)(acc + d_c), ld, ld, req_ids, positions, block_table, batch,
-                           max_pages, reinterpret_cast<uint8_t*>(cache_ptr), num_pages, P, d_c, d_r, 1,
-                           rt, cache_scale, status);
-  note_launch();
-  return e;
-}
-
 template <typename AT, typename CT>
 static cudaError_t append_from_h_t(const void* h, const void* W, int T, int d,
                                    const int32_t* req_ids, const int32_t* positions,
@@ -899,7 +841,10 @@ static cudaError_t absorb_t(const void* W_UK, const void* W_UV, const void* W_O,
   note_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // block i of W_comb = W_UV[:, i*d_v:(i+1)*d_v] . W_O[i*d_v:(i+1)*d_v, :]
+  // block i of W_comb = W_UV[:, i*d_v:(i+1)*d_v] . W_O[i*d_v:(i+1)*d_v, :]; bf16 on the
+  // tensor cores where the tensor maps' 16-byte row strides allow
+  if (sizeof(T) == 2 && d % 8 == 0 && d_v % 8 == 0)
+    return launch_fold_tc(W_UV, W_O, H, d_c, d_v, d, W_comb, nullptr, s);
   StoreEpi<T> epi{reinterpret_cast<T*>(W_comb), (long long)d, (long long)d_c * d};
   return simt_gemm(reinterpret_cast<const T*>(W_UV), (long long)H * d_v, (long long)d_v,
                    reinterpret_cast<const T*>(W_O), (long long)d, (long long)d_v * d, d_c, d, d_v,

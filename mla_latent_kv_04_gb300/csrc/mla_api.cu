@@ -206,9 +206,8 @@ mla_status mla_append_cache_workspace_size(const mla_config* cfg, int T, size_t*
   mla_status st = check_config(cfg);
   if (st != MLA_OK) return st;
   if (T < 0 || !bytes) return invalid("T must be >= 0 and bytes non-NULL");
-  *bytes = cfg->act_dtype == MLA_BF16
-               ? align256((size_t)T * (cfg->d_latent + cfg->d_rope) * sizeof(float))
-               : 0;
+  // the bf16 append sums its split-K partials on chip and the others use none: no scratch
+  *bytes = 0;
   return MLA_OK;
 }
 
@@ -225,22 +224,18 @@ mla_status mla_append_cache(const mla_config* cfg, const void* h, const void* W_
   const RopeTable rt = rope_table(cfg);
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e;
-  if (cfg->act_dtype == MLA_BF16) {
-    const int Dc = cfg->d_latent + cfg->d_rope;
-    const size_t need = align256((size_t)T * Dc * sizeof(float));
-    if (!workspace || workspace_bytes < need) {
-      g_last_error = "workspace smaller than mla_append_cache_workspace_size";
-      return MLA_ERR_WORKSPACE;
-    }
-    if (((uintptr_t)workspace & 255) != 0) return invalid("workspace must be 256-byte aligned");
-    float* acc = (float*)workspace;
-    e = launch_append_proj_tc(h, W_DKV_KR, T, cfg->d_model, Dc, acc, dev_status, s);
-    if (e != cudaSuccess) return cuda_fail(e, "mla_append_cache (projection)");
-    e = launch_append_finish(cfg->cache_dtype, acc, T, req_ids, positions, block_table, batch,
-                             max_pages, cache, num_pages, cfg->page_size, cfg->d_latent,
-                             cfg->d_rope, rt, cfg->cache_scale, dev_status, s);
-    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_append_cache (encode)");
+  (void)workspace;
+  (void)workspace_bytes;
+  if (cfg->act_dtype == MLA_BF16 && cfg->d_model % 8 == 0 &&
+      (cfg->d_latent + cfg->d_rope) % 8 == 0) {
+    e = launch_append_tc(cfg->cache_dtype, h, W_DKV_KR, T, cfg->d_model, cfg->d_latent, cfg->d_rope,
+                         req_ids, positions, block_table, batch, max_pages, cache, num_pages,
+                         cfg->page_size, rt, cfg->cache_scale, dev_status, s);
+    return e == cudaSuccess ? MLA_OK : cuda_fail(e, "mla_append_cache");
   }
+  if (cfg->cache_dtype == MLA_FP8_E4M3_B128)
+    return unsupported("the block-scaled cache from h needs d_model and d_latent + d_rope "
+                       "multiples of 8");
   e = launch_append_from_h(cfg->act_dtype, cfg->cache_dtype, h, W_DKV_KR, T, cfg->d_model, req_ids,
                            positions, block_table, batch, max_pages, cache, num_pages,
                            cfg->page_size, cfg->d_latent, cfg->d_rope, rt, cfg->cache_scale,
@@ -455,8 +450,8 @@ mla_status mla_output_proj(const mla_config* cfg, const void* out_latent, const 
   cudaError_t e;
   if (cfg->act_dtype == MLA_BF16)
     e = launch_output_proj_tc(out_latent, W_comb, rows, cfg->num_heads * cfg->d_latent,
-                              cfg->d_model, out, (float*)workspace,
-                              (int32_t*)((char*)workspace + acc_bytes), (cudaStream_t)stream);
+                              cfg->d_model, out, (int32_t*)((char*)workspace + acc_bytes),
+                              (cudaStream_t)stream);
   else
     e = launch_output_proj_simt_ws(cfg->act_dtype, out_latent, W_comb, rows,
                                    cfg->num_heads * cfg->d_latent, cfg->d_model, out,
@@ -502,7 +497,7 @@ mla_status mla_output_proj_unfolded(const mla_config* cfg, const void* out_laten
   cudaError_t e;
   if (cfg->act_dtype == MLA_BF16 && d_c % 64 == 0 && d_v % 64 == 0) {
     e = launch_lift_tc(out_latent, W_UV, rows, H, d_c, d_v, u, status, s);
-    if (e == cudaSuccess) e = launch_output_proj_tc(u, W_O, rows, H * d_v, d, out, acc, status, s);
+    if (e == cudaSuccess) e = launch_output_proj_tc(u, W_O, rows, H * d_v, d, out, status, s);
   } else {
     e = launch_lift_simt(cfg->act_dtype, out_latent, W_UV, rows, H, d_c, d_v, u, s);
     if (e == cudaSuccess)
@@ -557,9 +552,9 @@ mla_status mla_query_from_hidden(const mla_config* cfg, int d_q, const void* h, 
                   n_nope % 8 == 0;
   cudaError_t e;
   if (tc) {
-    e = launch_output_proj_tc(h, W_DQ, T, d, d_q, c_q, acc, status, s);
-    if (e == cudaSuccess) e = launch_output_proj_tc(h, W_QR, T, d, n_pe, q_pe, acc, status, s);
-    if (e == cudaSuccess) e = launch_output_proj_tc(c_q, W_UQ, T, d_q, n_nope, q_nope, acc, status, s);
+    e = launch_output_proj_tc(h, W_DQ, T, d, d_q, c_q, status, s);
+    if (e == cudaSuccess) e = launch_output_proj_tc(h, W_QR, T, d, n_pe, q_pe, status, s);
+    if (e == cudaSuccess) e = launch_output_proj_tc(c_q, W_UQ, T, d_q, n_nope, q_nope, status, s);
   } else {
     e = launch_output_proj_simt_ws(cfg->act_dtype, h, W_DQ, T, d, d_q, c_q, acc, s);
     if (e == cudaSuccess)

@@ -69,6 +69,12 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local_addr, uint32_t ra
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
   return r;
 }
+// fp32 load from another CTA's shared memory (an address from map_to_rank).
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
 // Bulk copy (TMA engine) from this CTA's shared memory into another CTA's; the bytes are
 // counted on that CTA's mbarrier. Both addresses 16-byte aligned, size a multiple of 16.
 __device__ __forceinline__ void bulk_s2s(uint32_t remote_dst, uint32_t local_src, uint32_t bytes,

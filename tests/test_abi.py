@@ -119,7 +119,8 @@ def test_workspace_grows_with_batch(lib):
     b = M.mla_decode_workspace_size(c, 64, 2, num_workers=8)
     assert b > a > 0
     assert M.mla_output_proj_workspace_size(c, 32) == 32 * 5120 * 4 + 256
-    assert M.mla_append_cache_workspace_size(c, 32) == 32 * 576 * 4
+    # the bf16 append sums its split-K partials on chip: no scratch
+    assert M.mla_append_cache_workspace_size(c, 32) == 0
 
 
 def test_query_call_validates_before_any_launch(lib):
