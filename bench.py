@@ -234,6 +234,29 @@ def step(st, inp, ev=None):
         ev["oproj"][1].record()
 
 
+L2_FLUSH_BYTES = 256 << 20      # twice the GB300's 129 MB L2
+PART_REPS = 20
+
+
+def graph_ms(fn, reps, mk):
+    """Mean device time of fn(): `reps` calls captured back to back as one CUDA graph, the
+    graph replayed 3 times after a warm-up replay, timed with CUDA events."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = mk()
+    a.record()
+    for _ in range(3):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / (3 * reps)
+
+
 # ----------------------------------------------------------------------------- roofline
 
 def kernel_work(wl):
@@ -510,44 +533,48 @@ def main():
     s1.record()
     torch.cuda.synchronize()
     ms_stream = s0.elapsed_time(s1) / K
-    # per-part breakdown in a second pass: the events recorded between the parts (and around
-    # the attention kernel) sit between kernels chained by programmatic dependent launch and
-    # cost overlap, so they stay out of the headline loop above
+    # per-part breakdown. The attention kernel's own duration comes from the events libmla
+    # records around it on its stream (a pass of its own: events between kernels chained by
+    # programmatic dependent launch cost overlap). Each call of the step (append, decode,
+    # output projection) is timed as a CUDA graph of L2 flush + call, minus a graph of the
+    # flush alone, so that it starts from a cold L2 and without host launch gaps, as it does
+    # inside the step; a stream pass with events between the calls would count the host's
+    # launch time of the small calls instead.
     for i in range(K):
         step(st, inp, evs[i])
     torch.cuda.synchronize()
-    parts = {k: sum(event_ms(e[k][0], e[k][1]) for e in evs) / K
-             for k in ("append", "decode", "attn", "oproj")}
+    parts = {"attn": sum(event_ms(e["attn"][0], e["attn"][1]) for e in evs) / K}
+    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    calls = {
+        "append": lambda: M.mla_append_cache(st["cfg"], inp["h"], st["dw"]["W_DKV_KR"], st["new_req"],
+                                             st["new_pos"], st["bt_d"], st["cache"],
+                                             dev_status=st["status"], workspace=st["ws_a"]),
+        "decode": lambda: M.mla_decode(st["cfg"], inp["q_nope"], inp["q_pe"], st["W_UK_abs"],
+                                       st["cache"], st["bt_d"], inp["seq_lens"], st["out_lat"],
+                                       st["lse"], st["ws"], num_workers=st["workers"]),
+        "oproj": lambda: M.mla_output_proj(st["cfg"], st["out_lat"], st["W_comb"], st["out"],
+                                           st["ws_o"]),
+    }
+    # the flush reads its buffer: clean lines, so no write-back of dirty ones lands on the call
+    t_flush = graph_ms(lambda: flush.sum(), PART_REPS, mk)
+    for k, f in calls.items():
+        parts[k] = graph_ms(lambda: (flush.sum(), f()), PART_REPS, mk) - t_flush
+    del flush
     # mla_decode alone, back to back with nothing recorded inside (its four kernels overlap
-    # through programmatic dependent launch)
-    d0, d1 = mk()
-    d0.record()
-    for i in range(K):
-        M.mla_decode(st["cfg"], inp["q_nope"], inp["q_pe"], st["W_UK_abs"], st["cache"], st["bt_d"],
-                     inp["seq_lens"], st["out_lat"], st["lse"], st["ws"], num_workers=st["workers"])
-    d1.record()
-    torch.cuda.synchronize()
-    decode_alone_ms = d0.elapsed_time(d1) / K
-    # the unfolded output path (u_i = o_i W_i^UV, then u W_O), alone, back to back; it is an
-    # alternative to the step's folded projection and not part of the step
-    u0, u1 = mk()
-    u0.record()
-    for i in range(K):
-        M.mla_output_proj_unfolded(st["cfg"], st["out_lat"], st["dw"]["W_UV"], st["dw"]["W_O"],
-                                   st["out"], st["ws_u"])
-    u1.record()
-    torch.cuda.synchronize()
-    oproj_unfolded_ms = u0.elapsed_time(u1) / K
+    # through programmatic dependent launch; the 151 MB cache is larger than L2)
+    decode_alone_ms = graph_ms(calls["decode"], K, mk)
+    # the unfolded output path (u_i = o_i W_i^UV, then u W_O), alone, back to back as a graph;
+    # an alternative to the step's folded projection, not part of the step (its 185 MB of
+    # weights are larger than L2)
+    oproj_unfolded_ms = graph_ms(
+        lambda: M.mla_output_proj_unfolded(st["cfg"], st["out_lat"], st["dw"]["W_UV"], st["dw"]["W_O"],
+                                           st["out"], st["ws_u"]), K, mk)
     # the queries from h (c^Q = h W^DQ, q^C = c^Q W^UQ, q^R = h W^QR), alone, back to back
+    # (150 MB of weights)
     qj = st["query"]
-    v0, v1 = mk()
-    v0.record()
-    for i in range(K):
-        M.mla_query_from_hidden(st["cfg"], wl.dims.d_q, qj["h"], qj["w"]["W_DQ"], qj["w"]["W_UQ"],
-                                qj["w"]["W_QR"], qj["q_nope"], qj["q_pe"], qj["ws"])
-    v1.record()
-    torch.cuda.synchronize()
-    query_ms = v0.elapsed_time(v1) / K
+    query_ms = graph_ms(
+        lambda: M.mla_query_from_hidden(st["cfg"], wl.dims.d_q, qj["h"], qj["w"]["W_DQ"], qj["w"]["W_UQ"],
+                                        qj["w"]["W_QR"], qj["q_nope"], qj["q_pe"], qj["ws"]), K, mk)
     ms = max_over_ranks(ms, world)
     value = job_throughput(wl.batch * wl.q_len, world, ms)
     code = M.mla_read_device_status(st["status"])
@@ -624,6 +651,9 @@ def main():
         "decode_roofline": dict(rl["attn"], kernel="mla_decode attention kernel",
                                 traffic=ncu_traffic("attn", wl.name)),
         "parts_ms": {k: round(v, 4) for k, v in parts.items()},
+        "parts_method": "append, decode, oproj: a CUDA graph of an L2 flush (a 256 MB read) and "
+                        "the call, minus the flush alone (cold L2, no host launch gaps); attn: CUDA "
+                        "events around the attention kernel on its stream",
         "decode_alone_ms": round(decode_alone_ms, 4),
         "ms_per_step_stream": round(ms_stream, 4),
         "query_from_hidden": dict(roofline_entry(work["query"], query_ms, peaks, tpk),

@@ -37,6 +37,8 @@ struct Params {
   int M, N, K;           // D^T is M x N; K is the contraction length
   int batch;             // z dimension (heads for the query absorption)
   int m_tiles, n_tiles, k_blocks, k_splits;
+  int m_tiles_a;         // cluster kernel: M tiles [0, m_tiles_a) read the first A map, the rest
+                         // the second (two weights of one token operand in one launch)
   int32_t* status;
   int reset_status;      // 1: block 0 clears *status first (the first kernel of a decode call)
   int pdl;               // 1: launched with programmatic serialization after the kernel it
@@ -254,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int BN, int NS, class Fin>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_cluster_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmA2,
                            const __grid_constant__ CUtensorMap tmB, const Params gp, const Fin fin) {
   using C = Cfg<BN, NS>;
   extern __shared__ uint8_t smem_raw[];
@@ -272,7 +275,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nt = tile % gp.n_tiles, mt = tile / gp.n_tiles;
   const int kb0 = (int)((long long)rank * gp.k_blocks / KS);
   const int kb1 = (int)((long long)(rank + 1) * gp.k_blocks / KS);
-  const int m0 = mt * kBM, n0 = nt * BN;
+  // m0: the tile's first row of D^T in the concatenation of the two weights (each padded to
+  // whole tiles), as the functor sees it; ma: the same row within its own weight
+  const bool second = mt >= gp.m_tiles_a;
+  const int m0 = mt * kBM, ma = (second ? mt - gp.m_tiles_a : mt) * kBM, n0 = nt * BN;
+  const CUtensorMap* A = second ? &tmA2 : &tmA;
 
   if (t == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -282,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(done, 1);
     *abort = 0;
     ptx::fence_mbar_init();
-    ptx::prefetch_tensormap(&tmA);
+    ptx::prefetch_tensormap(A);
     ptx::prefetch_tensormap(&tmB);
   }
   if (warp == 0) {
@@ -302,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // this CTA's columns go there (visible to every thread after the first cluster barrier)
   void* scratch = basep + C::kScratchOff;
   if (warp >= 2) fin.prepare(m0, n0 + c0, n0 + c1, t - 64, kThreads - 64, scratch);
-  k_loop<BN, NS>(&tmA, &tmB, base, tmem, m0, n0, 0, kb0, kb1, abort, gp.status);
+  k_loop<BN, NS>(A, &tmB, base, tmem, ma, n0, 0, kb0, kb1, abort, gp.status);
   const bool ok = wait_bar(done, 0, abort, gp.status);
   const bool good = __syncthreads_and(ok && !*abort) != 0;
   ptx::tc_fence_after();
@@ -385,6 +392,23 @@ struct FinStore {             // bf16 out[n][m] = v
                                              const void*) const {
     const int m = m0 + t;
     if (good && m < M && n < N) out[(long long)n * ld + m] = __float2bfloat16_rn(v);
+  }
+};
+
+struct FinStore2 {            // rows m < Ma: out_a[n][m]; rows m >= Ma: out_b[n][m - Ma]
+  bf16* out_a;
+  bf16* out_b;
+  int M_a, Ma, M_b, N;     // M_a: A's columns, Ma: A's M tiles x 128, M_b: A2's columns
+  __device__ __forceinline__ void prepare(int, int, int, int, int, void*) const {}
+  __device__ __forceinline__ void operator()(int m0, int t, int n, int, float v, bool good,
+                                             const void*) const {
+    const int m = m0 + t;
+    if (!good || n >= N) return;
+    if (m < Ma) {
+      if (m < M_a) out_a[(long long)n * M_a + m] = __float2bfloat16_rn(v);
+    } else if (m - Ma < M_b) {
+      out_b[(long long)n * M_b + (m - Ma)] = __float2bfloat16_rn(v);
+    }
   }
 };
 
@@ -577,8 +601,8 @@ static bool cluster16_fits(int need) {
 }
 
 template <int BN, int NS, class Fin>
-static cudaError_t run_cluster(const CUtensorMap& A, const CUtensorMap& B, Params gp, const Fin& fin,
-                               cudaStream_t s) {
+static cudaError_t run_cluster(const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap& B,
+                               Params gp, const Fin& fin, cudaStream_t s) {
   using C = Cfg<BN, NS>;
   auto kern = tc_gemm_cluster_kernel<BN, NS, Fin>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
@@ -601,7 +625,7 @@ static cudaError_t run_cluster(const CUtensorMap& A, const CUtensorMap& B, Param
   attrs[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attrs;
   cfg.numAttrs = 2;
-  e = cudaLaunchKernelEx(&cfg, kern, A, B, gp, fin);
+  e = cudaLaunchKernelEx(&cfg, kern, A, A2, B, gp, fin);
   note_launch();
   return e;
 }
@@ -614,8 +638,8 @@ static cudaError_t run_cluster(const CUtensorMap& A, const CUtensorMap& B, Param
 // (W_comb, 671 MB): splits of 3, 4, 5, 6 and 7 take 117.6, 104, 100, 96.6 and 134 us;
 // clusters of 7 at two CTAs per SM do not all fit on the SMs at once.
 template <int BN, class Fin>
-static cudaError_t cluster_bn(const CUtensorMap& A, const CUtensorMap& B, Params gp, const Fin& fin,
-                              cudaStream_t s) {
+static cudaError_t cluster_bn(const CUtensorMap& A, const CUtensorMap& A2, const CUtensorMap& B,
+                              Params gp, const Fin& fin, cudaStream_t s) {
   const int sms = sm_count();
   const int tiles = gp.m_tiles * gp.n_tiles;
   const int kmax2 = gp.k_blocks / 2 > 0 ? gp.k_blocks / 2 : 1;
@@ -626,7 +650,7 @@ static cudaError_t cluster_bn(const CUtensorMap& A, const CUtensorMap& B, Params
       if (ks > 8 && !cluster16_fits<BN, 8, Fin>(tiles)) ks = 8;
       if (ks > kmax2) ks = kmax2;
       gp.k_splits = ks < 1 ? 1 : ks;
-      return run_cluster<BN, 8>(A, B, gp, fin, s);
+      return run_cluster<BN, 8>(A, A2, B, gp, fin, s);
     }
   }
   int ks = (16 * sms + 5 * tiles) / (10 * tiles);     // round(1.6 sms / tiles)
@@ -635,21 +659,24 @@ static cudaError_t cluster_bn(const CUtensorMap& A, const CUtensorMap& B, Params
   if (ks > 8) ks = 8;
   if (ks > kmax4) ks = kmax4;
   gp.k_splits = ks < 1 ? 1 : ks;
-  return run_cluster<BN, 4>(A, B, gp, fin, s);
+  return run_cluster<BN, 4>(A, A2, B, gp, fin, s);
 }
 
+// gp.m_tiles = the M tiles of A, plus those of A2 if A2 is given (m_tiles_a = A's).
 template <class Fin>
-static cudaError_t dispatch_cluster(const CUtensorMap (&Bm)[4], const CUtensorMap& A, Params gp,
-                                    const Fin& fin, cudaStream_t s) {
+static cudaError_t dispatch_cluster(const CUtensorMap (&Bm)[4], const CUtensorMap& A,
+                                    const CUtensorMap* A2, Params gp, const Fin& fin, cudaStream_t s) {
   const int bn = gp.N <= 32 ? 32 : (gp.N <= 64 ? 64 : (gp.N <= 128 ? 128 : 256));
   gp.n_tiles = (gp.N + bn - 1) / bn;
   gp.k_blocks = (gp.K + kBK - 1) / kBK;
   gp.batch = 1;
+  if (!A2) gp.m_tiles_a = gp.m_tiles;
+  const CUtensorMap& a2 = A2 ? *A2 : A;
   switch (bn) {
-    case 32: return cluster_bn<32>(A, Bm[0], gp, fin, s);
-    case 64: return cluster_bn<64>(A, Bm[1], gp, fin, s);
-    case 128: return cluster_bn<128>(A, Bm[2], gp, fin, s);
-    default: return cluster_bn<256>(A, Bm[3], gp, fin, s);
+    case 32: return cluster_bn<32>(A, a2, Bm[0], gp, fin, s);
+    case 64: return cluster_bn<64>(A, a2, Bm[1], gp, fin, s);
+    case 128: return cluster_bn<128>(A, a2, Bm[2], gp, fin, s);
+    default: return cluster_bn<256>(A, a2, Bm[3], gp, fin, s);
   }
 }
 
@@ -681,7 +708,32 @@ cudaError_t launch_output_proj_tc(const void* x, const void* W, int rows, int K,
   gp.K = K;
   gp.m_tiles = (N + kBM - 1) / kBM;
   gp.status = status;
-  return dispatch_cluster(Bm, A, gp, FinStore{reinterpret_cast<bf16*>(out), (long long)N, N, rows}, s);
+  return dispatch_cluster(Bm, A, nullptr, gp, FinStore{reinterpret_cast<bf16*>(out), (long long)N, N, rows}, s);
+}
+
+// out_a[rows][N_a] = x . W_a and out_b[rows][N_b] = x . W_b in one launch (x [rows][K],
+// W_a [K][N_a], W_b [K][N_b]; bf16 in and out, fp32 sums): two weights applied to the same
+// tokens, e.g. the query-side W_DQ and W_QR applied to h.
+cudaError_t launch_two_proj_tc(const void* x, const void* W_a, const void* W_b, int rows, int K,
+                               int N_a, int N_b, void* out_a, void* out_b, int32_t* status,
+                               cudaStream_t s) {
+  using namespace gemm;
+  if (rows <= 0) return cudaSuccess;
+  CUtensorMap A, A2, Bm[4];
+  if (!map3d(&A, W_a, (uint64_t)N_a, (uint64_t)K, 1, (uint64_t)N_a * 2, (uint64_t)N_a * K * 2, 64, 64) ||
+      !map3d(&A2, W_b, (uint64_t)N_b, (uint64_t)K, 1, (uint64_t)N_b * 2, (uint64_t)N_b * K * 2, 64, 64) ||
+      !b_maps(Bm, x, (uint64_t)K, (uint64_t)rows, 1, (uint64_t)K * 2, (uint64_t)K * rows * 2))
+    return cudaErrorInvalidValue;
+  Params gp{};
+  gp.M = N_a + N_b;
+  gp.N = rows;
+  gp.K = K;
+  gp.m_tiles_a = (N_a + kBM - 1) / kBM;
+  gp.m_tiles = gp.m_tiles_a + (N_b + kBM - 1) / kBM;
+  gp.status = status;
+  return dispatch_cluster(Bm, A, &A2, gp,
+                          FinStore2{reinterpret_cast<bf16*>(out_a), reinterpret_cast<bf16*>(out_b), N_a,
+                                    gp.m_tiles_a * kBM, N_b, rows}, s);
 }
 
 // u[r][h][0:d_v] = o_lat[r][h][:] . W_UV[:, h d_v : (h + 1) d_v]  (per head, bf16 out).
@@ -811,9 +863,10 @@ cudaError_t launch_append_tc(mla_dtype cache_dtype, const void* h, const void* W
     f.status = status;
     return f;
   };
-  if (cache_dtype == MLA_BF16) return dispatch_cluster(Bm, A, gp, fill(FinAppend<0>{}), s);
-  if (cache_dtype == MLA_FP8_E4M3) return dispatch_cluster(Bm, A, gp, fill(FinAppend<1>{}), s);
-  return dispatch_cluster(Bm, A, gp, fill(FinAppend<2>{}), s);
+  if (cache_dtype == MLA_BF16) return dispatch_cluster(Bm, A, nullptr, gp, fill(FinAppend<0>{}), s);
+  if (cache_dtype == MLA_FP8_E4M3)
+    return dispatch_cluster(Bm, A, nullptr, gp, fill(FinAppend<1>{}), s);
+  return dispatch_cluster(Bm, A, nullptr, gp, fill(FinAppend<2>{}), s);
 }
 
 }  // namespace mla

@@ -115,6 +115,10 @@ cudaError_t launch_absorb(mla_dtype act, const void* W_UK, const void* W_UV, con
 // out[rows][N] = x[rows][K] . W[K][N] through the cluster split-K GEMM (bf16, fp32 sums).
 cudaError_t launch_output_proj_tc(const void* x, const void* W, int rows, int K, int N, void* out,
                                   int32_t* status, cudaStream_t s);
+// out_a = x . W_a and out_b = x . W_b (same tokens, two weights) in one launch (bf16).
+cudaError_t launch_two_proj_tc(const void* x, const void* W_a, const void* W_b, int rows, int K,
+                               int N_a, int N_b, void* out_a, void* out_b, int32_t* status,
+                               cudaStream_t s);
 // The one-time fold W_comb[h] = W_UV[:, h] . W_O[h] on the tensor cores (bf16).
 cudaError_t launch_fold_tc(const void* W_UV, const void* W_O, int H, int d_c, int d_v, int d,
                            void* W_comb, int32_t* status, cudaStream_t s);

@@ -552,8 +552,8 @@ mla_status mla_query_from_hidden(const mla_config* cfg, int d_q, const void* h, 
                   n_nope % 8 == 0;
   cudaError_t e;
   if (tc) {
-    e = launch_output_proj_tc(h, W_DQ, T, d, d_q, c_q, status, s);
-    if (e == cudaSuccess) e = launch_output_proj_tc(h, W_QR, T, d, n_pe, q_pe, status, s);
+    // c_q and q_pe both read h: one launch for the two weights, then q_nope from c_q
+    e = launch_two_proj_tc(h, W_DQ, W_QR, T, d, d_q, n_pe, c_q, q_pe, status, s);
     if (e == cudaSuccess) e = launch_output_proj_tc(c_q, W_UQ, T, d_q, n_nope, q_nope, status, s);
   } else {
     e = launch_output_proj_simt_ws(cfg->act_dtype, h, W_DQ, T, d, d_q, c_q, acc, s);

@@ -165,6 +165,30 @@ def test_output_projection_bf16(rows):
     assert np.array_equal(got_a, ref_a)           # a pure relayout: exact
 
 
+def test_fold_every_element_at_v2_shapes():
+    # mla_absorb_weights with bf16 weights at DeepSeek-V2 shapes (the tensor-core GEMM):
+    # every element of W_comb = W_i^UV W_i^O (huny.dev §3-2) is the fp64 fold of the same
+    # bf16 inputs rounded once to bf16 (|err| <= 2^-8 |ref|), up to the fp32 accumulation of
+    # its 128 products (|err| <= 2^-16 sum_k |W_UV| |W_O|, far above the fp32 bound).
+    wl = W.WORKLOADS["v2_b32_s4096"]
+    H = wl.dims.num_heads
+    wts = W.weights(wl)
+    dw = {k: Hn.to_dev(v, torch.bfloat16, DEV) for k, v in wts.items() if k != "W_DKV_KR"}
+    W_UK_abs = torch.empty(H * 128 * 512, dtype=torch.bfloat16, device=DEV)
+    W_comb = torch.full((H * 512 * 5120,), float("nan"), dtype=torch.bfloat16, device=DEV)
+    cfg = Hn.config(wl)
+    M.mla_absorb_weights(cfg, dw["W_UK"], dw["W_UV"], dw["W_O"], W_UK_abs, W_comb)
+    torch.cuda.synchronize()
+    got = W_comb.float().cpu().numpy().astype(np.float64).reshape(H * 512, 5120)
+    ref = oracle.absorb_weights(wts["W_UK"], wts["W_UV"], wts["W_O"], H)[1]
+    mag = oracle.absorb_weights(np.abs(wts["W_UK"]), np.abs(wts["W_UV"]), np.abs(wts["W_O"]), H)[1]
+    err = np.abs(got - ref)
+    bound = 2.0 ** -8 * np.abs(ref) + 2.0 ** -16 * mag
+    bad = np.argwhere(~(err <= bound))
+    assert bad.size == 0, f"{len(bad)} elements off, first {bad[0]}: got {got[tuple(bad[0])]}, " \
+                          f"ref {ref[tuple(bad[0])]}"
+
+
 @pytest.mark.parametrize("wl_name,rows", [("v2_b32_s4096", 3), ("v2_b32_s4096", 40),
                                           ("tiny_f32", 5)])
 def test_output_projection_unfolded(wl_name, rows):
