@@ -198,3 +198,32 @@ def run_full_step_tiny(wl, dev):
             "out": out.float().cpu().numpy().astype(np.float64).reshape(B, qn, d),
             "expected": {"out_latent": np.stack(exp_o), "lse": np.stack(exp_l),
                          "out": np.stack(exp_out).reshape(B, qn, d)}}
+
+
+def run_small_step_v2_bf16(dev):
+    """Smoke path on the tensor cores: DeepSeek-V2 head shapes in bf16, two short requests
+    whose last two tokens come from h (the cluster-GEMM append), a decode on the tcgen05
+    kernel with split work, and the unfolded output projection of the two rows. Returns the
+    device results and the fp64 oracle's expectations for the same inputs."""
+    wl = W.scaled(W.WORKLOADS["v2_b32_s4096"], (70, 130), name="v2_smoke", new_from_h=2)
+    st = build_state(wl, dev)
+    r = run_decode(wl, st, dev, kernel=M.KERNEL_TC, num_workers=3)
+    cfg = st["cfg"]
+    B, H, d = wl.batch, wl.dims.num_heads, wl.dims.d_model
+    wts = st["weights"]
+    out = torch.empty(B * d, dtype=torch.bfloat16, device=dev)
+    ws = torch.zeros(M.mla_output_proj_unfolded_workspace_size(cfg, B), dtype=torch.uint8, device=dev)
+    M.mla_output_proj_unfolded(cfg, r["out_latent_dev"], st["dw"]["W_UV"], st["dw"]["W_O"], out, ws)
+    torch.cuda.synchronize()
+    W_UK_abs64 = np.stack([wts["W_UK"][:, i * 128:(i + 1) * 128].T.astype(np.float64) for i in range(H)])
+    exp_o, exp_l = [], []
+    for b in range(B):
+        o, l = expected_request(wl, b, wts, r["q"], W_UK_abs64)
+        exp_o.append(o)
+        exp_l.append(l)
+    exp_o = np.stack(exp_o)
+    u = oracle.lift_latent(r["out_latent"].reshape(B, H * 512), wts["W_UV"], H)
+    exp_out = oracle.mha_output(u, wts["W_O"])
+    return {"wl": wl, "status": r["status"], "out_latent": r["out_latent"], "lse": r["lse"],
+            "out": out.float().cpu().numpy().astype(np.float64).reshape(B, d),
+            "expected": {"out_latent": exp_o, "lse": np.stack(exp_l), "out": exp_out}}
