@@ -108,7 +108,6 @@ struct Shared {
   uint8_t* base;       // 1 KB aligned
   uint32_t base_u32;
   volatile int* abort;
-  uint64_t limit_ns;   // how long a barrier wait may last (default 2 s)
   uint32_t* tmem_slot;
   __device__ uint32_t bar(int i) const { return base_u32 + kOffBar + 8 * i; }
   __device__ uint32_t stage(int s) const { return base_u32 + kOffStage + s * kStageBytes; }
@@ -117,8 +116,10 @@ struct Shared {
   __device__ uint32_t qpe() const { return base_u32 + kOffQPe; }
 };
 
+// The limit and the status word are read from the kernel's parameters on the slow path only:
+// a limit held in a register cost the fp8 kernel (96 registers a thread) about 4% of its time.
 __device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_t parity,
-                                         int32_t* status, bool cluster_scope = false) {
+                                         const DecodeParams& p, bool cluster_scope = false) {
   // polled without a suspend hint: waking a suspended warp costs more than the issue
   // slots the polling takes from the other warps
   auto probe = [&]() {
@@ -129,9 +130,9 @@ __device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_
   while (true) {
     if (probe()) return true;
     if (*sh.abort) return false;
-    if (ptx::globaltimer() - t0 > sh.limit_ns) {
+    if (ptx::globaltimer() - t0 > p.wait_limit_ns) {
       *sh.abort = 1;
-      flag_status(status, MLA_ERR_TIMEOUT);
+      flag_status(p.status, MLA_ERR_TIMEOUT);
       return false;
     }
   }
@@ -172,10 +173,13 @@ struct PageCursor {
 // load, issued when a stage frees up, reads L2 rather than HBM.
 // An fp8 cache lands as e4m3 bytes (18 KB, unswizzled) in the back half of the stage, for
 // the converter warps to expand into the bf16 layout the MMAs read.
-template <bool kFp8, bool kB128>
-__device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensorMap* tm_kc,
-                         const CUtensorMap* tm_kpe, const CUtensorMap* tm_qpe,
-                         const CUtensorMap* tm_sc, int worker, int rank) {
+// kHook: the testing hook (mla_decode_opts.withhold_page) is compiled into a loop of its own,
+// taken by worker 0 only when the hook is set: inside the common loop its test cost the fp8
+// kernel about 4% of its time.
+template <bool kFp8, bool kB128, bool kHook>
+__device__ void producer_loop(const Shared& sh, const DecodeParams& p, const CUtensorMap* tm_kc,
+                              const CUtensorMap* tm_kpe, const CUtensorMap* tm_qpe,
+                              const CUtensorMap* tm_sc, int worker, int rank) {
   constexpr int kRowBytes = kB128 ? kB128RowBytes : kD * (kFp8 ? 1 : 2);   // cache bytes per row
   const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
   const uint8_t* cache = reinterpret_cast<const uint8_t*>(p.cache);
@@ -197,7 +201,7 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
   for (int it = it0; it < it1; ++it) {
     const WorkItem item = p.items[it];
     const int g = item.group, b = g / p.q_len;
-    if (!wait_bar(sh, sh.bar(B_QPEEMPTY), (q_iter & 1) ^ 1, p.status)) return;
+    if (!wait_bar(sh, sh.bar(B_QPEEMPTY), (q_iter & 1) ^ 1, p)) return;
     ptx::mbar_arrive_expect_tx(sh.bar(B_QPEFULL), kQPeBytes);
     ptx::tma_load_3d(sh.qpe(), tm_qpe, 32 * rank, 0, g, sh.bar(B_QPEFULL));
     ++q_iter;
@@ -216,19 +220,21 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
         if (rank == 0) flag_status(p.status, MLA_ERR_DEVICE_GUARD);
         page = 0;
       }
-      if (!wait_bar(sh, sh.bar(B_EMPTY0 + stage), (wrap & 1) ^ 1, p.status)) return;
+      if (!wait_bar(sh, sh.bar(B_EMPTY0 + stage), (wrap & 1) ^ 1, p)) return;
       const uint32_t full = sh.bar(B_FULL0 + stage);
-      // testing hook: this page of worker 0 is never loaded, so the wait for it runs out
-      if (worker == 0 && p.withhold_page > 0 && np_seq == (uint32_t)(p.withhold_page - 1)) {
-        prefetch_next();
-        ++np_seq;
-        if (++stage == kNS) {
-          stage = 0;
-          ++wrap;
+      if constexpr (kHook) {
+        // testing hook: this page of worker 0 is never loaded, so the wait for it runs out
+        if (np_seq == (uint32_t)(p.withhold_page - 1)) {
+          prefetch_next();
+          ++np_seq;
+          if (++stage == kNS) {
+            stage = 0;
+            ++wrap;
+          }
+          continue;
         }
-        continue;
+        ++np_seq;
       }
-      ++np_seq;
       if constexpr (kB128) {
         const uint32_t st = sh.stage(stage);
         ptx::mbar_arrive_expect_tx(full, 16384 + 64 * 16 + kKTilePE);
@@ -261,6 +267,16 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
   }
 }
 
+template <bool kFp8, bool kB128>
+__device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensorMap* tm_kc,
+                         const CUtensorMap* tm_kpe, const CUtensorMap* tm_qpe,
+                         const CUtensorMap* tm_sc, int worker, int rank) {
+  if (worker == 0 && p.withhold_page > 0)
+    producer_loop<kFp8, kB128, true>(sh, p, tm_kc, tm_kpe, tm_qpe, tm_sc, worker, rank);
+  else
+    producer_loop<kFp8, kB128, false>(sh, p, tm_kc, tm_kpe, tm_qpe, tm_sc, worker, rank);
+}
+
 // Score MMAs: S = Q_r K_r^T for every page, as soon as the page has landed (with an fp8
 // cache: has been converted) and the exchange warps have read the previous raw scores.
 template <bool kFp8>
@@ -272,11 +288,11 @@ __device__ void qk_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem
     const WorkItem item = p.items[it];
     for (int pg = item.page_begin; pg < item.page_end; ++pg) {
       if (pg == item.page_begin) {
-        if (!wait_bar(sh, sh.bar(B_QFULL), item_idx & 1, p.status)) return;
-        if (!wait_bar(sh, sh.bar(B_QPEFULL), item_idx & 1, p.status)) return;
+        if (!wait_bar(sh, sh.bar(B_QFULL), item_idx & 1, p)) return;
+        if (!wait_bar(sh, sh.bar(B_QPEFULL), item_idx & 1, p)) return;
       }
-      if (!wait_bar(sh, sh.bar((kFp8 ? B_CONV0 : B_FULL0) + stage), wrap & 1, p.status)) return;
-      if (!wait_bar(sh, sh.bar(B_SFREE), (n & 1) ^ 1, p.status)) return;
+      if (!wait_bar(sh, sh.bar((kFp8 ? B_CONV0 : B_FULL0) + stage), wrap & 1, p)) return;
+      if (!wait_bar(sh, sh.bar(B_SFREE), (n & 1) ^ 1, p)) return;
       ptx::tc_fence_after();
       const uint32_t st = sh.stage(stage);
 #pragma unroll
@@ -313,8 +329,8 @@ __device__ void pv_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem
     const WorkItem item = p.items[it];
     for (int pg = item.page_begin; pg < item.page_end; ++pg) {
       const bool first = (pg == item.page_begin);
-      if (!wait_bar(sh, sh.bar(B_PFULL0 + (n & 1)), (n >> 1) & 1, p.status)) return;
-      if (first && !wait_bar(sh, sh.bar(B_OFREE), (item_idx & 1) ^ 1, p.status)) return;
+      if (!wait_bar(sh, sh.bar(B_PFULL0 + (n & 1)), (n >> 1) & 1, p)) return;
+      if (first && !wait_bar(sh, sh.bar(B_OFREE), (item_idx & 1) ^ 1, p)) return;
       ptx::tc_fence_after();
       const uint32_t sb = sh.stage(stage);
 #pragma unroll
@@ -386,7 +402,7 @@ __device__ void send_warps(const Shared& sh, const DecodeParams& p, uint32_t tme
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(sh.bar(B_QFULL));
     }
-    if (!wait_bar(sh, sh.bar(B_SFULL), n & 1, p.status)) return;
+    if (!wait_bar(sh, sh.bar(B_SFULL), n & 1, p)) return;
     ptx::tc_fence_after();
     uint32_t r[64];
     ptx::tmem_ld32(t_row + kColS, *reinterpret_cast<uint32_t(*)[32]>(r));
@@ -400,8 +416,8 @@ __device__ void send_warps(const Shared& sh, const DecodeParams& p, uint32_t tme
       ptx::mbar_arrive(sh.bar(B_SFREE));
       // staging buffer j: our softmax has read page n - kXB from it, and the peer has read
       // its receive buffer j (so the copy of page n - kXB out of staging j has landed)
-      ok = wait_bar(sh, sh.bar(B_STGFREE0 + j), xpar ^ 1, p.status) &&
-                   wait_bar(sh, sh.bar(B_XEMPTY0 + j), xpar ^ 1, p.status, true)
+      ok = wait_bar(sh, sh.bar(B_STGFREE0 + j), xpar ^ 1, p) &&
+                   wait_bar(sh, sh.bar(B_XEMPTY0 + j), xpar ^ 1, p, true)
                ? 1 : 0;
     }
     if (!__shfl_sync(0xffffffffu, ok, 0)) return;
@@ -429,7 +445,7 @@ __device__ void send_warps(const Shared& sh, const DecodeParams& p, uint32_t tme
       // one 16 KB copy per page once all four quarters are staged: a bulk copy between
       // CTAs costs about the same fixed time whatever its size up to 16 KB
       if (quarter == 0) {
-        ok = wait_bar(sh, sh.bar(B_STGREADY0 + j), xpar, p.status) ? 1 : 0;
+        ok = wait_bar(sh, sh.bar(B_STGREADY0 + j), xpar, p) ? 1 : 0;
         if (ok) {
           ptx::bulk_s2s(peer_x + j * kXBytes, sh.stg(j), kXBytes, peer_xfull0 + 8 * j);
           ptx::bulk_commit();
@@ -474,9 +490,9 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
     // our own (staging n % kXB); P goes to TMEM buffer n & 1
     const uint32_t xj = n % kXB, xpar = (n / kXB) & 1;
     const uint32_t j = n & 1;
-    if (!wait_bar(sh, sh.bar(B_XFULL0 + xj), xpar, p.status, true)) return;
+    if (!wait_bar(sh, sh.bar(B_XFULL0 + xj), xpar, p, true)) return;
     if (warp == 6 && lane == 0) ptx::mbar_arrive_expect_tx(sh.bar(B_XFULL0 + xj), kXBytes);
-    if (!wait_bar(sh, sh.bar(B_STGREADY0 + xj), xpar, p.status)) return;
+    if (!wait_bar(sh, sh.bar(B_STGREADY0 + xj), xpar, p)) return;
     uint32_t xa[16], xb[16];                              // packed fp16 pairs, columns 32 half + 2i, +1
     {
       const uint8_t* xrow = sh.base + kOffX + xj * kXBytes + row * 128;
@@ -576,7 +592,7 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
     // first page, or a rescale).
     const bool early = (m_used != -INFINITY) && !(mine > m_used + 8.f);
     if (early) exps(m_used);
-    if (!wait_bar(sh, sh.bar(B_RED0 + 2 * quarter + j), (n >> 1) & 1, p.status)) return;
+    if (!wait_bar(sh, sh.bar(B_RED0 + 2 * quarter + j), (n >> 1) & 1, p)) return;
     const float mx = fmaxf(mine, slot[(half ^ 1) * 128 + row]);
     bool rescale = false;
     float alpha = 1.f;
@@ -602,12 +618,12 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
     l += psum;
     // P buffer n & 1 was last read by the product of page n-2; a rescale of O needs the
     // product of page n-1 done too
-    if (n >= 2 && !wait_bar(sh, sh.bar(B_PVDONE0 + j), ((n >> 1) & 1) ^ 1, p.status)) return;
+    if (n >= 2 && !wait_bar(sh, sh.bar(B_PVDONE0 + j), ((n >> 1) & 1) ^ 1, p)) return;
     // tcgen05 loads and stores are warp-collective: the warp rescales its 32 rows together
     // when any of them needs it (alpha is 1 for the others)
     const bool warp_rescale = __any_sync(0xffffffffu, rescale);
     if (warp_rescale && n >= 1 &&
-        !wait_bar(sh, sh.bar(B_PVDONE0 + ((n - 1) & 1)), ((n - 1) >> 1) & 1, p.status))
+        !wait_bar(sh, sh.bar(B_PVDONE0 + ((n - 1) & 1)), ((n - 1) >> 1) & 1, p))
       return;
     ptx::tc_fence_after();
     if (warp_rescale) {
@@ -637,10 +653,10 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
       lslot[half * 128 + row] = l;
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(sh.bar(B_LRED0 + quarter));
-      if (!wait_bar(sh, sh.bar(B_LRED0 + quarter), n_items & 1, p.status)) return;
+      if (!wait_bar(sh, sh.bar(B_LRED0 + quarter), n_items & 1, p)) return;
       ++n_items;
       const float l_row = l + lslot[(half ^ 1) * 128 + row];
-      if (!wait_bar(sh, sh.bar(B_PVDONE0 + j), (n >> 1) & 1, p.status)) return;
+      if (!wait_bar(sh, sh.bar(B_PVDONE0 + j), (n >> 1) & 1, p)) return;
       ptx::tc_fence_after();
       const float inv = (l_row > 0.f) ? p.out_scale / l_row : 0.f;
       const float lse_v = (l_row > 0.f) ? (m_used + log2f(l_row)) * kLn2 : -INFINITY;
@@ -750,7 +766,7 @@ __device__ void convert_warps(const Shared& sh, const DecodeParams& p, int worke
   int stage = 0;
   uint32_t wrap = 0, n = 0;
   while (cur.valid()) {
-    if (!wait_bar(sh, sh.bar(B_FULL0 + stage), wrap & 1, p.status)) return;
+    if (!wait_bar(sh, sh.bar(B_FULL0 + stage), wrap & 1, p)) return;
     uint8_t* st = sh.base + kOffStage + stage * kStageBytes;
     const uint8_t* land = st + (kB128 ? kB128Codes : kStageBytes / 2);
     uint4 in[9];
@@ -774,7 +790,7 @@ __device__ void convert_warps(const Shared& sh, const DecodeParams& p, int worke
     }
     const uint32_t all = __ballot_sync(0xffffffffu, dep != 0x7fc00001u);
     if (lane == 0 && all != 0x12345678u) ptx::mbar_arrive(sh.bar(B_CVREAD));
-    if (!wait_bar(sh, sh.bar(B_CVREAD), n & 1, p.status)) return;
+    if (!wait_bar(sh, sh.bar(B_CVREAD), n & 1, p)) return;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int i = t + 128 * k, j = i >> 9, r = (i >> 3) & 63, u = i & 7;
@@ -823,7 +839,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
   sh.base_u32 = aligned;
   sh.abort = reinterpret_cast<volatile int*>(sh.base + kOffBar + kBarArea - 16);
   sh.tmem_slot = reinterpret_cast<uint32_t*>(sh.base + kOffBar + kBarArea - 8);
-  sh.limit_ns = p.wait_limit_ns;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (int)ptx::cluster_ctarank();
   const int worker = blockIdx.x >> 1;
@@ -902,7 +917,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
   if (warp == 1) {
     if (lane == 0) {
       const uint64_t t0 = ptx::globaltimer();
-      while (!ptx::mbar_try_wait(sh.bar(B_TEARDOWN), 0) && ptx::globaltimer() - t0 < sh.limit_ns) {
+      while (!ptx::mbar_try_wait(sh.bar(B_TEARDOWN), 0) && ptx::globaltimer() - t0 < p.wait_limit_ns) {
       }
     }
     __syncwarp();
