@@ -15,14 +15,15 @@
 //      into TMEM (A = the latent part of Q_r held in TMEM, and the k_pe part from shared
 //      memory),
 //   3. send warps read S_r, round it to fp16 (columns past the last token as 0, values
-//      beyond the fp16 range saturated), stage it in shared memory and move it with one
-//      bulk copy per warp into one of the peer's two receive buffers (counted on the peer's
-//      mbarrier),
+//      beyond the fp16 range saturated), stage it in shared memory and, once the four warps
+//      have staged their rows, move it with one 16 KB bulk copy into one of the peer's two
+//      receive buffers (counted on the peer's mbarrier),
 //   4. softmax warps combine the peer's fp16 partial with their own staged fp16 partial
 //      (identical combined scores f16(S_0) + f16(S_1) in both CTAs; the fp16 rounding,
 //      relative 2^-11, is below the bf16 rounding of P), run the online softmax (one thread
 //      per head row, exp2, O rescaled lazily, only when the running maximum grows by more
-//      than 2^8) and write P (bf16) into one of two TMEM buffers,
+//      than 2^8) and write P (bf16; f16 with the per-tensor fp8 cache, whose MMAs all
+//      take f16 operands) into one of two TMEM buffers,
 //   5. O_r += P C_r (M = 128, N = 256, K = 64; A = P from TMEM, B = the staged page).
 // The query arrives pre-multiplied by softmax_scale * log2(e), so scores are already in
 // log2 units: the softmax forms each exponent as (f32) own half + (f32) peer half - m with
@@ -39,7 +40,7 @@
 // TMEM: O_r 256 columns, raw S 64, P 2 x 32, Q_r latent part 128.
 // Split partials are written bf16 [item][d_c / 8][128 heads][8], so the 32 threads of a
 // warp (32 consecutive heads) store one contiguous 512-byte run per instruction.
-// Every mbarrier wait is bounded (2 s): on timeout the kernel records MLA_ERR_TIMEOUT,
+// Every mbarrier wait is bounded (2 s unless the caller sets a limit): on timeout the kernel records MLA_ERR_TIMEOUT,
 // every role leaves its loop, TMEM is freed and the pair meets at a final cluster
 // barrier before exit.
 #include <cuda_fp16.h>
@@ -88,8 +89,17 @@ constexpr int kThreads = 480;                            // 15 warps (bf16 cache
 constexpr int kWarpConv0 = 15;                           // fp8 cache: 4 converter warps after them
 constexpr int kThreadsFp8 = kThreads + 4 * 32;
 constexpr int kSoftmaxWarps = 8;                         // two per head row (column halves)
-constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 64, false, false);
-constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, 256, false, true);
+// kF16: the operands of every MMA in f16 instead of bf16 (the per-tensor e4m3 cache, whose
+// codes convert to f16 exactly in one instruction per pair); query, cache and P then all
+// share that type.
+template <bool kF16>
+constexpr uint32_t idesc_qk() {
+  return kF16 ? ptx::idesc_f16_f32(128, 64, false, false) : ptx::idesc_bf16_f32(128, 64, false, false);
+}
+template <bool kF16>
+constexpr uint32_t idesc_pv() {
+  return kF16 ? ptx::idesc_f16_f32(128, 256, false, true) : ptx::idesc_bf16_f32(128, 256, false, true);
+}
 
 // mbarrier slots (8 bytes each) at kOffBar
 enum {
@@ -279,8 +289,9 @@ __device__ void producer(const Shared& sh, const DecodeParams& p, const CUtensor
 
 // Score MMAs: S = Q_r K_r^T for every page, as soon as the page has landed (with an fp8
 // cache: has been converted) and the exchange warps have read the previous raw scores.
-template <bool kFp8>
+template <bool kFp8, bool kF16>
 __device__ void qk_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker) {
+  constexpr uint32_t kIdescQK = idesc_qk<kF16>();
   const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
   int stage = 0;
   uint32_t wrap = 0, n = 0, item_idx = 0;
@@ -321,7 +332,9 @@ __device__ void qk_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem
 
 // Output MMAs: O_r += P C_r once P is in TMEM. The page's score MMA finished before its P
 // existed, so the stage is free once this product is done.
+template <bool kF16>
 __device__ void pv_issuer(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker) {
+  constexpr uint32_t kIdescPV = idesc_pv<kF16>();
   const int it0 = p.worker_off[worker], it1 = p.worker_off[worker + 1];
   int stage = 0;
   uint32_t n = 0, item_idx = 0;
@@ -461,6 +474,7 @@ __device__ void send_warps(const Shared& sh, const DecodeParams& p, uint32_t tme
 // Softmax warps: the pair's fp16 partial scores -> combined scores -> online softmax -> P
 // into TMEM buffer n & 1; the item's output at its last page. Thread (row, half) handles
 // columns [32 half, 32 half + 32) of each page and O columns [128 half, 128 half + 128).
+template <bool kF16>
 __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32_t tmem, int worker,
                                  int rank, int warp, int lane) {
   const int quarter = warp & 3;
@@ -581,8 +595,13 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
                                       ((e[8 * i + 4] + e[8 * i + 5]) + (e[8 * i + 6] + e[8 * i + 7]));
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const __nv_bfloat162 h2 = __floats2bfloat162_rn(e[2 * i], e[2 * i + 1]);
-        packed[i] = *reinterpret_cast<const uint32_t*>(&h2);
+        if constexpr (kF16) {
+          const __half2 h2 = __floats2half2_rn(e[2 * i], e[2 * i + 1]);
+          packed[i] = *reinterpret_cast<const uint32_t*>(&h2);
+        } else {
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(e[2 * i], e[2 * i + 1]);
+          packed[i] = *reinterpret_cast<const uint32_t*>(&h2);
+        }
       }
       psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
     };
@@ -710,16 +729,12 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
   }
 }
 
-// Two e4m3 values (low byte first) -> two bf16 (low half first), exactly: e4m3 -> f16 is
-// exact in hardware, and every e4m3 value (at most 4 significant bits, exponents 2^-9 ..
-// 2^8) is exact in f32 and in bf16.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t v16) {
-  uint32_t h2, out;
+// Two e4m3 values (low byte first) -> two f16 (low half first), exactly: every e4m3 value
+// (at most 4 significant bits, exponents 2^-9 .. 2^8) is an f16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
+  uint32_t h2;
   asm("{\n\t.reg .b16 x;\n\tcvt.u16.u32 x, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, x;\n\t}" : "=r"(h2) : "r"(v16));
-  asm("{\n\t.reg .f16 lo, hi;\n\t.reg .f32 flo, fhi;\n\tmov.b32 {lo, hi}, %1;\n\t"
-      "cvt.f32.f16 flo, lo;\n\tcvt.f32.f16 fhi, hi;\n\tcvt.rn.bf16x2.f32 %0, fhi, flo;\n\t}"
-      : "=r"(out) : "r"(h2));
-  return out;
+  return h2;
 }
 
 // Two e4m3 codes (low byte first) times a block scale -> two bf16, rounded to nearest
@@ -739,19 +754,20 @@ __device__ __forceinline__ void e4m3x16_to_bf16_scaled(const uint4& in, float s,
                   e4m3x2_to_bf16x2_scaled(in.w & 0xFFFFu, s), e4m3x2_to_bf16x2_scaled(in.w >> 16, s));
 }
 
-// 16 e4m3 bytes -> 16 bf16 as two 16-byte vectors (elements in order).
-__device__ __forceinline__ void e4m3x16_to_bf16(const uint4& in, uint4& lo, uint4& hi) {
-  lo = make_uint4(e4m3x2_to_bf16x2(in.x & 0xFFFFu), e4m3x2_to_bf16x2(in.x >> 16),
-                  e4m3x2_to_bf16x2(in.y & 0xFFFFu), e4m3x2_to_bf16x2(in.y >> 16));
-  hi = make_uint4(e4m3x2_to_bf16x2(in.z & 0xFFFFu), e4m3x2_to_bf16x2(in.z >> 16),
-                  e4m3x2_to_bf16x2(in.w & 0xFFFFu), e4m3x2_to_bf16x2(in.w >> 16));
+// 16 e4m3 bytes -> 16 f16 as two 16-byte vectors (elements in order).
+__device__ __forceinline__ void e4m3x16_to_f16(const uint4& in, uint4& lo, uint4& hi) {
+  lo = make_uint4(e4m3x2_to_f16x2(in.x & 0xFFFFu), e4m3x2_to_f16x2(in.x >> 16),
+                  e4m3x2_to_f16x2(in.y & 0xFFFFu), e4m3x2_to_f16x2(in.y >> 16));
+  hi = make_uint4(e4m3x2_to_f16x2(in.z & 0xFFFFu), e4m3x2_to_f16x2(in.z >> 16),
+                  e4m3x2_to_f16x2(in.w & 0xFFFFu), e4m3x2_to_f16x2(in.w >> 16));
 }
 
 // Converter warps (fp8 cache): each page's e4m3 slice (two 128-dim boxes and the 32-dim
-// rope box, unswizzled, in the back half of the stage) -> the bf16 slice in the layout the
-// MMAs read (four 64-dim SW128 chunks and the SW64 rope tile, the whole stage). The stored
-// codes are converted exactly; the cache's scale is folded into the query and the output.
-// The bf16 writes overlap the e4m3 bytes, so every converter reads its share first and the
+// rope box, unswizzled, in the back half of the stage) -> the 16-bit slice in the layout the
+// MMAs read (four 64-dim SW128 chunks and the SW64 rope tile, the whole stage). Per-tensor
+// codes become f16 exactly, one instruction per pair (the kernel's MMAs then run on f16
+// operands); the cache's scale is folded into the query and the output.
+// The 16-bit writes overlap the e4m3 bytes, so every converter reads its share first and the
 // four warps meet at a barrier before any writes. Thread t reads eight 16-byte units of the
 // c boxes (a warp covers 4 rows x 128 bytes, conflict-free) and one of the rope box.
 // Block-scaled cache (kB128): the 256 codes of each row are read with the row's two scales
@@ -799,7 +815,7 @@ __device__ void convert_warps(const Shared& sh, const DecodeParams& p, int worke
       const int cb = 2 * (u & 3);
       uint4 lo, hi;
       if constexpr (kB128) e4m3x16_to_bf16_scaled(in[k], scl[k], lo, hi);
-      else e4m3x16_to_bf16(in[k], lo, hi);
+      else e4m3x16_to_f16(in[k], lo, hi);
       *reinterpret_cast<uint4*>(row + ((cb ^ (r & 7)) * 16)) = lo;
       *reinterpret_cast<uint4*>(row + (((cb + 1) ^ (r & 7)) * 16)) = hi;
     }
@@ -809,7 +825,7 @@ __device__ void convert_warps(const Shared& sh, const DecodeParams& p, int worke
       const int r = t >> 1, cb = 2 * (t & 1);
       uint8_t* row = st + 4 * kKTileC + 64 * r;
       uint4 lo, hi;
-      e4m3x16_to_bf16(in[8], lo, hi);
+      e4m3x16_to_f16(in[8], lo, hi);
       *reinterpret_cast<uint4*>(row + ((cb ^ ((r >> 1) & 3)) * 16)) = lo;
       *reinterpret_cast<uint4*>(row + (((cb + 1) ^ ((r >> 1) & 3)) * 16)) = hi;
     }
@@ -831,6 +847,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
                      const __grid_constant__ CUtensorMap tm_kpe,
                      const __grid_constant__ CUtensorMap tm_qpe,
                      const __grid_constant__ CUtensorMap tm_sc, const DecodeParams p) {
+  // per-tensor e4m3 cache: f16 operands (the query arrives in f16 from the prologue)
+  constexpr bool kF16 = kFp8 && !kB128;
   extern __shared__ uint8_t smem_raw[];
   Shared sh;
   const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -898,15 +916,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kFp8 ? kThreadsFp8 :
   if (warp == 0) {
     if (lane == 0) producer<kFp8, kB128>(sh, p, &tm_kc, &tm_kpe, &tm_qpe, &tm_sc, worker, rank);
   } else if (warp == 1) {
-    if (lane == 0) qk_issuer<kFp8>(sh, p, tmem, worker);
+    if (lane == 0) qk_issuer<kFp8, kF16>(sh, p, tmem, worker);
   } else if (kFp8 && warp >= kWarpConv0) {
     convert_warps<kB128>(sh, p, worker, rank, warp, lane);
   } else if (warp <= 5) {
     send_warps(sh, p, tmem, worker, rank, warp, lane);
   } else if (warp <= 13) {
-    softmax_epilogue(sh, p, tmem, worker, rank, warp, lane);
+    softmax_epilogue<kF16>(sh, p, tmem, worker, rank, warp, lane);
   } else {
-    if (lane == 0) pv_issuer(sh, p, tmem, worker);
+    if (lane == 0) pv_issuer<kF16>(sh, p, tmem, worker);
   }
 
   // teardown: every role gets here, normally or after a bounded wait gave up

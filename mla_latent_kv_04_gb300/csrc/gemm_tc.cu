@@ -166,10 +166,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const RopeJob& q = gp.rope;
       if (q.d_r % 16 == 0)
         rope_body_bf16x8(q.q_pe, q.seq_lens, q.q_len, q.H, q.d_c, q.d_r, q.rt, q.qs, q.planar, q.q_lat,
-                         r / q.hblocks, r % q.hblocks, 32);
+                         r / q.hblocks, r % q.hblocks, 32, q.f16);
       else
         rope_body<bf16>(q.q_pe, q.seq_lens, q.q_len, q.H, q.d_c, q.d_r, q.rt, q.qs, q.planar, q.q_lat,
-                        r / q.hblocks, r % q.hblocks, 32);
+                        r / q.hblocks, r % q.hblocks, 32, q.f16);
     }
     ptx::griddep_wait();
     return;
@@ -351,15 +351,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------------------ epilogues
-struct EpiQLat {              // bf16(qs * v) at (group n, head z, latent dim m), row-major or planar
-  bf16* q;
+struct EpiQLat {              // bf16(qs * v) (f16 if f16) at (group n, head z, latent dim m),
+  bf16* q;                    // row-major or planar
   int H, D;
   float qs;
-  int planar;
+  int planar, f16;
   __device__ __forceinline__ void operator()(int z, int m, int n, float v) const {
     const long long i = planar ? (long long)n * H * D + ((long long)(m >> 3) * H + z) * 8 + (m & 7)
                                : ((long long)n * H + z) * D + m;
-    q[i] = __float2bfloat16_rn(qs * v);
+    q[i] = f16 ? __ushort_as_bfloat16(__half_as_ushort(__float2half_rn(qs * v)))
+               : __float2bfloat16_rn(qs * v);
   }
 };
 
@@ -791,9 +792,9 @@ cudaError_t launch_fold_tc(const void* W_UV, const void* W_O, int H, int d_c, in
 
 // q_lat[g][h][0:d_c] = q_nope[g][h][:] . W_UK_abs[h]  (per head, bf16 out).
 cudaError_t launch_query_absorb_tc(const void* q_nope, const void* W_UK_abs, int groups, int H,
-                                   int d_n, int d_c, int D, float q_scale, int planar, void* q_lat,
-                                   int32_t* status, const PlanParams* plan, const RopeJob* rope,
-                                   cudaStream_t s) {
+                                   int d_n, int d_c, int D, float q_scale, int planar, int f16,
+                                   void* q_lat, int32_t* status, const PlanParams* plan,
+                                   const RopeJob* rope, cudaStream_t s) {
   using namespace gemm;
   CUtensorMap A, Bm[4];
   // A = W_UK_abs[h] : dims {d_c (m), d_n (k), H (z)}
@@ -822,7 +823,7 @@ cudaError_t launch_query_absorb_tc(const void* q_nope, const void* W_UK_abs, int
   gp.rope_blocks = rope ? rope->groups * rope->hblocks : 0;
   if (rope) gp.rope = *rope;
   return dispatch(A, Bm[0], Bm[1], Bm[2], Bm[3], gp,
-                  EpiQLat{reinterpret_cast<bf16*>(q_lat), H, D, q_scale, planar}, s);
+                  EpiQLat{reinterpret_cast<bf16*>(q_lat), H, D, q_scale, planar, f16}, s);
 }
 
 // The append from hidden states in one launch: [c | k_raw] = h W_DKV_KR (h [T][d],

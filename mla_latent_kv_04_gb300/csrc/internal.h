@@ -133,10 +133,12 @@ cudaError_t launch_fold_tc(const void* W_UV, const void* W_O, int H, int d_c, in
 // status word) and the q_pe rotation, and the GEMM is the decode's first kernel; if null,
 // the GEMM follows the prep kernel (which did both) with programmatic serialization.
 struct RopeJob;
+// f16: the query is stored as f16 instead of bf16 (the tensor-core kernel on a per-tensor
+// e4m3 cache, whose MMAs take f16 operands).
 cudaError_t launch_query_absorb_tc(const void* q_nope, const void* W_UK_abs, int groups, int H,
-                                   int d_n, int d_c, int D, float q_scale, int planar, void* q_lat,
-                                   int32_t* status, const PlanParams* plan, const RopeJob* rope,
-                                   cudaStream_t s);
+                                   int d_n, int d_c, int D, float q_scale, int planar, int f16,
+                                   void* q_lat, int32_t* status, const PlanParams* plan,
+                                   const RopeJob* rope, cudaStream_t s);
 // Append from h in one launch: projection, RoPE, encoding and page scatter (bf16 h and W).
 cudaError_t launch_append_tc(mla_dtype cache_dtype, const void* h, const void* W, int T, int d,
                              int d_c, int d_r, const int32_t* req_ids, const int32_t* positions,
@@ -148,7 +150,7 @@ cudaError_t launch_append_tc(mla_dtype cache_dtype, const void* h, const void* W
 // query absorption GEMM (which planned) with programmatic serialization.
 cudaError_t launch_prep(const PlanParams& pp, const void* q_pe, const int32_t* seq_lens, int q_len,
                         int H, int d_c, int d_r, const RopeTable& rt, float q_scale, int planar,
-                        void* q_lat, cudaStream_t s);
+                        int f16, void* q_lat, cudaStream_t s);
 cudaError_t launch_q_rope(mla_dtype act, const void* q_pe, const int32_t* seq_lens, int batch,
                           int q_len, int H, int d_c, int d_r, const RopeTable& rt, float q_scale,
                           int planar, void* q_lat, cudaStream_t s);

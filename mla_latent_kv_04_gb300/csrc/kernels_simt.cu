@@ -283,7 +283,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) prep_kernel(PlanParams pp, const T* __restrict__ q_pe,
                                                    const int32_t* seq_lens, int q_len, int H, int d_c,
                                                    int d_r, RopeTable rt, float qs, int planar,
-                                                   T* __restrict__ q_lat, int hblocks) {
+                                                   T* __restrict__ q_lat, int hblocks, int f16) {
   extern __shared__ int sm[];
   const int plan = pp.workers > 0 ? 1 : 0;
   if (plan && blockIdx.x == 0) {
@@ -295,7 +295,8 @@ __global__ void __launch_bounds__(256) prep_kernel(PlanParams pp, const T* __res
     plan_body(pp, sm, false);
   } else {
     const int b = blockIdx.x - plan;
-    rope_body<T>(q_pe, seq_lens, q_len, H, d_c, d_r, rt, qs, planar, q_lat, b / hblocks, b % hblocks);
+    rope_body<T>(q_pe, seq_lens, q_len, H, d_c, d_r, rt, qs, planar, q_lat, b / hblocks, b % hblocks, 16,
+                 f16);
   }
   ptx::griddep_wait();
 }
@@ -642,7 +643,7 @@ static cudaError_t query_prologue_t(const void* q_nope, const void* q_pe, const 
 
 cudaError_t launch_prep(const PlanParams& pp, const void* q_pe, const int32_t* seq_lens, int q_len,
                         int H, int d_c, int d_r, const RopeTable& rt, float q_scale, int planar,
-                        void* q_lat, cudaStream_t s) {
+                        int f16, void* q_lat, cudaStream_t s) {
   const int groups = pp.batch * q_len;
   const int hblocks = (H + 15) / 16;
   const bool plan = pp.workers > 0;
@@ -664,7 +665,7 @@ cudaError_t launch_prep(const PlanParams& pp, const void* q_pe, const int32_t* s
   cfg.numAttrs = plan ? 0 : 1;
   cudaError_t e = cudaLaunchKernelEx(&cfg, kern, pp, reinterpret_cast<const bf16*>(q_pe), seq_lens, q_len,
                                      H, d_c, d_r, rt, q_scale, planar, reinterpret_cast<bf16*>(q_lat),
-                                     hblocks);
+                                     hblocks, f16);
   note_launch();
   return e;
 }

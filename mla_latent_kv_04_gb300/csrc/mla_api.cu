@@ -330,6 +330,9 @@ mla_status mla_decode_ex(const mla_config* cfg, const void* q_nope, const void* 
     const float q_scale = tc ? softmax_scale_of(cfg) * kLog2e * code_scale : 1.f;
     // ... and in the planar layout (see internal.h)
     const int planar = tc ? 1 : 0;
+    // the tensor-core kernel on a per-tensor e4m3 cache takes an f16 query (its codes convert
+    // to f16 exactly, and every MMA's two operands share one type)
+    const int f16 = (tc && cfg->cache_dtype == MLA_FP8_E4M3) ? 1 : 0;
     // one launch: the query absorption GEMM with the planner (which clears the status word)
     // and the q_pe rotation as extra blocks. A plan too large for the GEMM block's shared
     // memory runs in the prep kernel, which then goes first.
@@ -345,17 +348,18 @@ mla_status mla_decode_ex(const mla_config* cfg, const void* q_nope, const void* 
       rj.d_r = cfg->d_rope;
       rj.planar = planar;
       rj.hblocks = (cfg->num_heads + 31) / 32;
+      rj.f16 = f16;
       rj.qs = q_scale;
       rj.rt = rt;
       e = launch_query_absorb_tc(q_nope, W_UK_abs, batch * q_len, cfg->num_heads, cfg->d_nope,
-                                 cfg->d_latent, D, q_scale, planar, ws + w.q_lat, pp.status, &pp,
+                                 cfg->d_latent, D, q_scale, planar, f16, ws + w.q_lat, pp.status, &pp,
                                  &rj, s);
     } else {
       e = launch_prep(pp, q_pe, seq_lens, q_len, cfg->num_heads, cfg->d_latent, cfg->d_rope, rt,
-                      q_scale, planar, ws + w.q_lat, s);
+                      q_scale, planar, f16, ws + w.q_lat, s);
       if (e == cudaSuccess)
         e = launch_query_absorb_tc(q_nope, W_UK_abs, batch * q_len, cfg->num_heads, cfg->d_nope,
-                                   cfg->d_latent, D, q_scale, planar, ws + w.q_lat, pp.status,
+                                   cfg->d_latent, D, q_scale, planar, f16, ws + w.q_lat, pp.status,
                                    nullptr, nullptr, s);
     }
   } else {

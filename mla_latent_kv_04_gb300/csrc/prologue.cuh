@@ -171,11 +171,21 @@ __device__ inline void plan_body(const PlanParams& p, int* sm, bool reset_status
 
 // One block per (group, hpb heads): the d_r/2 rotation angles of the group's position are
 // computed once into shared memory, then applied to those heads' q_pe.
+// A rotated query value as stored in q_lat: the activation type, or (f16 set, bf16
+// activations) the bits of an f16.
+template <typename T>
+__device__ __forceinline__ T q_out(float v, int f16) {
+  if constexpr (sizeof(T) == 2) {
+    if (f16) return __ushort_as_bfloat16(__half_as_ushort(__float2half_rn(v)));
+  }
+  return from_f32<T>(v);
+}
+
 template <typename T>
 __device__ __forceinline__ void rope_body(const T* __restrict__ q_pe, const int32_t* seq_lens,
                                           int q_len, int H, int d_c, int d_r, const RopeTable& rt,
                                           float qs, int planar, T* __restrict__ q_lat, int g, int hy,
-                                          int hpb = 16) {
+                                          int hpb = 16, int f16 = 0) {
   __shared__ float cs[kMaxRopePairs], sn[kMaxRopePairs];
   const int h0 = hy * hpb, h1 = min(H, h0 + hpb);
   const int b = g / q_len, t = g % q_len;
@@ -201,8 +211,8 @@ __device__ __forceinline__ void rope_body(const T* __restrict__ q_pe, const int3
     }
     const long long o = planar ? (long long)g * H * D + (long long)d_c * H + (long long)h * d_r + 2 * k
                                : gh * D + d_c + 2 * k;
-    q_lat[o] = from_f32<T>(y0);
-    q_lat[o + 1] = from_f32<T>(y1);
+    q_lat[o] = q_out<T>(y0, f16);
+    q_lat[o + 1] = q_out<T>(y1, f16);
   }
 }
 
@@ -213,7 +223,7 @@ __device__ __forceinline__ void rope_body(const T* __restrict__ q_pe, const int3
 __device__ __forceinline__ void rope_body_bf16x8(const bf16* __restrict__ q_pe, const int32_t* seq_lens,
                                                  int q_len, int H, int d_c, int d_r, const RopeTable& rt,
                                                  float qs, int planar, bf16* __restrict__ q_lat, int g,
-                                                 int hy, int hpb) {
+                                                 int hy, int hpb, int f16) {
   __shared__ float cs[kMaxRopePairs], sn[kMaxRopePairs];
   const int h0 = hy * hpb, h1 = min(H, h0 + hpb);
   const int chunks = d_r / 16;
@@ -254,8 +264,13 @@ __device__ __forceinline__ void rope_body_bf16x8(const bf16* __restrict__ q_pe, 
         y0 = (x.x * cs[k] - x.y * sn[k]) * qs;
         y1 = (x.x * sn[k] + x.y * cs[k]) * qs;
       }
-      const __nv_bfloat162 yb = __floats2bfloat162_rn(y0, y1);
-      out[j] = *reinterpret_cast<const uint32_t*>(&yb);
+      if (f16) {
+        const __half2 yh = __floats2half2_rn(y0, y1);
+        out[j] = *reinterpret_cast<const uint32_t*>(&yh);
+      } else {
+        const __nv_bfloat162 yb = __floats2bfloat162_rn(y0, y1);
+        out[j] = *reinterpret_cast<const uint32_t*>(&yb);
+      }
     }
     const long long gh = (long long)g * H + h;
     const long long o = planar ? (long long)g * H * D + (long long)d_c * H + (long long)h * d_r + 16 * c
@@ -273,6 +288,7 @@ struct RopeJob {
   const int32_t* seq_lens;
   bf16* q_lat;
   int groups, q_len, H, d_c, d_r, planar, hblocks;
+  int f16;     // store the rotated query as f16 (the tensor-core kernel on an e4m3 cache)
   float qs;
   RopeTable rt;
 };
