@@ -866,7 +866,9 @@ static cudaError_t output_proj_t(const void* o_lat, const void* W_comb, int rows
                                  void* out, float* acc, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(acc, 0, (size_t)rows * N * sizeof(float), s);
   if (e != cudaSuccess) return e;
-  const int splits = max(1, min(64, K / 1024));
+  // a split per 128 of K (at most 64): with a handful of rows the grid is otherwise a few
+  // blocks each walking all of K
+  const int splits = max(1, min(64, K / 128));
   AtomicAddEpi epi{acc, (long long)N};
   e = simt_gemm(reinterpret_cast<const T*>(o_lat), (long long)K, 0LL,
                 reinterpret_cast<const T*>(W_comb), (long long)N, 0LL, rows, N, K, 1, splits, epi, s);
