@@ -132,6 +132,19 @@ __device__ __forceinline__ void k_loop(const CUtensorMap* tmA, const CUtensorMap
   __syncwarp();
 }
 
+// L2 prefetch of the weight (A) tiles of the first `ahead` K blocks, issued before the wait
+// for the kernel before this one: the weights are not what that kernel writes in a step, and
+// a prefetch only warms L2 (the loads after the wait read whatever is current), so the
+// weight stream starts while that kernel ends.
+__device__ __forceinline__ void prefetch_a(const CUtensorMap* tmA, int m0, int z, int kb0, int kb1,
+                                           int ahead) {
+  const uint64_t pol = ptx::l2_policy_evict_first();
+  for (int kb = kb0; kb < kb1 && kb < kb0 + ahead; ++kb) {
+    ptx::tma_prefetch_3d_hint(tmA, m0, kb * kBK, z, pol);
+    ptx::tma_prefetch_3d_hint(tmA, m0 + 64, kb * kBK, z, pol);
+  }
+}
+
 // D^T[z][m][n] = sum_k A[z][k][m] * B[z][n][k]; A is the MN-major weight, B the K-major
 // token matrix. Work unit = (z, m tile, n tile, k split), one per CTA.
 template <int BN, int NS, class Epi>
@@ -207,6 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (gp.wait_first && warp == 0 && lane == 0) prefetch_a(&tmA, m0, z, kb0, kb1, C::kStages);
   if (gp.wait_first) ptx::griddep_wait();   // the inputs (the token operand) are the previous kernels'
   bool ok = true;
 
@@ -302,6 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   // launched with programmatic serialization: the token operand may be the previous
   // kernel's output (and the weight a still earlier one's)
+  if (t == 0) prefetch_a(A, ma, 0, kb0, kb1, C::kStages);
   ptx::griddep_wait();
   const int per = (BN + KS - 1) / KS;
   const int c0 = rank * per, c1 = min(BN, c0 + per);

@@ -127,6 +127,12 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
       : "memory");
 }
+// Prefetch of one tensor-map tile into L2 (no shared memory, no barrier; a hint only).
+__device__ __forceinline__ void tma_prefetch_3d_hint(const CUtensorMap* map, int x, int y, int z,
+                                                     uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.L2::cache_hint [%0, {%1, %2, %3}], %4;"
+               ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "l"(policy) : "memory");
+}
 // bulk_prefetch_l2 with an L2 cache policy.
 __device__ __forceinline__ void bulk_prefetch_l2_hint(const void* src, uint32_t bytes, uint64_t policy) {
   asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;"
