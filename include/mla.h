@@ -284,7 +284,8 @@ const char* mla_status_string(mla_status status);
 /* Text of the last CUDA error seen by this thread's calls ("" if none). */
 const char* mla_last_error(void);
 
-/* Library ABI version (major * 100 + minor). */
+/* Library ABI version (major * 100 + minor). 1.02: mla_append_cache needs no workspace
+ * (its size is 0). */
 int mla_version(void);
 
 /* Number of CUDA kernels the library has launched in this process so far (all

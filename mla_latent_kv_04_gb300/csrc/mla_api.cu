@@ -151,7 +151,7 @@ void set_last_error(const std::string& what) { g_last_error = what; }
 
 extern "C" {
 
-int mla_version(void) { return 101; }
+int mla_version(void) { return 102; }
 
 uint64_t mla_kernel_launches(void) { return (uint64_t)mla::g_launches.load(); }
 
