@@ -298,12 +298,12 @@ NCU_TRAFFIC = {
     "attn": {"bytes": 155805440 + 2639104, "workload": "v2_b32_s4096",
              "source": "mla_latent_kv_04_gb300/csrc/decode_tc.cu",
              "sha256": "2fad967b9841a920d0d141e9c1994683135ad4b418469ccb3e1c4b71c177cefe"},
-    "oproj": {"bytes": 675327744 + 64768, "workload": "v2_b32_s4096",
+    "oproj": {"bytes": 675331072 + 132096, "workload": "v2_b32_s4096",
               "source": "mla_latent_kv_04_gb300/csrc/gemm_tc.cu",
-              "sha256": "9c42058674bb80998a87c1c3f76fd6c1a10584746d4e624fac20286486970a3d"},
-    "append": {"bytes": 6257920 + 0, "workload": "v2_b32_s4096",
+              "sha256": "af7fe9e3019323f5dc975359741254a343fdd133e51549604dd35c04e563295d"},
+    "append": {"bytes": 6258432 + 0, "workload": "v2_b32_s4096",
                "source": "mla_latent_kv_04_gb300/csrc/gemm_tc.cu",
-               "sha256": "9c42058674bb80998a87c1c3f76fd6c1a10584746d4e624fac20286486970a3d"},
+               "sha256": "af7fe9e3019323f5dc975359741254a343fdd133e51549604dd35c04e563295d"},
 }
 
 
