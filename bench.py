@@ -491,7 +491,7 @@ def main():
     for _ in range(args.warmup):
         step(st, inp)
     torch.cuda.synchronize()
-    # The step as one CUDA graph: the library's calls captured once (their launches, memsets
+    # The step as one CUDA graph: the library's calls captured once (their launches
     # and programmatic launch dependencies), then replayed; this removes the host launch
     # gaps between the step's kernels. The library counts launches when they are issued, so
     # the kernels of one step are counted at capture.
@@ -662,7 +662,7 @@ def main():
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "decode_workers": args.workers if args.workers > 0 else "library default",
                    "launch": "the step captured once as a CUDA graph and replayed (its kernels, "
-                             "memsets and programmatic launch dependencies); ms_per_step_stream "
+                             "and programmatic launch dependencies); ms_per_step_stream "
                              "is the same step issued call by call",
                    "l2": f"inputs larger than L2: the step streams the {cache_mb:.0f} MB cache "
                          f"and the {wcomb_mb:.0f} MB folded W_comb"},
