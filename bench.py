@@ -661,7 +661,7 @@ def main():
                    "cache_dtype": wl.cache, "page_size": wl.dims.page_size,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "decode_workers": args.workers if args.workers > 0 else "library default",
-                   "launch": "the step captured once as a CUDA graph and replayed (its kernels, "
+                   "launch": "the step captured once as a CUDA graph and replayed (its kernels "
                              "and programmatic launch dependencies); ms_per_step_stream "
                              "is the same step issued call by call",
                    "l2": f"inputs larger than L2: the step streams the {cache_mb:.0f} MB cache "
