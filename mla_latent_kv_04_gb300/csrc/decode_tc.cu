@@ -729,12 +729,13 @@ __device__ void softmax_epilogue(const Shared& sh, const DecodeParams& p, uint32
   }
 }
 
-// Two e4m3 values (low byte first) -> two f16 (low half first), exactly: every e4m3 value
-// (at most 4 significant bits, exponents 2^-9 .. 2^8) is an f16 value.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
-  uint32_t h2;
-  asm("{\n\t.reg .b16 x;\n\tcvt.u16.u32 x, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, x;\n\t}" : "=r"(h2) : "r"(v16));
-  return h2;
+// Four e4m3 values (low byte first) -> four f16 as two f16x2 words (low pair first), exactly:
+// every e4m3 value (at most 4 significant bits, exponents 2^-9 .. 2^8) is an f16 value. The
+// word's two 16-bit halves go to the two conversions without shifts or masks.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi) : "r"(w));
 }
 
 // Two e4m3 codes (low byte first) times a block scale -> two bf16, rounded to nearest
@@ -756,10 +757,10 @@ __device__ __forceinline__ void e4m3x16_to_bf16_scaled(const uint4& in, float s,
 
 // 16 e4m3 bytes -> 16 f16 as two 16-byte vectors (elements in order).
 __device__ __forceinline__ void e4m3x16_to_f16(const uint4& in, uint4& lo, uint4& hi) {
-  lo = make_uint4(e4m3x2_to_f16x2(in.x & 0xFFFFu), e4m3x2_to_f16x2(in.x >> 16),
-                  e4m3x2_to_f16x2(in.y & 0xFFFFu), e4m3x2_to_f16x2(in.y >> 16));
-  hi = make_uint4(e4m3x2_to_f16x2(in.z & 0xFFFFu), e4m3x2_to_f16x2(in.z >> 16),
-                  e4m3x2_to_f16x2(in.w & 0xFFFFu), e4m3x2_to_f16x2(in.w >> 16));
+  e4m3x4_to_f16x4(in.x, lo.x, lo.y);
+  e4m3x4_to_f16x4(in.y, lo.z, lo.w);
+  e4m3x4_to_f16x4(in.z, hi.x, hi.y);
+  e4m3x4_to_f16x4(in.w, hi.z, hi.w);
 }
 
 // Converter warps (fp8 cache): each page's e4m3 slice (two 128-dim boxes and the 32-dim
