@@ -738,21 +738,29 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
       : "=r"(lo), "=r"(hi) : "r"(w));
 }
 
-// Two e4m3 codes (low byte first) times a block scale -> two bf16, rounded to nearest
-// even: the codes convert exactly to fp16 and then fp32, and only the product is rounded.
-__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2_scaled(uint32_t v16, float s) {
-  uint32_t h2;
-  asm("{\n\t.reg .b16 x;\n\tcvt.u16.u32 x, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, x;\n\t}" : "=r"(h2) : "r"(v16));
-  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-  const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * s, f.y * s);
-  return *reinterpret_cast<const uint32_t*>(&b);
+// Four e4m3 codes (low byte first) times a block scale -> four bf16 as two bf16x2 words, each
+// rounded to nearest even once: the codes convert exactly to f16 and then f32, the products
+// are IEEE f32 multiplies (two at a time), and only their bf16 rounding is inexact.
+__device__ __forceinline__ void e4m3x4_to_bf16x4_scaled(uint32_t w, uint64_t s2, uint32_t& lo,
+                                                        uint32_t& hi) {
+  uint32_t h0, h1;
+  e4m3x4_to_f16x4(w, h0, h1);
+  asm("{\n\t.reg .b16 a, b, c, d;\n\t.reg .f32 fa, fb, fc, fd;\n\t.reg .b64 p, q;\n\t"
+      "mov.b32 {a, b}, %2;\n\tmov.b32 {c, d}, %3;\n\t"
+      "cvt.f32.f16 fa, a;\n\tcvt.f32.f16 fb, b;\n\tcvt.f32.f16 fc, c;\n\tcvt.f32.f16 fd, d;\n\t"
+      "mov.b64 p, {fa, fb};\n\tmov.b64 q, {fc, fd};\n\t"
+      "mul.rn.f32x2 p, p, %4;\n\tmul.rn.f32x2 q, q, %4;\n\t"
+      "mov.b64 {fa, fb}, p;\n\tmov.b64 {fc, fd}, q;\n\t"
+      "cvt.rn.bf16x2.f32 %0, fb, fa;\n\tcvt.rn.bf16x2.f32 %1, fd, fc;\n\t}"
+      : "=r"(lo), "=r"(hi) : "r"(h0), "r"(h1), "l"(s2));
 }
 
 __device__ __forceinline__ void e4m3x16_to_bf16_scaled(const uint4& in, float s, uint4& lo, uint4& hi) {
-  lo = make_uint4(e4m3x2_to_bf16x2_scaled(in.x & 0xFFFFu, s), e4m3x2_to_bf16x2_scaled(in.x >> 16, s),
-                  e4m3x2_to_bf16x2_scaled(in.y & 0xFFFFu, s), e4m3x2_to_bf16x2_scaled(in.y >> 16, s));
-  hi = make_uint4(e4m3x2_to_bf16x2_scaled(in.z & 0xFFFFu, s), e4m3x2_to_bf16x2_scaled(in.z >> 16, s),
-                  e4m3x2_to_bf16x2_scaled(in.w & 0xFFFFu, s), e4m3x2_to_bf16x2_scaled(in.w >> 16, s));
+  const uint64_t s2 = ((uint64_t)__float_as_uint(s) << 32) | __float_as_uint(s);
+  e4m3x4_to_bf16x4_scaled(in.x, s2, lo.x, lo.y);
+  e4m3x4_to_bf16x4_scaled(in.y, s2, lo.z, lo.w);
+  e4m3x4_to_bf16x4_scaled(in.z, s2, hi.x, hi.y);
+  e4m3x4_to_bf16x4_scaled(in.w, s2, hi.z, hi.w);
 }
 
 // 16 e4m3 bytes -> 16 f16 as two 16-byte vectors (elements in order).
