@@ -589,14 +589,20 @@ static cudaError_t dispatch(const CUtensorMap& A, const CUtensorMap& Bmap32, con
 // clusters above 8 CTAs are a non-portable size that the kernel must opt in to.
 template <int BN, int NS, class Fin>
 static bool cluster16_fits(int need) {
-  static int fits = -1;        // per instantiation: number of co-resident clusters of 16
-  if (fits < 0) {
+  // per instantiation and device: number of co-resident clusters of 16 (-1: not asked yet)
+  static int fits[64] = {-1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1,
+                         -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1,
+                         -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1,
+                         -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1, -1};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (fits[dev] < 0) {
     using C = Cfg<BN, NS>;
     auto kern = tc_gemm_cluster_kernel<BN, NS, Fin>;
-    fits = 0;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) ==
-            cudaSuccess &&
-        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+    int n = 0;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(16, 1, 1);
       cfg.blockDim = dim3(kThreads, 1, 1);
@@ -608,12 +614,15 @@ static bool cluster16_fits(int need) {
       attr.val.clusterDim.z = 1;
       cfg.attrs = &attr;
       cfg.numAttrs = 1;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess) fits = n;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
     }
-    cudaGetLastError();        // a refused query leaves no error behind
+    if (e != cudaSuccess) {
+      n = 0;
+      cudaGetLastError();      // the refusal of our own query: leave no error behind
+    }
+    fits[dev] = n;
   }
-  return fits >= need;
+  return fits[dev] >= need;
 }
 
 template <int BN, int NS, class Fin>
